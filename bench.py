@@ -1,0 +1,532 @@
+#!/usr/bin/env python3
+"""Benchmark of the gated-DeltaNet decode step (one JSON line on stdout).
+
+A step is one dn_step call: one layer advances every sequence of its batch by
+one token (in_proj GEMV, conv + SiLU with the ring, L2 norms, gated delta
+rule, readout, gated RMSNorm, out_proj GEMV).  The headline workload is the
+35B-shape layer (hidden 2048, 16 q/k heads and 32 value heads of 128, conv
+kernel 4, int8 projections 2048 -> 12288 and 4096 -> 2048) at batch 64 with
+random initial state; the batch-1 workload of the same layer is measured in
+the same run and reported under "batch1".
+
+Timed regions rotate over --layers independent layer objects (distinct
+weights and states), so the working set of consecutive steps (about 300 MB
+per layer-step at batch 64) is larger than the 129 MB L2: nothing of a step
+is served from L2 by the previous step of the same layer.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (torchrun) every rank runs independent replicas of the same
+workload (the sequences of a batch are independent; nothing is exchanged);
+`value` counts the layer-steps of all ranks divided by the slowest rank's
+time.  --impl reference times the CPU oracle (float64 numpy) on a bounded
+sample of the same workload, on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from gated_deltanet_hybrid_gb300.inputs import (SHAPE_35B, WORKLOADS, DNConfig,  # noqa: E402
+                                                WorkloadStream, gates_from_ab, make_weights)
+
+METRIC = "DeltaNet layer-steps/s and achieved HBM GB/s (% of roofline) at batch 1 and 64"
+UNIT = "layer-steps/s"
+KERNELS = ("in_proj_gemv", "dn_core", "out_proj_gemv")
+
+
+# --------------------------------------------------------------------- bytes
+def step_bytes(cfg: DNConfig, B: int) -> int:
+    """Algorithmic HBM bytes of one layer-step: weights once, plus per
+    sequence the state read and written, the ring's conv_k-1 slots read and
+    one slot written, x, out and the two gates.  Scratch is not counted."""
+    shared = (cfg.in_rows * cfg.hidden + cfg.in_rows * 4 + cfg.hidden * cfg.v_dim + cfg.hidden * 4
+              + cfg.conv_ch * cfg.conv_k * 4 + cfg.dv * 4)
+    per_seq = (2 * cfg.n_v_heads * cfg.dk * cfg.dv * 4 + (cfg.conv_k - 1) * cfg.conv_ch * 4
+               + cfg.conv_ch * 4 + 2 * cfg.hidden * 4 + 2 * cfg.n_v_heads * 4)
+    return shared + B * per_seq
+
+
+def kernel_bytes(cfg: DNConfig, B: int) -> dict[str, int]:
+    """Algorithmic bytes of each kernel of the step (its unique inputs and
+    outputs, scratch included, since it is that kernel's real traffic)."""
+    k1 = cfg.in_rows * cfg.hidden + cfg.in_rows * 4 + B * (cfg.hidden + cfg.in_rows) * 4
+    core_seq = (2 * cfg.n_v_heads * cfg.dk * cfg.dv * 4 + (cfg.conv_k - 1) * cfg.conv_ch * 4
+                + cfg.conv_ch * 4 + cfg.in_rows * 4 + cfg.v_dim * 4 + 2 * cfg.n_v_heads * 4)
+    k2 = B * core_seq + cfg.conv_ch * cfg.conv_k * 4 + cfg.dv * 4
+    k3 = cfg.hidden * cfg.v_dim + cfg.hidden * 4 + B * (cfg.v_dim + cfg.hidden) * 4
+    return {"in_proj_gemv": k1, "dn_core": k2, "out_proj_gemv": k3}
+
+
+def load_peaks() -> tuple[float, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gated_deltanet_hybrid_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str) -> float | None:
+    """DRAM bytes per launch from the committed ncu summary of this kernel
+    and workload, if it was taken from the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith(("- source_hash", "- dram_bytes_per_launch")):
+                k, v = line.strip()[2:].split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_hash") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# --------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons; each sample is
+    stamped on arrival so that only those inside the timed region count."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_uuid: str | None):
+        self.uuid = device_uuid
+        self.proc = None
+        self.rows: list[tuple[float, list[str]]] = []
+
+    def _reader(self):
+        for ln in self.proc.stdout:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) >= 9:
+                self.rows.append((time.time(), parts))
+
+    def __enter__(self):
+        import threading
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._reader, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self, t_start: float, t_end: float) -> dict:
+        inside = [r for t, r in self.rows if t_start <= t <= t_end + 0.05]
+        where = "timed region"
+        if not inside:  # region shorter than one sampling period: nearest samples
+            inside = [r for t, r in sorted(self.rows, key=lambda tr: abs(tr[0] - t_end))[:3]]
+            where = "nearest to the timed region"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in inside if num(r[1]) is not None]
+        smax = [num(r[2]) for r in inside if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(inside), "samples_from": where,
+                "power_w_max": max((num(r[3]) or 0.0) for r in inside)}
+
+
+# --------------------------------------------------------------------- GPU arm
+def setup_layers(cfg: DNConfig, B: int, n_layers: int, init_std: float, seed: int, torch, abi):
+    """n_layers layer objects with seeded weights; the initial state is drawn
+    on the device (normal, std init_std) and pushed through dn_set_state."""
+    layers = []
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    for l in range(n_layers):
+        w = make_weights(cfg, np.random.Generator(np.random.PCG64(seed * 1000 + l)))
+        h = abi.dn_create(cfg, w, B)
+        if init_std > 0:
+            S = torch.randn((B, cfg.n_v_heads, cfg.dk, cfg.dv), generator=gen, device="cuda") * init_std
+            ring = torch.randn((B, cfg.conv_k - 1, cfg.conv_ch), generator=gen, device="cuda") * init_std
+            rp = torch.zeros(B, dtype=torch.int32, device="cuda")
+            abi.dn_set_state(h, 0, S, ring, rp)
+            del S, ring
+        layers.append(h)
+    return layers
+
+
+def make_inputs(cfg: DNConfig, B: int, n: int, seed: int):
+    """n sets of (x, g, beta) on the host, float32, drawn with the workload's
+    recipe (x ~ N(0,1); a, b ~ N(0,1) -> g, beta)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    sets = []
+    for _ in range(n):
+        x = rng.standard_normal((B, cfg.hidden)).astype(np.float32)
+        g, beta = gates_from_ab(rng.standard_normal((B, cfg.n_v_heads)), rng.standard_normal((B, cfg.n_v_heads)))
+        sets.append((x, g, beta))
+    return sets
+
+
+def bench_gpu(cfg, B, init_std, steps, warmup, n_layers, seed, use_graph, dist_ctx, torch, abi):
+    dev = torch.device("cuda")
+    layers = setup_layers(cfg, B, n_layers, init_std, seed, torch, abi)
+    host_inputs = make_inputs(cfg, B, n_layers, seed + 7)
+    d_in = [(torch.from_numpy(x).to(dev), torch.from_numpy(g).to(dev), torch.from_numpy(b).to(dev))
+            for x, g, b in host_inputs]
+    d_out = [torch.empty((B, cfg.hidden), dtype=torch.float32, device=dev) for _ in range(n_layers)]
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        l = i % n_layers
+        x, g, b = d_in[l]
+        abi.dn_step(layers[l], B, x, g, b, d_out[l])
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    graph = None
+    if use_graph:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream()
+            cap.wait_stream(stream)
+            with torch.cuda.stream(cap):
+                with torch.cuda.graph(graph, stream=cap):
+                    for i in range(n_layers):
+                        step(i)
+            torch.cuda.synchronize()
+        except Exception as e:  # capture not possible: time eager launches
+            print(f"[bench] graph capture failed ({e}); timing eager launches", file=sys.stderr)
+            graph = None
+    launches_per_step = 3
+
+    # ---- timed region ----
+    def run_region():
+        if graph is not None:
+            reps, rem = divmod(steps, n_layers)
+            for _ in range(reps):
+                graph.replay()
+            for i in range(rem):
+                step(i)
+        else:
+            for i in range(steps):
+                step(i)
+
+    dist_ctx.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    run_region()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    dist_ctx.barrier()
+    t1 = time.time()
+    ms = ev0.elapsed_time(ev1)
+    ms = dist_ctx.max(ms)
+
+    # ---- per-kernel device times (CUDA events between the kernels) ----
+    n_prof = min(steps, 2048)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_prof)]
+    torch.cuda.synchronize()
+    if hasattr(torch.cuda, "_sleep"):
+        torch.cuda._sleep(200_000_000)  # ~0.1 s: the CPU queues the steps meanwhile
+    for i in range(n_prof):
+        l = i % n_layers
+        abi.dn_profile_next_step(layers[l], evs[i])
+        x, g, b = d_in[l]
+        abi.dn_step(layers[l], B, x, g, b, d_out[l])
+    torch.cuda.synchronize()
+    per_kernel = {k: 0.0 for k in KERNELS}
+    for e in evs:
+        for j, k in enumerate(KERNELS):
+            per_kernel[k] += e[j].elapsed_time(e[j + 1])
+    per_kernel = {k: v / n_prof for k, v in per_kernel.items()}
+
+    # ---- end to end through the ABI with host buffers ----
+    n_e2e = min(steps, 2000)
+    hx = [torch.from_numpy(x).pin_memory() for x, _, _ in host_inputs]
+    hg = [torch.from_numpy(g).pin_memory() for _, g, _ in host_inputs]
+    hb = [torch.from_numpy(b).pin_memory() for _, _, b in host_inputs]
+    ho = [torch.empty((B, cfg.hidden), dtype=torch.float32).pin_memory() for _ in range(n_layers)]
+    for i in range(min(warmup, 8)):
+        l = i % n_layers
+        abi.dn_step(layers[l], B, hx[l], hg[l], hb[l], ho[l], stream=stream.cuda_stream)
+    dist_ctx.barrier()
+    torch.cuda.synchronize()
+    te0 = time.perf_counter()
+    for i in range(n_e2e):
+        l = i % n_layers
+        abi.dn_step(layers[l], B, hx[l], hg[l], hb[l], ho[l], stream=stream.cuda_stream)
+    torch.cuda.synchronize()
+    e2e_s = dist_ctx.max(time.perf_counter() - te0)
+    dist_ctx.barrier()
+
+    for h in layers:
+        abi.dn_destroy(h)
+    return {"ms": ms, "t_wall": (t0, t1), "per_kernel_ms": per_kernel, "graph": graph is not None,
+            "launches": steps * launches_per_step, "e2e_s": e2e_s, "n_e2e": n_e2e,
+            "h2d_bytes": B * (cfg.hidden + 2 * cfg.n_v_heads) * 4, "d2h_bytes": B * cfg.hidden * 4}
+
+
+# --------------------------------------------------------------------- CPU oracle
+def oracle_rate(cfg: DNConfig, B: int, init_std: float, budget_s: float, n_seq: int = 1):
+    """The oracle as it stands on a bounded sample: n_seq sequences of the
+    workload stepped until budget_s has passed.  Returns (sequence-steps/s,
+    steps done, threads)."""
+    from oracle import OracleLayer
+    from gated_deltanet_hybrid_gb300.inputs import random_state, zero_state
+
+    rng = np.random.Generator(np.random.PCG64(99))
+    w = make_weights(cfg, rng)
+    st = random_state(cfg, n_seq, rng, init_std) if init_std > 0 else zero_state(cfg, n_seq)
+    layer = OracleLayer(cfg, w, st)
+    inputs = make_inputs(cfg, n_seq, 4, 123)
+    layer.step(*inputs[0])  # warm
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        layer.step(*inputs[n % 4])
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return n * n_seq / dt, n, blas_threads()
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        info = [i for i in threadpool_info() if i.get("user_api") == "blas"]
+        if info:
+            return int(max(i.get("num_threads", 1) for i in info))
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+# --------------------------------------------------------------------- distributed
+class DistCtx:
+    def __init__(self, torch):
+        self.torch = torch
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.dist = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if torch.cuda.is_available():
+                torch.cuda.set_device(self.local_rank)
+            dist.init_process_group(backend=backend)
+            self.dist = dist
+
+    def barrier(self):
+        if self.dist is not None:
+            if self.torch.cuda.is_available():
+                self.dist.barrier(device_ids=[self.local_rank])
+            else:
+                self.dist.barrier()
+
+    def max(self, v: float) -> float:
+        if self.dist is None:
+            return v
+        dev = "cuda" if self.torch.cuda.is_available() else "cpu"
+        t = self.torch.tensor([float(v)], dtype=self.torch.float64, device=dev)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.dist is not None:
+            self.dist.destroy_process_group()
+
+
+# --------------------------------------------------------------------- arms
+WORKLOAD_SPECS = {
+    "35b_b64": (SHAPE_35B, 64, 0.02),
+    "35b_b1": (SHAPE_35B, 1, 0.0),
+}
+
+
+def run_ours(args, torch, dist_ctx):
+    from gated_deltanet_hybrid_gb300 import abi
+    abi.load_library()
+    hbm_peak, peak_kind = load_peaks()
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+    except Exception:
+        pass
+    cfg, B, init_std = WORKLOAD_SPECS[args.workload]
+    with ClockSampler(uuid) as clk:
+        r = bench_gpu(cfg, B, init_std, args.steps, args.warmup, args.layers, 2, args.graph,
+                      dist_ctx, torch, abi)
+    clocks = clk.summary(*r["t_wall"])
+    n = dist_ctx.world
+    ms_per_step = r["ms"] / args.steps
+    value = n * args.steps / (r["ms"] / 1e3)
+    sb = step_bytes(cfg, B)
+    kb = kernel_bytes(cfg, B)
+    dom = max(KERNELS, key=lambda k: r["per_kernel_ms"][k])
+    dom_ms = r["per_kernel_ms"][dom]
+    achieved = kb[dom] / (dom_ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": n, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32 (int8 weights)",
+        "data": "synthetic (seeded random weights, state and inputs of the 35B-shape layer)",
+        "config": {"workload": args.workload, "hidden": cfg.hidden, "qk_heads": cfg.n_qk_heads,
+                   "v_heads": cfg.n_v_heads, "dk": cfg.dk, "dv": cfg.dv, "conv_k": cfg.conv_k,
+                   "batch": B, "layers_rotated": args.layers,
+                   "l2": f"inputs larger than L2: {args.layers} layer objects rotated, "
+                         f"{sb / 1e6:.1f} MB per layer-step",
+                   "launch": "cuda graph of one step per layer" if r["graph"] else "eager",
+                   "parallelism": f"replicas x{n}" if n > 1 else "single GPU"},
+        "hbm_gbs_step": sb / (ms_per_step / 1e3) / 1e9,
+        "step_roofline_frac": sb / (ms_per_step / 1e3) / 1e9 / hbm_peak,
+        "per_kernel_us": {k: v * 1e3 for k, v in r["per_kernel_ms"].items()},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm_peak,
+                     "algorithmic_bytes_per_launch": kb[dom],
+                     "traffic": ncu_traffic(dom, args.workload),
+                     "timing": "CUDA events around each kernel, eager pass over min(K, 2048) steps"},
+        "clocks": clocks,
+        "gpu_launches": r["launches"] * n,
+        "e2e": {"value": n * r["n_e2e"] / r["e2e_s"], "unit": UNIT,
+                "h2d_bytes_per_step": r["h2d_bytes"], "d2h_bytes_per_step": r["d2h_bytes"],
+                "steps": r["n_e2e"], "api": "dn_step with pinned host pointers (copies + sync inside)"},
+    }
+    if args.secondary and args.workload != "35b_b1":
+        cfg1, B1, std1 = WORKLOAD_SPECS["35b_b1"]
+        r1 = bench_gpu(cfg1, B1, std1, max(args.steps, 2000), args.warmup, args.layers, 1, True,
+                       dist_ctx, torch, abi)
+        ms1 = r1["ms"] / max(args.steps, 2000)
+        sb1 = step_bytes(cfg1, B1)
+        line["batch1"] = {"value": n / (ms1 / 1e3), "unit": UNIT, "ms_per_step": ms1,
+                          "hbm_gbs_step": sb1 / (ms1 / 1e3) / 1e9,
+                          "step_roofline_frac": sb1 / (ms1 / 1e3) / 1e9 / hbm_peak,
+                          "per_kernel_us": {k: v * 1e3 for k, v in r1["per_kernel_ms"].items()},
+                          "launch": "cuda graph" if r1["graph"] else "eager",
+                          "e2e_value": n * r1["n_e2e"] / r1["e2e_s"]}
+        line["gpu_launches"] += r1["launches"] * n
+    if dist_ctx.rank == 0 and not args.no_cpu_baseline:
+        rate, nst, thr = oracle_rate(cfg, B, init_std, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate / B, "unit": UNIT, "cores": thr, "kind": "oracle",
+                                "sample": f"{nst} sequence-steps of one sequence of the {args.workload} "
+                                          f"layer (float64 numpy oracle, {args.cpu_seconds:.0f} s), "
+                                          f"scaled to layer-steps of batch {B}"}
+    return line
+
+
+def run_reference(args, dist_ctx):
+    """The oracle as the reference arm: each step is one sequence-step of the
+    workload's layer (a bounded sample of the batch), scaled to layer-steps."""
+    if dist_ctx.rank != 0:
+        return None
+    from oracle import OracleLayer
+    from gated_deltanet_hybrid_gb300.inputs import random_state, zero_state
+    cfg, B, init_std = WORKLOAD_SPECS[args.workload]
+    rng = np.random.Generator(np.random.PCG64(99))
+    w = make_weights(cfg, rng)
+    st = random_state(cfg, 1, rng, init_std) if init_std > 0 else zero_state(cfg, 1)
+    layer = OracleLayer(cfg, w, st)
+    inputs = make_inputs(cfg, 1, 4, 123)
+    for i in range(args.warmup):
+        layer.step(*inputs[i % 4])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        layer.step(*inputs[i % 4])
+    dt = time.perf_counter() - t0
+    value = args.steps / dt / B
+    thr = blas_threads()
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist_ctx.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * B * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": args.workload, "batch": B},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle",
+                             "sample": f"each step is one sequence-step of one sequence of the "
+                                       f"batch-{B} layer, scaled to layer-steps"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=tuple(WORKLOAD_SPECS), default="35b_b64")
+    ap.add_argument("--layers", type=int, default=8, help="layer objects rotated in the timed region")
+    ap.add_argument("--graph", action=argparse.BooleanOptionalAction, default=False,
+                    help="replay a CUDA graph of one step per layer in the timed region")
+    ap.add_argument("--secondary", action=argparse.BooleanOptionalAction, default=True,
+                    help="also measure the batch-1 workload")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    import torch
+    dist_ctx = DistCtx(torch)
+    try:
+        if args.impl == "reference":
+            line = run_reference(args, dist_ctx)
+        else:
+            if not torch.cuda.is_available():
+                raise SystemExit("bench.py --impl ours needs a CUDA device")
+            torch.cuda.set_device(dist_ctx.local_rank)
+            line = run_ours(args, torch, dist_ctx)
+        if line is not None and dist_ctx.rank == 0:
+            print(json.dumps(line), flush=True)
+    finally:
+        dist_ctx.close()
+
+
+if __name__ == "__main__":
+    main()

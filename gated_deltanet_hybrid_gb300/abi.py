@@ -1,0 +1,209 @@
+"""Python binding of libdn: the C ABI of include/dn.h under the same names.
+
+Argument marshalling only.  Every step of the layer runs in the library's
+CUDA kernels; nothing here computes.  Host arrays are numpy arrays (or CPU
+torch tensors) and are passed as DN_PTR_HOST; CUDA torch tensors are passed
+as DN_PTR_DEVICE together with torch's current stream.  There is no
+fallback: if libdn.so is missing, loading fails with an error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+DN_OK = 0
+DN_EINVAL = -1
+DN_ENOMEM = -2
+DN_ECUDA = -3
+DN_EFAILED = -4
+DN_EINJECTED = -5
+DN_PTR_HOST = 0
+DN_PTR_DEVICE = 1
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdn.so")
+
+#: every call the header declares, in declaration order
+ABI_SYMBOLS = ("dn_create", "dn_set_state", "dn_get_state", "dn_step", "dn_destroy",
+               "dn_debug_fail_next", "dn_profile_next_step", "dn_device_bytes", "dn_strerror")
+
+
+class DNError(RuntimeError):
+    def __init__(self, call: str, code: int):
+        self.code = code
+        super().__init__(f"{call} failed: {code} ({_strerror(code)})")
+
+
+class dn_config(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("n_qk_heads", ctypes.c_int32),
+                ("n_v_heads", ctypes.c_int32), ("dk", ctypes.c_int32), ("dv", ctypes.c_int32),
+                ("conv_k", ctypes.c_int32), ("max_batch", ctypes.c_int32),
+                ("l2_eps", ctypes.c_float), ("norm_eps", ctypes.c_float),
+                ("q_scale", ctypes.c_float)]
+
+
+class dn_weights(ctypes.Structure):
+    _fields_ = [("w_in", ctypes.c_void_p), ("s_in", ctypes.c_void_p),
+                ("w_conv", ctypes.c_void_p), ("w_norm", ctypes.c_void_p),
+                ("w_out", ctypes.c_void_p), ("s_out", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libdn.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with gated_deltanet_hybrid_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    vp, i32, f32p = ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p
+    lib.dn_create.argtypes = [ctypes.POINTER(dn_config), ctypes.POINTER(dn_weights), vp,
+                              ctypes.POINTER(ctypes.c_void_p)]
+    lib.dn_create.restype = i32
+    lib.dn_set_state.argtypes = [vp, i32, i32, f32p, f32p, vp, i32]
+    lib.dn_set_state.restype = i32
+    lib.dn_get_state.argtypes = [vp, i32, i32, f32p, f32p, vp, i32]
+    lib.dn_get_state.restype = i32
+    lib.dn_step.argtypes = [vp, i32, f32p, f32p, f32p, f32p, i32, vp]
+    lib.dn_step.restype = i32
+    lib.dn_destroy.argtypes = [vp]
+    lib.dn_destroy.restype = None
+    lib.dn_debug_fail_next.argtypes = [vp, i32]
+    lib.dn_debug_fail_next.restype = i32
+    lib.dn_profile_next_step.argtypes = [vp, ctypes.POINTER(ctypes.c_void_p)]
+    lib.dn_profile_next_step.restype = i32
+    lib.dn_device_bytes.argtypes = []
+    lib.dn_device_bytes.restype = ctypes.c_int64
+    lib.dn_strerror.argtypes = [i32]
+    lib.dn_strerror.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _strerror(code: int) -> str:
+    try:
+        return load_library().dn_strerror(code).decode()
+    except Exception:  # pragma: no cover
+        return "?"
+
+
+def _check(call: str, rc: int, check: bool) -> int:
+    if check and rc != DN_OK:
+        raise DNError(call, rc)
+    return rc
+
+
+def _is_cuda_tensor(a) -> bool:
+    return hasattr(a, "is_cuda") and bool(a.is_cuda)
+
+
+def _ptr(a, dtype: str):
+    """(pointer, kind) of a contiguous array of the given dtype name."""
+    if a is None:
+        return None, None
+    if hasattr(a, "data_ptr"):  # torch tensor
+        import torch
+        want = {"float32": torch.float32, "int32": torch.int32, "int8": torch.int8}[dtype]
+        if a.dtype != want or not a.is_contiguous():
+            raise TypeError(f"expected a contiguous {dtype} tensor")
+        return a.data_ptr(), (DN_PTR_DEVICE if a.is_cuda else DN_PTR_HOST)
+    arr = a
+    if not isinstance(arr, np.ndarray) or arr.dtype != np.dtype(dtype) or not arr.flags.c_contiguous:
+        raise TypeError(f"expected a C-contiguous numpy {dtype} array")
+    return arr.ctypes.data, DN_PTR_HOST
+
+
+def _same_kind(*kinds):
+    ks = {k for k in kinds if k is not None}
+    if len(ks) != 1:
+        raise TypeError("all array arguments of one call must be on the host or all on the device")
+    return ks.pop()
+
+
+def _stream_of(stream, kind):
+    if stream is not None:
+        return ctypes.c_void_p(int(stream))
+    if kind == DN_PTR_DEVICE:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    return ctypes.c_void_p(None)
+
+
+def dn_create(cfg, weights, max_batch: int, stream=None, check: bool = True):
+    """Create a layer from a DNConfig-like object and host weight arrays.
+    Returns the layer handle (ctypes.c_void_p)."""
+    lib = load_library()
+    c = dn_config(cfg.hidden, cfg.n_qk_heads, cfg.n_v_heads, cfg.dk, cfg.dv, cfg.conv_k,
+                  int(max_batch), cfg.l2_eps, cfg.norm_eps, cfg.qscale)
+    arrs = [np.ascontiguousarray(weights.w_in, np.int8), np.ascontiguousarray(weights.s_in, np.float32),
+            np.ascontiguousarray(weights.w_conv, np.float32), np.ascontiguousarray(weights.w_norm, np.float32),
+            np.ascontiguousarray(weights.w_out, np.int8), np.ascontiguousarray(weights.s_out, np.float32)]
+    w = dn_weights(*[a.ctypes.data for a in arrs])
+    if stream is None:
+        try:
+            import torch
+            stream = torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+        except ImportError:  # pragma: no cover
+            stream = None
+    handle = ctypes.c_void_p()
+    rc = lib.dn_create(ctypes.byref(c), ctypes.byref(w), ctypes.c_void_p(stream), ctypes.byref(handle))
+    _check("dn_create", rc, check)
+    return handle if rc == DN_OK else rc
+
+
+def dn_set_state(layer, seq0: int, S, ring, ring_pos, check: bool = True) -> int:
+    lib = load_library()
+    ps, ks = _ptr(S, "float32")
+    pr, kr = _ptr(ring, "float32")
+    pp, kp = _ptr(ring_pos, "int32")
+    kind = _same_kind(ks, kr, kp)
+    n = int(S.shape[0])
+    rc = lib.dn_set_state(layer, int(seq0), n, ps, pr, pp, kind)
+    return _check("dn_set_state", rc, check)
+
+
+def dn_get_state(layer, seq0: int, n: int, S=None, ring=None, ring_pos=None, check: bool = True) -> int:
+    """Fill whichever of S, ring, ring_pos are given (host or device arrays)."""
+    lib = load_library()
+    ps, ks = _ptr(S, "float32")
+    pr, kr = _ptr(ring, "float32")
+    pp, kp = _ptr(ring_pos, "int32")
+    kind = _same_kind(ks, kr, kp)
+    rc = lib.dn_get_state(layer, int(seq0), int(n), ps, pr, pp, kind)
+    return _check("dn_get_state", rc, check)
+
+
+def dn_step(layer, batch: int, x, g, beta, out, stream=None, check: bool = True) -> int:
+    lib = load_library()
+    px, kx = _ptr(x, "float32")
+    pg, kg = _ptr(g, "float32")
+    pb, kb = _ptr(beta, "float32")
+    po, ko = _ptr(out, "float32")
+    kind = _same_kind(kx, kg, kb, ko)
+    rc = lib.dn_step(layer, int(batch), px, pg, pb, po, kind, _stream_of(stream, kind))
+    return _check("dn_step", rc, check)
+
+
+def dn_destroy(layer) -> None:
+    load_library().dn_destroy(layer)
+
+
+def dn_debug_fail_next(layer, code: int, check: bool = True) -> int:
+    return _check("dn_debug_fail_next", load_library().dn_debug_fail_next(layer, int(code)), check)
+
+
+def dn_profile_next_step(layer, events, check: bool = True) -> int:
+    """events: four torch.cuda.Event(enable_timing=True) (or None to cancel)."""
+    lib = load_library()
+    if events is None:
+        return _check("dn_profile_next_step", lib.dn_profile_next_step(layer, None), check)
+    arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    return _check("dn_profile_next_step", lib.dn_profile_next_step(layer, arr), check)
+
+
+def dn_device_bytes() -> int:
+    return int(load_library().dn_device_bytes())

@@ -1,0 +1,324 @@
+// C ABI of libdn: the five layer calls of the page "qwen36: run the DeltaNet
+// layer end to end on the card (Q36_DN_GPU=1)" (section "What the PR does":
+// create / set_state / get_state / step / destroy on one object per layer),
+// plus failure injection and device-memory accounting for tests.  See
+// include/dn.h for the contract of every call.
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "dn_internal.cuh"
+
+#define DN_API extern "C" __attribute__((visibility("default")))
+
+struct dn_layer {
+    dn::Dims d;
+    dn::LayerDev L;
+    cudaStream_t stream;
+    int device;
+    int failed;
+    int fail_next;
+    cudaEvent_t prof[4];  // one-shot per-kernel events for the next step
+    int prof_armed;
+    size_t bytes;
+    std::vector<void *> allocs;
+};
+
+namespace {
+
+std::atomic<int64_t> g_device_bytes{0};
+
+int layer_alloc(dn_layer *l, void **p, size_t n) {
+    *p = nullptr;
+    if (n == 0) return DN_OK;
+    cudaError_t e = cudaMalloc(p, n);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();  // allocation failures are not sticky; clear it
+        *p = nullptr;
+        return e == cudaErrorMemoryAllocation ? DN_ENOMEM : DN_ECUDA;
+    }
+    l->allocs.push_back(*p);
+    l->bytes += n;
+    g_device_bytes += (int64_t)n;
+    return DN_OK;
+}
+
+void layer_free_all(dn_layer *l) {
+    for (void *p : l->allocs) cudaFree(p);
+    g_device_bytes -= (int64_t)l->bytes;
+    l->allocs.clear();
+    l->bytes = 0;
+}
+
+bool valid_cfg(const dn_config *c) {
+    if (c->hidden < 16 || c->hidden > 16384 || c->hidden % 16 != 0) return false;
+    if (c->n_qk_heads < 1 || c->n_v_heads < 1 || c->n_v_heads > 64) return false;
+    if (c->n_v_heads % c->n_qk_heads != 0) return false;
+    if (!(c->dk == 32 || c->dk == 64 || c->dk == 128)) return false;
+    if (!(c->dv == 32 || c->dv == 64 || c->dv == 128)) return false;
+    if (c->conv_k < 2 || c->conv_k > 8) return false;
+    if (c->max_batch < 1 || c->max_batch > 1024) return false;
+    if (!(c->l2_eps > 0.f) || !(c->norm_eps > 0.f)) return false;
+    if (c->q_scale != c->q_scale) return false;  // NaN
+    return true;
+}
+
+int cuda_fail(dn_layer *l) {
+    l->failed = 1;
+    return DN_ECUDA;
+}
+
+#define DN_TRY(layer, expr)                            \
+    do {                                               \
+        cudaError_t e_ = (expr);                       \
+        if (e_ != cudaSuccess) return cuda_fail(layer); \
+    } while (0)
+
+}  // namespace
+
+namespace dn {
+int num_sms() {
+    static int cached_dev = -1, cached = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev != cached_dev) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cached = n > 0 ? n : 1;
+        cached_dev = dev;
+    }
+    return cached;
+}
+}  // namespace dn
+
+DN_API const char *dn_strerror(int code) {
+    switch (code) {
+        case DN_OK: return "ok";
+        case DN_EINVAL: return "invalid argument";
+        case DN_ENOMEM: return "out of device memory";
+        case DN_ECUDA: return "CUDA error (layer is now failed)";
+        case DN_EFAILED: return "layer failed earlier";
+        case DN_EINJECTED: return "injected failure";
+        default: return "unknown status";
+    }
+}
+
+DN_API int64_t dn_device_bytes(void) { return g_device_bytes.load(); }
+
+DN_API int dn_create(const dn_config *cfg, const dn_weights *w, void *stream, dn_layer **out) {
+    if (out == nullptr) return DN_EINVAL;
+    *out = nullptr;
+    if (cfg == nullptr || w == nullptr || !valid_cfg(cfg)) return DN_EINVAL;
+    if (!w->w_in || !w->s_in || !w->w_conv || !w->w_norm || !w->w_out || !w->s_out)
+        return DN_EINVAL;
+
+    dn_layer *l = new (std::nothrow) dn_layer();
+    if (l == nullptr) return DN_ENOMEM;
+    dn::Dims &d = l->d;
+    d.hidden = cfg->hidden;
+    d.n_qk = cfg->n_qk_heads;
+    d.n_v = cfg->n_v_heads;
+    d.dk = cfg->dk;
+    d.dv = cfg->dv;
+    d.conv_k = cfg->conv_k;
+    d.max_batch = cfg->max_batch;
+    d.qk_dim = d.n_qk * d.dk;
+    d.v_dim = d.n_v * d.dv;
+    d.conv_ch = 2 * d.qk_dim + d.v_dim;
+    d.in_rows = d.conv_ch + d.v_dim;
+    d.l2_eps = cfg->l2_eps;
+    d.norm_eps = cfg->norm_eps;
+    d.q_scale = cfg->q_scale;
+    l->stream = (cudaStream_t)stream;
+    cudaGetDevice(&l->device);
+
+    const size_t MB = (size_t)d.max_batch;
+    const size_t s_elems = MB * d.n_v * d.dk * d.dv;
+    dn::LayerDev &L = l->L;
+    int rc = DN_OK;
+#define ALLOC(ptr, bytes)                                               \
+    if (rc == DN_OK) rc = layer_alloc(l, (void **)&(ptr), (size_t)(bytes));
+    ALLOC(L.w_in, (size_t)d.in_rows * d.hidden);
+    ALLOC(L.s_in, (size_t)d.in_rows * 4);
+    ALLOC(L.wconv_t, (size_t)d.conv_k * d.conv_ch * 4);
+    ALLOC(L.w_norm, (size_t)d.dv * 4);
+    ALLOC(L.w_out, (size_t)d.hidden * d.v_dim);
+    ALLOC(L.s_out, (size_t)d.hidden * 4);
+    ALLOC(L.S, s_elems * 4);
+    ALLOC(L.ring, MB * d.conv_k * d.conv_ch * 4);
+    ALLOC(L.rpos, MB * 2 * 4);
+    ALLOC(L.qkvz, MB * d.in_rows * 4);
+    ALLOC(L.nrm, MB * d.v_dim * 4);
+    ALLOC(L.x_stage, MB * d.hidden * 4);
+    ALLOC(L.g_stage, MB * d.n_v * 4);
+    ALLOC(L.beta_stage, MB * d.n_v * 4);
+    ALLOC(L.out_stage, MB * d.hidden * 4);
+    ALLOC(L.ring_stage, MB * (d.conv_k - 1) * d.conv_ch * 4);
+    ALLOC(L.rp_stage, MB * 4);
+#undef ALLOC
+    if (rc != DN_OK) {
+        layer_free_all(l);
+        delete l;
+        return rc;
+    }
+
+    std::vector<float> wct((size_t)d.conv_k * d.conv_ch);
+    for (int c = 0; c < d.conv_ch; ++c)
+        for (int t = 0; t < d.conv_k; ++t)
+            wct[(size_t)t * d.conv_ch + c] = w->w_conv[(size_t)c * d.conv_k + t];
+
+    cudaStream_t st = l->stream;
+    cudaError_t e = cudaSuccess;
+    auto H2D = cudaMemcpyHostToDevice;
+    if (e == cudaSuccess) e = cudaMemcpyAsync(L.w_in, w->w_in, (size_t)d.in_rows * d.hidden, H2D, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(L.s_in, w->s_in, (size_t)d.in_rows * 4, H2D, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(L.wconv_t, wct.data(), wct.size() * 4, H2D, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(L.w_norm, w->w_norm, (size_t)d.dv * 4, H2D, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(L.w_out, w->w_out, (size_t)d.hidden * d.v_dim, H2D, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(L.s_out, w->s_out, (size_t)d.hidden * 4, H2D, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(L.S, 0, s_elems * 4, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(L.ring, 0, MB * d.conv_k * d.conv_ch * 4, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(L.rpos, 0, MB * 2 * 4, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) {
+        layer_free_all(l);
+        delete l;
+        return DN_ECUDA;
+    }
+    *out = l;
+    return DN_OK;
+}
+
+DN_API void dn_destroy(dn_layer *l) {
+    if (l == nullptr) return;
+    int cur = 0;
+    cudaGetDevice(&cur);
+    if (cur != l->device) cudaSetDevice(l->device);
+    cudaStreamSynchronize(l->stream);
+    layer_free_all(l);
+    if (cur != l->device) cudaSetDevice(cur);
+    delete l;
+}
+
+DN_API int dn_debug_fail_next(dn_layer *l, int code) {
+    if (l == nullptr || code > 0) return DN_EINVAL;
+    l->fail_next = code;
+    return DN_OK;
+}
+
+DN_API int dn_profile_next_step(dn_layer *l, void *const *events) {
+    if (l == nullptr) return DN_EINVAL;
+    if (events == nullptr) {
+        l->prof_armed = 0;
+        return DN_OK;
+    }
+    for (int i = 0; i < 4; ++i) {
+        if (events[i] == nullptr) return DN_EINVAL;
+        l->prof[i] = (cudaEvent_t)events[i];
+    }
+    l->prof_armed = 1;
+    return DN_OK;
+}
+
+DN_API int dn_set_state(dn_layer *l, int seq0, int n, const float *S, const float *ring,
+                        const int32_t *ring_pos, int ptr_kind) {
+    if (l == nullptr) return DN_EINVAL;
+    const dn::Dims &d = l->d;
+    if (ptr_kind != DN_PTR_HOST && ptr_kind != DN_PTR_DEVICE) return DN_EINVAL;
+    if (seq0 < 0 || n < 1 || seq0 + n > d.max_batch) return DN_EINVAL;
+    if (S == nullptr || ring == nullptr || ring_pos == nullptr) return DN_EINVAL;
+    if (l->failed) return DN_EFAILED;
+    cudaStream_t st = l->stream;
+
+    // ring positions are validated on the host before anything is written
+    std::vector<int32_t> rp((size_t)n);
+    if (ptr_kind == DN_PTR_HOST) {
+        std::memcpy(rp.data(), ring_pos, (size_t)n * 4);
+    } else {
+        DN_TRY(l, cudaMemcpyAsync(rp.data(), ring_pos, (size_t)n * 4, cudaMemcpyDeviceToHost, st));
+        DN_TRY(l, cudaStreamSynchronize(st));
+    }
+    for (int i = 0; i < n; ++i)
+        if (rp[i] < 0 || rp[i] > d.conv_k - 2) return DN_EINVAL;
+
+    const size_t tile = (size_t)d.n_v * d.dk * d.dv;
+    const size_t ring_n = (size_t)n * (d.conv_k - 1) * d.conv_ch;
+    const cudaMemcpyKind kind = ptr_kind == DN_PTR_HOST ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToDevice;
+    DN_TRY(l, cudaMemcpyAsync(l->L.S + (size_t)seq0 * tile, S, (size_t)n * tile * 4, kind, st));
+    DN_TRY(l, cudaMemcpyAsync(l->L.ring_stage, ring, ring_n * 4, kind, st));
+    DN_TRY(l, cudaMemcpyAsync(l->L.rp_stage, rp.data(), (size_t)n * 4, cudaMemcpyHostToDevice, st));
+    DN_TRY(l, dn::launch_ring_import(d, l->L, seq0, n, st));
+    DN_TRY(l, cudaStreamSynchronize(st));
+    return DN_OK;
+}
+
+DN_API int dn_get_state(dn_layer *l, int seq0, int n, float *S, float *ring, int32_t *ring_pos,
+                        int ptr_kind) {
+    if (l == nullptr) return DN_EINVAL;
+    const dn::Dims &d = l->d;
+    if (ptr_kind != DN_PTR_HOST && ptr_kind != DN_PTR_DEVICE) return DN_EINVAL;
+    if (seq0 < 0 || n < 1 || seq0 + n > d.max_batch) return DN_EINVAL;
+    cudaStream_t st = l->stream;
+    const size_t tile = (size_t)d.n_v * d.dk * d.dv;
+    const size_t ring_n = (size_t)n * (d.conv_k - 1) * d.conv_ch;
+    const cudaMemcpyKind kind = ptr_kind == DN_PTR_HOST ? cudaMemcpyDeviceToHost : cudaMemcpyDeviceToDevice;
+    cudaError_t e = cudaSuccess;
+    if (S != nullptr)
+        e = cudaMemcpyAsync(S, l->L.S + (size_t)seq0 * tile, (size_t)n * tile * 4, kind, st);
+    if (e == cudaSuccess && (ring != nullptr || ring_pos != nullptr))
+        e = dn::launch_ring_export(d, l->L, seq0, n, st);
+    if (e == cudaSuccess && ring != nullptr)
+        e = cudaMemcpyAsync(ring, l->L.ring_stage, ring_n * 4, kind, st);
+    if (e == cudaSuccess && ring_pos != nullptr)
+        e = cudaMemcpyAsync(ring_pos, l->L.rp_stage, (size_t)n * 4, kind, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(l);
+    return DN_OK;
+}
+
+DN_API int dn_step(dn_layer *l, int batch, const float *x, const float *g, const float *beta,
+                   float *out, int ptr_kind, void *stream) {
+    if (l == nullptr) return DN_EINVAL;
+    const dn::Dims &d = l->d;
+    if (ptr_kind != DN_PTR_HOST && ptr_kind != DN_PTR_DEVICE) return DN_EINVAL;
+    if (batch < 1 || batch > d.max_batch) return DN_EINVAL;
+    if (x == nullptr || g == nullptr || beta == nullptr || out == nullptr) return DN_EINVAL;
+    if (l->failed) return DN_EFAILED;
+    if (l->fail_next != 0) {
+        const int code = l->fail_next;
+        l->fail_next = 0;
+        l->failed = 1;
+        return code;
+    }
+    cudaStream_t st = stream != nullptr ? (cudaStream_t)stream : l->stream;
+    const dn::LayerDev &L = l->L;
+    const float *xd = x, *gd = g, *bd = beta;
+    float *od = out;
+    if (ptr_kind == DN_PTR_HOST) {
+        DN_TRY(l, cudaMemcpyAsync(L.x_stage, x, (size_t)batch * d.hidden * 4, cudaMemcpyHostToDevice, st));
+        DN_TRY(l, cudaMemcpyAsync(L.g_stage, g, (size_t)batch * d.n_v * 4, cudaMemcpyHostToDevice, st));
+        DN_TRY(l, cudaMemcpyAsync(L.beta_stage, beta, (size_t)batch * d.n_v * 4, cudaMemcpyHostToDevice, st));
+        xd = L.x_stage;
+        gd = L.g_stage;
+        bd = L.beta_stage;
+        od = L.out_stage;
+    }
+    const bool prof = l->prof_armed != 0;
+    l->prof_armed = 0;
+    if (prof) DN_TRY(l, cudaEventRecord(l->prof[0], st));
+    DN_TRY(l, dn::launch_gemv_i8(L.w_in, L.s_in, xd, L.qkvz, d.in_rows, d.hidden, batch, nullptr,
+                                 d.conv_k, st));
+    if (prof) DN_TRY(l, cudaEventRecord(l->prof[1], st));
+    DN_TRY(l, dn::launch_dn_core(d, L, batch, gd, bd, st));
+    if (prof) DN_TRY(l, cudaEventRecord(l->prof[2], st));
+    DN_TRY(l, dn::launch_gemv_i8(L.w_out, L.s_out, L.nrm, od, d.hidden, d.v_dim, batch, L.rpos,
+                                 d.conv_k, st));
+    if (prof) DN_TRY(l, cudaEventRecord(l->prof[3], st));
+    if (ptr_kind == DN_PTR_HOST) {
+        DN_TRY(l, cudaMemcpyAsync(out, L.out_stage, (size_t)batch * d.hidden * 4, cudaMemcpyDeviceToHost, st));
+        DN_TRY(l, cudaStreamSynchronize(st));
+    }
+    return DN_OK;
+}

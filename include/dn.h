@@ -1,0 +1,188 @@
+/*
+ * dn.h — C ABI of the gated-DeltaNet decode-step library (libdn.so, sm_103a).
+ *
+ * One dn_layer is one gated-DeltaNet layer for up to max_batch independent
+ * sequences.  It follows the layer object of the page "qwen36: run the
+ * DeltaNet layer end to end on the card (Q36_DN_GPU=1): conv, recurrence and
+ * gated norm join the two projections", section "What the PR does": one
+ * object per layer holds the short-conv ring, the recurrent state
+ * [n_v_heads x dk x dv], the conv and norm weights, the two int8 projections
+ * and one token's scratch in device memory, behind five entry points
+ * (create / set_state / get_state / step / destroy).  The gates stay outside
+ * and arrive per head with every step.
+ *
+ * Conventions for every call:
+ *   - Return value: DN_OK (0) or a negative DN_E* code.  Argument checks run
+ *     on the host before any device work; a call that fails them returns
+ *     DN_EINVAL and leaves the layer and its state untouched.
+ *   - A CUDA error seen by a call marks the layer failed (sticky): afterwards
+ *     dn_step and dn_set_state return DN_EFAILED, while dn_get_state still
+ *     copies out what the device holds and dn_destroy still frees it (the
+ *     page: "get_state works after a failed step").
+ *   - Device work is enqueued on a CUDA stream and is asynchronous unless a
+ *     call says otherwise; errors of asynchronous work surface at a later
+ *     call on the same layer.
+ *   - Arrays are dense, row-major (last index fastest), fp32 unless stated.
+ *   - The library keeps no pointer to caller memory after a call returns.
+ */
+#ifndef DN_H
+#define DN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------- */
+#define DN_OK         0
+#define DN_EINVAL    -1  /* bad argument: nothing was done */
+#define DN_ENOMEM    -2  /* device allocation failed */
+#define DN_ECUDA     -3  /* a CUDA call failed; the layer is now failed */
+#define DN_EFAILED   -4  /* the layer failed earlier; only get_state/destroy work */
+#define DN_EINJECTED -5  /* failure injected with dn_debug_fail_next */
+
+/* ---- where a pointer argument lives ------------------------------------ */
+#define DN_PTR_HOST   0
+#define DN_PTR_DEVICE 1
+
+typedef struct dn_layer dn_layer; /* opaque; owns all of its device memory */
+
+/*
+ * Layer dimensions.  The page's backend object "takes those dimensions as
+ * parameters (vh <= 64, kdim/vdim <= 256)" (section "Where this goes next").
+ * This build accepts:
+ *   hidden      multiple of 16, 16 .. 16384
+ *   n_qk_heads  >= 1, divides n_v_heads; n_v_heads <= 64
+ *   dk, dv      each one of 32, 64, 128
+ *   conv_k      2 .. 8 (taps of the causal short conv; the ring keeps conv_k-1)
+ *   max_batch   1 .. 1024 (sequences the layer holds state for)
+ *   l2_eps      eps inside the square root of the q/k L2 norms (> 0)
+ *   norm_eps    eps of the gated RMSNorm (> 0)
+ *   q_scale     multiplies the normalised q (e.g. 1/sqrt(dk))
+ * Derived: conv_ch = 2*n_qk_heads*dk + n_v_heads*dv,
+ *          in_rows = conv_ch + n_v_heads*dv, v_dim = n_v_heads*dv.
+ */
+typedef struct dn_config {
+    int32_t hidden, n_qk_heads, n_v_heads, dk, dv, conv_k, max_batch;
+    float l2_eps, norm_eps, q_scale;
+} dn_config;
+
+/*
+ * Layer weights, host pointers, copied by dn_create (the caller may free
+ * them afterwards).  The fused in_proj is "qkv ++ z, one GEMV instead of
+ * two" with int8 rows and one fp32 scale per row (page "feat(qwen36): the
+ * dense trunk places itself", section "What this adds", item 1):
+ *   w_in   int8 [in_rows][hidden]; rows are q | k | v | z, head h of a block
+ *          is the contiguous slice h*d .. (h+1)*d; y[o] = s_in[o]*sum_i w_in[o][i]*x[i]
+ *   s_in   [in_rows]
+ *   w_conv [conv_ch][conv_k]; tap conv_k-1 meets the newest input
+ *   w_norm [dv]; one gated-RMSNorm weight vector shared by all value heads
+ *   w_out  int8 [hidden][v_dim]; out[o] = s_out[o]*sum_i w_out[o][i]*n[i]
+ *   s_out  [hidden]
+ * Value head h reads q/k head h / (n_v_heads / n_qk_heads).
+ */
+typedef struct dn_weights {
+    const int8_t *w_in;
+    const float  *s_in;
+    const float  *w_conv;
+    const float  *w_norm;
+    const int8_t *w_out;
+    const float  *s_out;
+} dn_weights;
+
+/*
+ * dn_create — allocate a layer on the current CUDA device, upload its
+ * weights and zero its state (S = 0, ring = 0, ring_pos = 0 for every
+ * sequence).  `stream` (a cudaStream_t, NULL for the legacy default stream)
+ * becomes the layer's stream for state copies and for dn_step calls that
+ * pass no stream.  Synchronous: the layer is ready when the call returns.
+ * On success *out receives the layer; on failure *out is set to NULL and
+ * nothing stays allocated.  Errors: DN_EINVAL, DN_ENOMEM, DN_ECUDA.
+ */
+int dn_create(const dn_config *cfg, const dn_weights *w, void *stream, dn_layer **out);
+
+/*
+ * dn_set_state — overwrite the state of sequences [seq0, seq0+n):
+ *   S        [n][n_v_heads][dk][dv]   recurrent state, row = key index
+ *   ring     [n][conv_k-1][conv_ch]   the last conv_k-1 conv inputs
+ *   ring_pos [n] int32 in [0, conv_k-2], the ring slot of the oldest input
+ * ptr_kind (DN_PTR_HOST or DN_PTR_DEVICE) says where all three live.  This
+ * is the push of the page's host-canonical state ("The host copy of the
+ * state stays the engine's, moved with set/get_state").  Returns after the
+ * copy has completed (synchronises the layer's stream).  Errors: DN_EINVAL
+ * (range, pointer or ring_pos out of range), DN_EFAILED, DN_ECUDA.
+ */
+int dn_set_state(dn_layer *layer, int seq0, int n, const float *S, const float *ring,
+                 const int32_t *ring_pos, int ptr_kind);
+
+/*
+ * dn_get_state — copy out the state of sequences [seq0, seq0+n) in the same
+ * layout as dn_set_state.  Any of S, ring, ring_pos may be NULL to skip it.
+ * Works on a failed layer (returns what the device holds).  Synchronises the
+ * layer's stream (so all prior dn_step work is included).  Errors:
+ * DN_EINVAL, DN_ECUDA.
+ */
+int dn_get_state(dn_layer *layer, int seq0, int n, float *S, float *ring, int32_t *ring_pos,
+                 int ptr_kind);
+
+/*
+ * dn_step — advance sequences [0, batch) by one decode token ("a decode
+ * token end to end": in_proj GEMV, causal conv + SiLU with the ring
+ * advancing, per value head the L2 norms of q and k, the decay, the delta
+ * against the decayed state, the write-back, out = q^T S over the updated
+ * state, the gated RMSNorm with silu(z), out_proj GEMV):
+ *   x    [batch][hidden]     layer input
+ *   g    [batch][n_v_heads]  log-decay per head (the state is scaled by exp(g))
+ *   beta [batch][n_v_heads]  write strength per head
+ *   out  [batch][hidden]     layer output (written)
+ * ptr_kind DN_PTR_DEVICE: all four are device pointers; the call only
+ *   enqueues kernels on `stream` (NULL: the layer's stream) and returns; it
+ *   allocates nothing and does not synchronise, so it can be captured in a
+ *   CUDA graph.  x/g/beta must stay valid until the work has run.
+ * ptr_kind DN_PTR_HOST: all four are host pointers; the call uploads x, g
+ *   and beta, runs the step, downloads out and synchronises `stream` before
+ *   returning (the page's "x up ... out down").  Pinned host memory makes
+ *   the copies asynchronous DMA.
+ * Sequences >= batch are untouched.  Errors: DN_EINVAL (batch < 1 or >
+ * max_batch, NULL pointer, bad ptr_kind), DN_EFAILED, DN_EINJECTED, DN_ECUDA.
+ */
+int dn_step(dn_layer *layer, int batch, const float *x, const float *g, const float *beta,
+            float *out, int ptr_kind, void *stream);
+
+/* dn_destroy — free the layer and all its device memory.  NULL-safe.  Waits
+ * for the layer's outstanding work first. */
+void dn_destroy(dn_layer *layer);
+
+/*
+ * dn_debug_fail_next — failure injection for tests: the next dn_step on this
+ * layer returns `code` (a negative DN_E* value) before any device work and
+ * marks the layer failed, as the page's fake backend "can be told to fail;
+ * a failing step turns the layer off".  code = 0 cancels a pending
+ * injection.  Errors: DN_EINVAL.
+ */
+int dn_debug_fail_next(dn_layer *layer, int code);
+
+/*
+ * dn_profile_next_step — instrumentation for benchmarks: the next dn_step on
+ * this layer records events[0] on its stream before its first kernel,
+ * events[1] after the in_proj GEMV, events[2] after the fused conv /
+ * recurrence / gated-norm kernel and events[3] after the out_proj GEMV, so
+ * that cudaEventElapsedTime gives each kernel's device time.  `events` points
+ * to four cudaEvent_t created by the caller (timing enabled); it is used by
+ * that one dn_step call only (one-shot).  NULL cancels.  Errors: DN_EINVAL.
+ */
+int dn_profile_next_step(dn_layer *layer, void *const *events);
+
+/* dn_device_bytes — device bytes currently held by all live layers of this
+ * process (leak accounting: 0 once every layer is destroyed). */
+int64_t dn_device_bytes(void);
+
+/* dn_strerror — a static string naming a status code. */
+const char *dn_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DN_H */

@@ -1,0 +1,223 @@
+"""The layer object's contract on the GPU: state ownership (set/get round
+trip, slices, ring-position convention), failure handling (the page's fake
+backend "can be told to fail; a failing step turns the layer off and the CPU
+continues from the card's state"), device-memory accounting, bitwise
+reproducibility and checkpoint/resume."""
+import numpy as np
+import pytest
+
+from gated_deltanet_hybrid_gb300 import abi
+from gated_deltanet_hybrid_gb300.inputs import (SHAPE_35B, TINY, DNState, WorkloadStream,
+                                                custom_workload, make_weights, random_state)
+
+from harness import GpuLayer
+
+pytestmark = pytest.mark.gpu
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dev_inputs(x, g, b):
+    torch = _torch()
+    return (torch.from_numpy(x).cuda(), torch.from_numpy(g).cuda(), torch.from_numpy(b).cuda(),
+            torch.empty(x.shape, dtype=torch.float32, device="cuda"))
+
+
+def _run(layer, stream, steps, batch):
+    outs = []
+    for _ in range(steps):
+        x, gates = stream.next_step()
+        xd, gd, bd, od = _dev_inputs(x[:batch], gates[0][0][:batch], gates[0][1][:batch])
+        abi.dn_step(layer.handle, batch, xd, gd, bd, od)
+        outs.append(od.cpu().numpy())
+    return outs
+
+
+def test_state_round_trip_is_exact_host_and_device():
+    torch = _torch()
+    rng = np.random.default_rng(0)
+    w = make_weights(TINY, rng)
+    st = random_state(TINY, 6, rng, 0.5)
+    st.ring_pos[:] = [0, 1, 2, 2, 1, 0]
+    layer = GpuLayer.create(TINY, w, 6, st)
+    try:
+        back = layer.get_state()
+        assert np.array_equal(back.S, st.S)
+        assert np.array_equal(back.ring, st.ring)
+        assert np.array_equal(back.ring_pos, st.ring_pos)
+        # slice [2, 5) through device pointers
+        S_d = torch.empty((3, 4, 32, 32), dtype=torch.float32, device="cuda")
+        r_d = torch.empty((3, 3, TINY.conv_ch), dtype=torch.float32, device="cuda")
+        p_d = torch.empty(3, dtype=torch.int32, device="cuda")
+        abi.dn_get_state(layer.handle, 2, 3, S_d, r_d, p_d)
+        assert np.array_equal(S_d.cpu().numpy(), st.S[2:5])
+        assert np.array_equal(r_d.cpu().numpy(), st.ring[2:5])
+        assert np.array_equal(p_d.cpu().numpy(), st.ring_pos[2:5])
+        # push a modified slice back through device pointers
+        abi.dn_set_state(layer.handle, 0, S_d * 2, r_d + 1, torch.tensor([1, 1, 1], dtype=torch.int32,
+                                                                          device="cuda"))
+        back2 = layer.get_state()
+        assert np.array_equal(back2.S[:3], st.S[2:5] * 2)
+        assert np.array_equal(back2.ring[:3], st.ring[2:5] + 1)
+        assert list(back2.ring_pos[:3]) == [1, 1, 1]
+        assert np.array_equal(back2.S[3:], st.S[3:])
+    finally:
+        layer.destroy()
+
+
+def test_ring_positions_advance_after_set_state():
+    """ring_pos set to p advances to (p + t) mod (conv_k-1) after t steps, and
+    the ring then holds exactly the last conv_k-1 in_proj outputs."""
+    rng = np.random.default_rng(1)
+    w = make_weights(TINY, rng)
+    st = random_state(TINY, 3, rng, 0.1)
+    st.ring_pos[:] = [2, 0, 1]
+    layer = GpuLayer.create(TINY, w, 3, st)
+    try:
+        stream = WorkloadStream(custom_workload("t", TINY, 3, 5, seed=3))
+        _run(layer, stream, 5, 3)
+        assert list(layer.get_state().ring_pos) == [(2 + 5) % 3, (0 + 5) % 3, (1 + 5) % 3]
+    finally:
+        layer.destroy()
+
+
+def test_invalid_arguments_leave_state_untouched():
+    torch = _torch()
+    rng = np.random.default_rng(2)
+    w = make_weights(TINY, rng)
+    st = random_state(TINY, 2, rng, 0.3)
+    layer = GpuLayer.create(TINY, w, 2, st)
+    try:
+        bad = st.ring_pos.copy()
+        bad[1] = 3  # conv_k - 1 slots: valid values 0..2
+        rc = abi.dn_set_state(layer.handle, 0, st.S * 0, st.ring * 0, bad, check=False)
+        assert rc == abi.DN_EINVAL
+        x = torch.zeros((3, 256), device="cuda")
+        g = torch.zeros((3, 4), device="cuda")
+        rc = abi.dn_step(layer.handle, 3, x, g, g, x.clone(), check=False)  # batch > max_batch
+        assert rc == abi.DN_EINVAL
+        assert abi.dn_get_state(layer.handle, 1, 2, np.empty((2, 4, 32, 32), np.float32),
+                                check=False) == abi.DN_EINVAL
+        back = layer.get_state()
+        assert np.array_equal(back.S, st.S) and np.array_equal(back.ring, st.ring)
+        assert np.array_equal(back.ring_pos, st.ring_pos)
+    finally:
+        layer.destroy()
+
+
+def test_injected_failure_turns_layer_off_and_state_stays_readable():
+    rng = np.random.default_rng(3)
+    w = make_weights(TINY, rng)
+    layer = GpuLayer.create(TINY, w, 2)
+    try:
+        stream = WorkloadStream(custom_workload("t", TINY, 2, 8, seed=4))
+        _run(layer, stream, 4, 2)
+        good = layer.get_state()
+        abi.dn_debug_fail_next(layer.handle, abi.DN_EINJECTED)
+        x, gates = stream.next_step()
+        xd, gd, bd, od = _dev_inputs(x, *gates[0])
+        assert abi.dn_step(layer.handle, 2, xd, gd, bd, od, check=False) == abi.DN_EINJECTED
+        assert abi.dn_step(layer.handle, 2, xd, gd, bd, od, check=False) == abi.DN_EFAILED
+        assert abi.dn_set_state(layer.handle, 0, good.S, good.ring, good.ring_pos,
+                                check=False) == abi.DN_EFAILED
+        after = layer.get_state()  # the engine continues from what the card holds
+        assert np.array_equal(after.S, good.S)
+        assert np.array_equal(after.ring, good.ring)
+        assert np.array_equal(after.ring_pos, good.ring_pos)
+    finally:
+        layer.destroy()
+
+
+def test_device_memory_accounting_returns_to_zero():
+    base = abi.dn_device_bytes()
+    w = make_weights(TINY, np.random.default_rng(4))
+    for i in range(10):
+        layer = GpuLayer.create(TINY, w, 1 + 7 * i)
+        assert abi.dn_device_bytes() > base
+        layer.destroy()
+        assert abi.dn_device_bytes() == base
+    assert base == 0
+
+
+def test_two_runs_are_bitwise_identical():
+    wl = custom_workload("det", SHAPE_35B, batch=3, steps=6, seed=9, init_std=0.02)
+    outs, states = [], []
+    for _ in range(2):
+        stream = WorkloadStream(wl)
+        layer = GpuLayer.create(wl.cfg, stream.weights[0], 3, stream.states[0])
+        try:
+            outs.append(_run(layer, stream, 6, 3))
+            states.append(layer.get_state())
+        finally:
+            layer.destroy()
+    for a, b in zip(outs[0], outs[1]):
+        assert np.array_equal(a, b)
+    assert np.array_equal(states[0].S, states[1].S)
+    assert np.array_equal(states[0].ring, states[1].ring)
+
+
+def test_host_pointer_step_equals_device_pointer_step():
+    wl = custom_workload("hd", TINY, batch=4, steps=5, seed=10, init_std=0.1)
+    s1, s2 = WorkloadStream(wl), WorkloadStream(wl)
+    a = GpuLayer.create(TINY, s1.weights[0], 4, s1.states[0])
+    b = GpuLayer.create(TINY, s2.weights[0], 4, s2.states[0])
+    try:
+        for _ in range(5):
+            x, gates = s1.next_step()
+            s2.next_step()
+            out_h = np.empty_like(x)
+            abi.dn_step(a.handle, 4, x, gates[0][0], gates[0][1], out_h)  # host pointers
+            xd, gd, bd, od = _dev_inputs(x, *gates[0])
+            abi.dn_step(b.handle, 4, xd, gd, bd, od)
+            assert np.array_equal(out_h, od.cpu().numpy())
+        assert np.array_equal(a.get_state().S, b.get_state().S)
+    finally:
+        a.destroy()
+        b.destroy()
+
+
+def test_sequences_beyond_batch_are_untouched():
+    rng = np.random.default_rng(11)
+    w = make_weights(TINY, rng)
+    st = random_state(TINY, 7, rng, 0.2)
+    layer = GpuLayer.create(TINY, w, 7, st)
+    try:
+        stream = WorkloadStream(custom_workload("u", TINY, 7, 4, seed=12))
+        _run(layer, stream, 4, 5)
+        back = layer.get_state()
+        assert np.array_equal(back.S[5:], st.S[5:])
+        assert np.array_equal(back.ring[5:], st.ring[5:])
+        assert np.array_equal(back.ring_pos[5:], st.ring_pos[5:])
+        assert not np.array_equal(back.S[:5], st.S[:5])
+    finally:
+        layer.destroy()
+
+
+def test_checkpoint_resume_is_bitwise():
+    """Checkpoint at step 128 with get_state, restore into a fresh layer with
+    set_state and continue: identical to 256 uninterrupted steps."""
+    wl = custom_workload("ck", SHAPE_35B, batch=2, steps=256, seed=13, init_std=0.02)
+    s_full = WorkloadStream(wl)
+    full = GpuLayer.create(wl.cfg, s_full.weights[0], 2, s_full.states[0])
+    s_ck = WorkloadStream(wl)
+    first = GpuLayer.create(wl.cfg, s_ck.weights[0], 2, s_ck.states[0])
+    try:
+        out_full = _run(full, s_full, 256, 2)
+        _run(first, s_ck, 128, 2)
+        ck = first.get_state()
+        first.destroy()
+        second = GpuLayer.create(wl.cfg, s_ck.weights[0], 2, ck)
+        try:
+            out_rest = _run(second, s_ck, 128, 2)
+            assert np.array_equal(out_rest[-1], out_full[-1])
+            fs, ss = full.get_state(), second.get_state()
+            assert np.array_equal(fs.S, ss.S) and np.array_equal(fs.ring, ss.ring)
+            assert np.array_equal(fs.ring_pos, ss.ring_pos)
+        finally:
+            second.destroy()
+    finally:
+        full.destroy()
+        first.destroy()
