@@ -270,6 +270,9 @@ def bench_gpu(cfg, B, init_std, steps, warmup, n_layers, seed, use_graph, dist_c
     # ---- per-kernel device times (CUDA events between the kernels) ----
     n_prof = min(steps, 2048)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_prof)]
+    for es in evs:  # torch creates the CUDA event on first record
+        for e in es:
+            e.record(stream)
     torch.cuda.synchronize()
     if hasattr(torch.cuda, "_sleep"):
         torch.cuda._sleep(200_000_000)  # ~0.1 s: the CPU queues the steps meanwhile

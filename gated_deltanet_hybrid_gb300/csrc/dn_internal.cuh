@@ -43,12 +43,24 @@ struct LayerDev {
     float *x_stage, *g_stage, *beta_stage, *out_stage;
     float *ring_stage;     // [max_batch][conv_k-1][conv_ch]
     int32_t *rp_stage;     // [max_batch]
+    // tensor-core projections: split-K partials, per-tile arrival counters
+    float *part_in, *part_out;
+    int *cnt_in, *cnt_out;
+    int *err;              // device-side error word (bounded waits that gave up)
 };
 
 // y[b][o] = s[o] * sum_k W[o][k] * x[b][k] for b < B.  Optionally advances
 // the per-sequence ring positions of `rpos` for b < B (done by block 0).
 cudaError_t launch_gemv_i8(const int8_t *W, const float *s, const float *x, float *y, int M,
                            int K, int B, int32_t *rpos_advance, int conv_k, cudaStream_t st);
+
+// Tensor-core (tcgen05) version of the same projection for batches >= 8.
+bool tc_gemm_supported(int M, int K);
+int tc_gemm_splits(int M, int K, int B);
+cudaError_t launch_gemm_i8_tc(const int8_t *W, const float *s, const float *x, float *y,
+                              float *part, int *counters, int *err, int M, int K, int B, int ks,
+                              int32_t *rpos_advance, int conv_k, cudaStream_t st);
+constexpr int kTcMinBatch = 8;
 
 // The fused conv / L2 / gated-delta / readout / gated-RMSNorm step.
 cudaError_t launch_dn_core(const Dims &d, const LayerDev &L, int B, const float *g,
