@@ -3,6 +3,7 @@
 // create / set_state / get_state / step / destroy on one object per layer),
 // plus failure injection and device-memory accounting for tests.  See
 // include/dn.h for the contract of every call.
+#include <algorithm>
 #include <atomic>
 #include <cstdlib>
 #include <cstring>
@@ -157,6 +158,27 @@ DN_API int dn_create(const dn_config *cfg, const dn_weights *w, void *stream, dn
     ALLOC(L.out_stage, MB * d.hidden * 4);
     ALLOC(L.ring_stage, MB * (d.conv_k - 1) * d.conv_ch * 4);
     ALLOC(L.rp_stage, MB * 4);
+    // tensor-core projections: the largest split-K partial buffer over all
+    // batch sizes the layer accepts, and one arrival counter per tile
+    const bool tc_in = dn::tc_gemm_supported(d.in_rows, d.hidden);
+    const bool tc_out = dn::tc_gemm_supported(d.hidden, d.v_dim);
+    size_t part_in = 0, part_out = 0;
+    for (int b = dn::kTcMinBatch; b <= d.max_batch; ++b) {
+        if (tc_in) {
+            const int ks = dn::tc_gemm_splits(d.in_rows, d.hidden, b);
+            if (ks > 1) part_in = std::max(part_in, (size_t)ks * b * d.in_rows);
+        }
+        if (tc_out) {
+            const int ks = dn::tc_gemm_splits(d.hidden, d.v_dim, b);
+            if (ks > 1) part_out = std::max(part_out, (size_t)ks * b * d.hidden);
+        }
+    }
+    const size_t chunks = (MB + 63) / 64;
+    ALLOC(L.part_in, part_in * 4);
+    ALLOC(L.part_out, part_out * 4);
+    ALLOC(L.cnt_in, chunks * (d.in_rows / 128 + 1) * 4);
+    ALLOC(L.cnt_out, chunks * (d.hidden / 128 + 1) * 4);
+    ALLOC(L.err, 4);
 #undef ALLOC
     if (rc != DN_OK) {
         layer_free_all(l);
@@ -181,6 +203,9 @@ DN_API int dn_create(const dn_config *cfg, const dn_weights *w, void *stream, dn
     if (e == cudaSuccess) e = cudaMemsetAsync(L.S, 0, s_elems * 4, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(L.ring, 0, MB * d.conv_k * d.conv_ch * 4, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(L.rpos, 0, MB * 2 * 4, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(L.cnt_in, 0, chunks * (d.in_rows / 128 + 1) * 4, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(L.cnt_out, 0, chunks * (d.hidden / 128 + 1) * 4, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(L.err, 0, 4, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) {
         layer_free_all(l);
@@ -273,8 +298,11 @@ DN_API int dn_get_state(dn_layer *l, int seq0, int n, float *S, float *ring, int
         e = cudaMemcpyAsync(ring, l->L.ring_stage, ring_n * 4, kind, st);
     if (e == cudaSuccess && ring_pos != nullptr)
         e = cudaMemcpyAsync(ring_pos, l->L.rp_stage, (size_t)n * 4, kind, st);
+    int dev_err = 0;
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&dev_err, l->L.err, 4, cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(l);
+    if (dev_err != 0) return cuda_fail(l);  // a kernel gave up on a bounded wait
     return DN_OK;
 }
 
@@ -308,13 +336,27 @@ DN_API int dn_step(dn_layer *l, int batch, const float *x, const float *g, const
     const bool prof = l->prof_armed != 0;
     l->prof_armed = 0;
     if (prof) DN_TRY(l, cudaEventRecord(l->prof[0], st));
-    DN_TRY(l, dn::launch_gemv_i8(L.w_in, L.s_in, xd, L.qkvz, d.in_rows, d.hidden, batch, nullptr,
-                                 d.conv_k, st));
+    const bool tc_in = batch >= dn::kTcMinBatch && dn::tc_gemm_supported(d.in_rows, d.hidden);
+    const bool tc_out = batch >= dn::kTcMinBatch && dn::tc_gemm_supported(d.hidden, d.v_dim);
+    if (tc_in)
+        DN_TRY(l, dn::launch_gemm_i8_tc(L.w_in, L.s_in, xd, L.qkvz, L.part_in, L.cnt_in, L.err,
+                                        d.in_rows, d.hidden, batch,
+                                        dn::tc_gemm_splits(d.in_rows, d.hidden, batch), nullptr,
+                                        d.conv_k, st));
+    else
+        DN_TRY(l, dn::launch_gemv_i8(L.w_in, L.s_in, xd, L.qkvz, d.in_rows, d.hidden, batch,
+                                     nullptr, d.conv_k, st));
     if (prof) DN_TRY(l, cudaEventRecord(l->prof[1], st));
     DN_TRY(l, dn::launch_dn_core(d, L, batch, gd, bd, st));
     if (prof) DN_TRY(l, cudaEventRecord(l->prof[2], st));
-    DN_TRY(l, dn::launch_gemv_i8(L.w_out, L.s_out, L.nrm, od, d.hidden, d.v_dim, batch, L.rpos,
-                                 d.conv_k, st));
+    if (tc_out)
+        DN_TRY(l, dn::launch_gemm_i8_tc(L.w_out, L.s_out, L.nrm, od, L.part_out, L.cnt_out, L.err,
+                                        d.hidden, d.v_dim, batch,
+                                        dn::tc_gemm_splits(d.hidden, d.v_dim, batch), L.rpos,
+                                        d.conv_k, st));
+    else
+        DN_TRY(l, dn::launch_gemv_i8(L.w_out, L.s_out, L.nrm, od, d.hidden, d.v_dim, batch, L.rpos,
+                                     d.conv_k, st));
     if (prof) DN_TRY(l, cudaEventRecord(l->prof[3], st));
     if (ptr_kind == DN_PTR_HOST) {
         DN_TRY(l, cudaMemcpyAsync(out, L.out_stage, (size_t)batch * d.hidden * 4, cudaMemcpyDeviceToHost, st));

@@ -68,3 +68,48 @@ def test_tiny_ragged_batch_in_larger_layer():
     5, and the untouched 2 keep their state (checked in the layer tests)."""
     wl = custom_workload("tiny_b5", TINY, batch=5, steps=30, seed=8, init_std=0.1)
     _assert_ok(run_parity(wl, max_batch=7))
+
+
+@pytest.mark.parametrize("batch", [8, 9, 40, 64, 65, 130])
+def test_tiny_tensor_core_batches(batch):
+    """Batches >= 8 take the tensor-core projections: padded batch columns
+    (9 -> 16), several 64-sequence chunks (65, 130) and split-K tiles."""
+    wl = custom_workload(f"tiny_b{batch}", TINY, batch=batch, steps=10, seed=30 + batch, init_std=0.05)
+    sample = np.array(sorted({0, batch // 2, batch - 1}))
+    _assert_ok(run_parity(wl, sample=sample))
+
+
+def test_35b_batch65_two_chunks():
+    wl = custom_workload("35b_b65", SHAPE_35B, batch=65, steps=6, seed=65, init_std=0.02)
+    _assert_ok(run_parity(wl, sample=np.array([0, 63, 64])))
+
+
+@pytest.mark.parametrize("batch", [1, 3, 8, 37, 64])
+def test_in_proj_exact_integer_case(batch):
+    """Integer x in [-3, 3] and power-of-two row scales make every partial
+    sum of the in_proj an exact integer below 2^24, on the CUDA cores and on
+    the tensor cores alike.  After one step the ring holds the in_proj's q|k|v
+    rows, which must then equal numpy's int64 matmul bitwise."""
+    import torch
+    from gated_deltanet_hybrid_gb300 import abi
+    from gated_deltanet_hybrid_gb300.inputs import make_weights
+    from harness import GpuLayer
+
+    cfg = SHAPE_35B
+    rng = np.random.default_rng(100 + batch)
+    w = make_weights(cfg, rng)
+    w.s_in[:] = (2.0 ** rng.integers(-3, 2, size=cfg.in_rows)).astype(np.float32)
+    x = rng.integers(-3, 4, size=(batch, cfg.hidden)).astype(np.float32)
+    exact = (x.astype(np.int64) @ w.w_in.astype(np.int64).T) * w.s_in.astype(np.float64)
+    layer = GpuLayer.create(cfg, w, batch)
+    try:
+        out = torch.empty((batch, cfg.hidden), device="cuda")
+        g = torch.zeros((batch, cfg.n_v_heads), device="cuda")
+        abi.dn_step(layer.handle, batch, torch.from_numpy(x).cuda(), g, g.clone(), out)
+        st = layer.get_state()
+        # ring_pos 0 -> 1 after one step: the newest input sits in slot 0
+        newest = st.ring[:, 0, :]
+        assert np.array_equal(newest.astype(np.float64), exact[:, :cfg.conv_ch])
+        assert np.all(st.ring_pos == 1)
+    finally:
+        layer.destroy()
