@@ -46,7 +46,7 @@ from gated_deltanet_hybrid_gb300.inputs import (SHAPE_35B, WORKLOADS, DNConfig, 
 
 METRIC = "DeltaNet layer-steps/s and achieved HBM GB/s (% of roofline) at batch 1 and 64"
 UNIT = "layer-steps/s"
-KERNELS = ("in_proj_gemv", "dn_core", "out_proj_gemv")
+KERNELS = ("in_proj", "dn_core", "out_proj")
 
 
 # --------------------------------------------------------------------- bytes
@@ -69,7 +69,7 @@ def kernel_bytes(cfg: DNConfig, B: int) -> dict[str, int]:
                 + cfg.conv_ch * 4 + cfg.in_rows * 4 + cfg.v_dim * 4 + 2 * cfg.n_v_heads * 4)
     k2 = B * core_seq + cfg.conv_ch * cfg.conv_k * 4 + cfg.dv * 4
     k3 = cfg.hidden * cfg.v_dim + cfg.hidden * 4 + B * (cfg.v_dim + cfg.hidden) * 4
-    return {"in_proj_gemv": k1, "dn_core": k2, "out_proj_gemv": k3}
+    return {"in_proj": k1, "dn_core": k2, "out_proj": k3}
 
 
 def load_peaks() -> tuple[float, str]:

@@ -66,6 +66,20 @@ bool valid_cfg(const dn_config *c) {
     return true;
 }
 
+// W [M][K] int8 -> [ceil(M/128)][ceil(K/64)][128][64], zero-padded
+std::vector<uint8_t> tile_weights(const int8_t *W, int M, int K) {
+    const int MT = (M + dn::kTileM - 1) / dn::kTileM, KT = (K + dn::kTileK - 1) / dn::kTileK;
+    std::vector<uint8_t> t((size_t)MT * KT * dn::kTileM * dn::kTileK, 0);
+    for (int m = 0; m < M; ++m) {
+        const int mt = m / dn::kTileM, r = m % dn::kTileM;
+        for (int k = 0; k < K; ++k) {
+            const int kt = k / dn::kTileK, kk = k % dn::kTileK;
+            t[(((size_t)mt * KT + kt) * dn::kTileM + r) * dn::kTileK + kk] = (uint8_t)W[(size_t)m * K + k];
+        }
+    }
+    return t;
+}
+
 int cuda_fail(dn_layer *l) {
     l->failed = 1;
     return DN_ECUDA;
@@ -141,16 +155,19 @@ DN_API int dn_create(const dn_config *cfg, const dn_weights *w, void *stream, dn
     int rc = DN_OK;
 #define ALLOC(ptr, bytes)                                               \
     if (rc == DN_OK) rc = layer_alloc(l, (void **)&(ptr), (size_t)(bytes));
-    ALLOC(L.w_in, (size_t)d.in_rows * d.hidden);
+    const std::vector<uint8_t> wt_in = tile_weights(w->w_in, d.in_rows, d.hidden);
+    const std::vector<uint8_t> wt_out = tile_weights(w->w_out, d.hidden, d.v_dim);
+    const size_t kt_in = (size_t)(d.hidden + dn::kTileK - 1) / dn::kTileK;
+    const size_t kt_out = (size_t)(d.v_dim + dn::kTileK - 1) / dn::kTileK;
+    ALLOC(L.w_in, wt_in.size());
     ALLOC(L.s_in, (size_t)d.in_rows * 4);
     ALLOC(L.wconv_t, (size_t)d.conv_k * d.conv_ch * 4);
     ALLOC(L.w_norm, (size_t)d.dv * 4);
-    ALLOC(L.w_out, (size_t)d.hidden * d.v_dim);
+    ALLOC(L.w_out, wt_out.size());
     ALLOC(L.s_out, (size_t)d.hidden * 4);
     ALLOC(L.S, s_elems * 4);
     ALLOC(L.ring, MB * d.conv_k * d.conv_ch * 4);
     ALLOC(L.rpos, MB * 2 * 4);
-    ALLOC(L.qkvz, MB * d.in_rows * 4);
     ALLOC(L.nrm, MB * d.v_dim * 4);
     ALLOC(L.x_stage, MB * d.hidden * 4);
     ALLOC(L.g_stage, MB * d.n_v * 4);
@@ -158,26 +175,31 @@ DN_API int dn_create(const dn_config *cfg, const dn_weights *w, void *stream, dn
     ALLOC(L.out_stage, MB * d.hidden * 4);
     ALLOC(L.ring_stage, MB * (d.conv_k - 1) * d.conv_ch * 4);
     ALLOC(L.rp_stage, MB * 4);
-    // tensor-core projections: the largest split-K partial buffer over all
-    // batch sizes the layer accepts, and one arrival counter per tile
-    const bool tc_in = dn::tc_gemm_supported(d.in_rows, d.hidden);
-    const bool tc_out = dn::tc_gemm_supported(d.hidden, d.v_dim);
-    size_t part_in = 0, part_out = 0;
-    for (int b = dn::kTcMinBatch; b <= d.max_batch; ++b) {
-        if (tc_in) {
-            const int ks = dn::tc_gemm_splits(d.in_rows, d.hidden, b);
-            if (ks > 1) part_in = std::max(part_in, (size_t)ks * b * d.in_rows);
-        }
-        if (tc_out) {
-            const int ks = dn::tc_gemm_splits(d.hidden, d.v_dim, b);
-            if (ks > 1) part_out = std::max(part_out, (size_t)ks * b * d.hidden);
-        }
-    }
+    // projections: the largest segment-partial buffer over all batch sizes
+    // the layer accepts; packed activations for the tensor-core path
     const size_t chunks = (MB + 63) / 64;
+    size_t part_in = 0, part_out = 0, tiles_in = 0, tiles_out = 0, xb_bytes_in = 0, xb_bytes_out = 0;
+    for (size_t ch = 1; ch <= chunks; ++ch) {
+        const int b = (int)std::min<size_t>(ch * 64, MB);
+        const dn::GemmPlan gi = dn::plan_tc_gemm(d.in_rows, d.hidden, b);
+        const dn::GemmPlan go = dn::plan_tc_gemm(d.hidden, d.v_dim, b);
+        part_in = std::max(part_in, (size_t)gi.tiles * gi.max_seg * 64 * 128);
+        part_out = std::max(part_out, (size_t)go.tiles * go.max_seg * 64 * 128);
+        tiles_in = std::max(tiles_in, (size_t)gi.tiles);
+        tiles_out = std::max(tiles_out, (size_t)go.tiles);
+        // the stream-K schedule computes c * U / G in 32 bits
+        if ((uint64_t)gi.U * gi.G >= (1ull << 32) || (uint64_t)go.U * go.G >= (1ull << 32)) rc = DN_EINVAL;
+    }
+    if (d.max_batch >= dn::kTcMinBatch) {
+        xb_bytes_in = chunks * kt_in * dn::kOpTile;
+        xb_bytes_out = chunks * kt_out * dn::kOpTile;
+    }
     ALLOC(L.part_in, part_in * 4);
     ALLOC(L.part_out, part_out * 4);
-    ALLOC(L.cnt_in, chunks * (d.in_rows / 128 + 1) * 4);
-    ALLOC(L.cnt_out, chunks * (d.hidden / 128 + 1) * 4);
+    ALLOC(L.nseg_in, tiles_in * 4);
+    ALLOC(L.nseg_out, tiles_out * 4);
+    ALLOC(L.xb_in, xb_bytes_in);
+    ALLOC(L.xb_out, xb_bytes_out);
     ALLOC(L.err, 4);
 #undef ALLOC
     if (rc != DN_OK) {
@@ -194,17 +216,17 @@ DN_API int dn_create(const dn_config *cfg, const dn_weights *w, void *stream, dn
     cudaStream_t st = l->stream;
     cudaError_t e = cudaSuccess;
     auto H2D = cudaMemcpyHostToDevice;
-    if (e == cudaSuccess) e = cudaMemcpyAsync(L.w_in, w->w_in, (size_t)d.in_rows * d.hidden, H2D, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(L.w_in, wt_in.data(), wt_in.size(), H2D, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(L.s_in, w->s_in, (size_t)d.in_rows * 4, H2D, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(L.wconv_t, wct.data(), wct.size() * 4, H2D, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(L.w_norm, w->w_norm, (size_t)d.dv * 4, H2D, st);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(L.w_out, w->w_out, (size_t)d.hidden * d.v_dim, H2D, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(L.w_out, wt_out.data(), wt_out.size(), H2D, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(L.s_out, w->s_out, (size_t)d.hidden * 4, H2D, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(L.S, 0, s_elems * 4, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(L.ring, 0, MB * d.conv_k * d.conv_ch * 4, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(L.rpos, 0, MB * 2 * 4, st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(L.cnt_in, 0, chunks * (d.in_rows / 128 + 1) * 4, st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(L.cnt_out, 0, chunks * (d.hidden / 128 + 1) * 4, st);
+    if (e == cudaSuccess && xb_bytes_in) e = cudaMemsetAsync(L.xb_in, 0, xb_bytes_in, st);
+    if (e == cudaSuccess && xb_bytes_out) e = cudaMemsetAsync(L.xb_out, 0, xb_bytes_out, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(L.err, 0, 4, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) {
@@ -336,27 +358,29 @@ DN_API int dn_step(dn_layer *l, int batch, const float *x, const float *g, const
     const bool prof = l->prof_armed != 0;
     l->prof_armed = 0;
     if (prof) DN_TRY(l, cudaEventRecord(l->prof[0], st));
-    const bool tc_in = batch >= dn::kTcMinBatch && dn::tc_gemm_supported(d.in_rows, d.hidden);
-    const bool tc_out = batch >= dn::kTcMinBatch && dn::tc_gemm_supported(d.hidden, d.v_dim);
-    if (tc_in)
-        DN_TRY(l, dn::launch_gemm_i8_tc(L.w_in, L.s_in, xd, L.qkvz, L.part_in, L.cnt_in, L.err,
-                                        d.in_rows, d.hidden, batch,
-                                        dn::tc_gemm_splits(d.in_rows, d.hidden, batch), nullptr,
-                                        d.conv_k, st));
-    else
-        DN_TRY(l, dn::launch_gemv_i8(L.w_in, L.s_in, xd, L.qkvz, d.in_rows, d.hidden, batch,
-                                     nullptr, d.conv_k, st));
+    const bool tc = batch >= dn::kTcMinBatch;
+    if (tc) {
+        DN_TRY(l, dn::launch_pack_b(xd, L.xb_in, batch, d.hidden, st));
+        DN_TRY(l, dn::launch_gemm_i8_tc(L.w_in, L.xb_in, L.part_in, L.nseg_in, L.err, d.in_rows,
+                                        d.hidden, batch, st));
+    } else {
+        DN_TRY(l, dn::launch_gemv_i8(L.w_in, xd, L.part_in, L.nseg_in, L.err, d.in_rows, d.hidden,
+                                     batch, st));
+    }
     if (prof) DN_TRY(l, cudaEventRecord(l->prof[1], st));
-    DN_TRY(l, dn::launch_dn_core(d, L, batch, gd, bd, st));
-    if (prof) DN_TRY(l, cudaEventRecord(l->prof[2], st));
-    if (tc_out)
-        DN_TRY(l, dn::launch_gemm_i8_tc(L.w_out, L.s_out, L.nrm, od, L.part_out, L.cnt_out, L.err,
-                                        d.hidden, d.v_dim, batch,
-                                        dn::tc_gemm_splits(d.hidden, d.v_dim, batch), L.rpos,
-                                        d.conv_k, st));
+    if (dn::dn_core_stream_ok(d, batch))
+        DN_TRY(l, dn::launch_dn_core_stream(d, L, batch, gd, bd, tc, st));
     else
-        DN_TRY(l, dn::launch_gemv_i8(L.w_out, L.s_out, L.nrm, od, d.hidden, d.v_dim, batch, L.rpos,
-                                     d.conv_k, st));
+        DN_TRY(l, dn::launch_dn_core(d, L, batch, gd, bd, tc, st));
+    if (prof) DN_TRY(l, cudaEventRecord(l->prof[2], st));
+    if (tc)
+        DN_TRY(l, dn::launch_gemm_i8_tc(L.w_out, L.xb_out, L.part_out, L.nseg_out, L.err, d.hidden,
+                                        d.v_dim, batch, st));
+    else
+        DN_TRY(l, dn::launch_gemv_i8(L.w_out, L.nrm, L.part_out, L.nseg_out, L.err, d.hidden,
+                                     d.v_dim, batch, st));
+    DN_TRY(l, dn::launch_splitk_reduce(L.part_out, L.nseg_out, L.s_out, od, d.hidden, d.v_dim, batch,
+                                       L.rpos, d.conv_k, st));
     if (prof) DN_TRY(l, cudaEventRecord(l->prof[3], st));
     if (ptr_kind == DN_PTR_HOST) {
         DN_TRY(l, cudaMemcpyAsync(out, L.out_stage, (size_t)batch * d.hidden * 4, cudaMemcpyDeviceToHost, st));

@@ -21,8 +21,10 @@
 // and stored back from registers: one read and one write of S per step.
 // Reductions run in a fixed order, so results are bitwise reproducible.
 #include <cooperative_groups.h>
+#include <cuda_bf16.h>
 
 #include "dn_internal.cuh"
+#include "dn_sched.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -32,20 +34,36 @@ namespace {
 constexpr int kThreads = 256;
 
 struct CoreParams {
-    const float *qkvz;     // [B][in_rows]
+    const float *part_in;  // in_proj segment partials (GEMV or tensor-core kernel),
+    const float *s_in;     // summed in slot order and scaled here by s_in
+    const int *nseg_in;    // segments per tile
+    SchedView sv;          // their schedule
     float *ring;           // [max_batch][conv_k][conv_ch]
     const int32_t *rpos;   // [max_batch][2]
     const float *wconv_t;  // [conv_k][conv_ch]
     const float *w_norm;   // [dv]
     float *S;              // [max_batch][n_v][dk][dv]
-    float *nrm;            // [B][v_dim]
+    float *nrm;            // [B][v_dim] fp32 output, or
+    uint8_t *xb_out;       // packed bf16 hi/lo B-operand tiles for the tensor-core out_proj
     const float *g;        // [B][n_v]
     const float *beta;     // [B][n_v]
-    int n_qk, n_v, dv, conv_k, conv_ch, qk_dim, in_rows, v_dim;
+    int n_qk, n_v, dv, conv_k, conv_ch, qk_dim, in_rows, v_dim, kt_out;
     float l2_eps, norm_eps, q_scale;
 };
 
 __device__ __forceinline__ float silu_f(float a) { return a / (1.0f + expf(-a)); }
+
+// in_proj output row c of sequence b: read directly, or summed from the
+// tensor-core kernel's segment partials in slot order, then scaled
+__device__ __forceinline__ float in_proj_out(const CoreParams &p, int b, int c) {
+    const int tile = (b >> 6) * p.sv.MT + (c >> 7);
+    const int nseg = p.nseg_in[tile];
+    const float *pt = p.part_in + (size_t)tile * p.sv.max_seg * (64 * 128) + (b & 63) * 128 + (c & 127);
+    float acc = 0.f;
+#pragma unroll 4
+    for (int k = 0; k < nseg; ++k) acc += __ldcg(pt + (size_t)k * (64 * 128));
+    return p.s_in[c] * acc;
+}
 
 template <int DK, int DJ, bool CLUSTER>
 __global__ void __launch_bounds__(kThreads, 2) dn_core_kernel(const CoreParams p) {
@@ -82,7 +100,6 @@ __global__ void __launch_bounds__(kThreads, 2) dn_core_kernel(const CoreParams p
     const int K = p.conv_k;
     int wslot = dpos + K - 1;
     if (wslot >= K) wslot -= K;
-    const float *xin = p.qkvz + (size_t)b * p.in_rows;
     float *rb = p.ring + (size_t)b * K * p.conv_ch;
     // q/k channels are shared by the `group` value heads of a q/k head and by
     // all column slices: exactly one block (first head of the group, slice 0)
@@ -96,7 +113,7 @@ __global__ void __launch_bounds__(kThreads, 2) dn_core_kernel(const CoreParams p
             c = p.qk_dim + hq * DK + (j - DK);
         else
             c = 2 * p.qk_dim + h * p.dv + col0 + (j - 2 * DK);
-        const float xv = xin[c];
+        const float xv = in_proj_out(p, b, c);
         float acc = 0.f;
         int slot = dpos;
         for (int m = 0; m < K - 1; ++m) {  // oldest input first
@@ -212,9 +229,22 @@ __global__ void __launch_bounds__(kThreads, 2) dn_core_kernel(const CoreParams p
     }
     if (tid < DJ) {
         const float rinv = 1.0f / sqrtf(total / (float)p.dv + p.norm_eps);
-        const float z = xin[p.conv_ch + h * p.dv + col0 + tid];
+        const float z = in_proj_out(p, b, p.conv_ch + h * p.dv + col0 + tid);
         const float n = o * rinv * p.w_norm[col0 + tid] * silu_f(z);
-        p.nrm[(size_t)b * p.v_dim + h * p.dv + col0 + tid] = n;
+        const int k = h * p.dv + col0 + tid;
+        if (p.xb_out == nullptr) {
+            p.nrm[(size_t)b * p.v_dim + k] = n;
+        } else {
+            // row 2*(b%64) holds bf16(n), row 2*(b%64)+1 holds bf16(n - hi), in the
+            // 8-row x 16-byte core-matrix layout of the out_proj's B operand
+            const __nv_bfloat16 hi = __float2bfloat16_rn(n);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(n - __bfloat162float(hi));
+            uint8_t *tile = p.xb_out + ((size_t)(b >> 6) * p.kt_out + (k >> 6)) * kOpTile;
+            const int kc = (k & 63) >> 3, e = k & 7;
+            const int rh = 2 * (b & 63), rl = rh + 1;
+            *reinterpret_cast<__nv_bfloat16 *>(tile + (rh >> 3) * 1024 + kc * 128 + (rh & 7) * 16 + e * 2) = hi;
+            *reinterpret_cast<__nv_bfloat16 *>(tile + (rl >> 3) * 1024 + kc * 128 + (rl & 7) * 16 + e * 2) = lo;
+        }
     }
 }
 
@@ -274,15 +304,23 @@ int choose_js(const Dims &d, int B) {
 }
 
 cudaError_t launch_dn_core(const Dims &d, const LayerDev &L, int B, const float *g,
-                           const float *beta, cudaStream_t st) {
+                           const float *beta, bool tc, cudaStream_t st) {
     CoreParams cp;
-    cp.qkvz = L.qkvz;
     cp.ring = L.ring;
     cp.rpos = L.rpos;
     cp.wconv_t = L.wconv_t;
     cp.w_norm = L.w_norm;
     cp.S = L.S;
     cp.nrm = L.nrm;
+    cp.xb_out = tc ? L.xb_out : nullptr;
+    cp.part_in = L.part_in;
+    cp.nseg_in = L.nseg_in;
+    cp.s_in = L.s_in;
+    {
+        const GemmPlan gp = plan_tc_gemm(d.in_rows, d.hidden, B);
+        cp.sv = SchedView{gp.U, gp.G, gp.KT, gp.MT, gp.max_seg};
+    }
+    cp.kt_out = (d.v_dim + kTileK - 1) / kTileK;
     cp.g = g;
     cp.beta = beta;
     cp.n_qk = d.n_qk;

@@ -5,65 +5,81 @@
 // int8 rows with one fp32 scale each, page "feat(qwen36): the dense trunk
 // places itself", section "What this adds", item 1).
 //
-// Precision.  int8 weights are exact in bf16.  The fp32 activations are split
-// into x = hi + lo with hi = bf16(x) and lo = bf16(x - hi), so that W*hi +
-// W*lo reproduces W*x to about 2^-17 relative per term, with fp32 tensor-core
-// accumulation.  hi and lo of sequence b are rows 2b and 2b+1 of the MMA's B
-// operand (N = 2 * padded batch), so one MMA covers both halves and the
-// epilogue adds columns 2b and 2b+1.
+// Precision.  int8 weights are exact in bf16.  The fp32 activations arrive
+// split into x = hi + lo with hi = bf16(x), lo = bf16(x - hi) (pack_b below),
+// so W*hi + W*lo reproduces W*x to about 2^-17 relative per term, with fp32
+// accumulation in tensor memory.  hi and lo of sequence b are rows 2b and
+// 2b+1 of the MMA's B operand (N = 2 * padded batch), so one MMA covers both
+// and the epilogue adds accumulator columns 2b and 2b+1.
 //
-// Work split.  One CTA per (128-row tile of W, K split, batch chunk of <= 64).
-// Warps 0-3 stream their 128 int8 rows from HBM with 16-byte loads (one tile
-// ahead in registers), convert to bf16 and store them in the MMA's canonical
-// K-major layout (8x16-byte core matrices); warps 4-5 convert the batch's x to
-// hi/lo bf16 the same way; warp 6 issues tcgen05.mma (M=128, N=2*B, K=16)
-// from one thread into a TMEM accumulator, STAGES shared-memory stages deep,
-// with mbarriers between the roles.  The epilogue (warps 0-3) reads TMEM with
-// tcgen05.ld.  With several K splits every CTA writes a partial tile; the
-// last CTA of a tile to finish (atomic counter) sums the partials in split
-// order, so results do not depend on scheduling.
+// Layouts.  The layer stores W as contiguous 8 KB tiles [m tile][k tile]
+// [128 rows][64 int8] and the activations as 16 KB tiles [batch chunk][k tile]
+// holding 128 B-operand rows of 64 bf16 in the MMA's canonical K-major layout
+// (8-row x 16-byte core matrices; 8-row groups 1024 bytes apart).  So every
+// pipeline stage is two 1-D bulk copies (cp.async.bulk, completed on an
+// mbarrier), and the k tiles of a row tile stream through HBM sequentially.
 //
-// Every wait is bounded (about one second of the global timer); on timeout
-// the kernel records an error in `err`, lets in-flight MMAs drain, frees its
-// TMEM and returns.
+// Work split (stream-K).  A unit is one (batch chunk, m tile, k tile).  The
+// grid has one CTA per SM; CTA c takes the contiguous unit range
+// [c*U/G, (c+1)*U/G), so all SMs get the same number of units whatever the
+// tile count.  A range covers the tail of one m tile and the head of the next
+// (a "segment" each); two TMEM accumulators alternate between segments.
+// Every segment's partial sums go to a slot of a partial buffer (schedule in
+// dn_sched.cuh); the consumer sums a tile's slots in slot order (the fused
+// core kernel for the in_proj, splitk_reduce_kernel for the out_proj), so
+// results do not depend on scheduling and no CTA waits on another.
+//
+// Roles: warp 0 issues the bulk copies, warp 1 (one thread) the MMAs, warps
+// 2-5 convert the int8 tile to bf16 in shared memory, warps 6-9 read the
+// accumulators (tcgen05.ld) and write results.  Every wait is bounded (about
+// one second of the global timer): on timeout the kernel records an error in
+// `err`, waits (bounded) for its own copies and MMAs in flight, frees its
+// tensor memory and returns.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "dn_internal.cuh"
+#include "dn_sched.cuh"
 
 namespace dn {
 namespace {
 
-constexpr int BM = 128;         // weight rows per tile (MMA M)
-constexpr int BK = 64;          // K per pipeline stage
-constexpr int STAGES = 3;
-constexpr int NB_CHUNK = 64;    // sequences per CTA (MMA N = 2 * padded count <= 128)
-constexpr int kThreads = 224;   // 7 warps
-constexpr int kProducers = 192; // warps 0-5
-constexpr uint32_t kCoreBytes = 128;             // one 8 x 16-byte core matrix
-constexpr uint32_t kGroupBytes = (BK / 8) * 128; // 8 rows x BK bf16 = 1024 bytes
+constexpr int BM = 128;          // weight rows per tile (MMA M)
+constexpr int BK = 64;           // K per unit / pipeline stage
+constexpr int STAGES = 4;
+constexpr int NB_CHUNK = 64;     // sequences per batch chunk (MMA N <= 128)
+constexpr int kThreads = 320;    // 10 warps
+constexpr int kConvThreads = 128;
+constexpr int kEpiThreads = 128;
+constexpr uint32_t kATileBytes = BM * BK;            // 8 KB int8
+constexpr uint32_t kOpTileBytes = 128 * BK * 2;      // 16 KB bf16
+constexpr uint32_t kCoreBytes = 128;
+constexpr uint32_t kGroupBytes = (BK / 8) * 128;     // 1024
+constexpr uint32_t kTmemCols = 256;                  // two 128-column accumulators
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 struct __align__(1024) GemmSmem {
-    uint8_t a[STAGES][BM * BK * 2];            // 16 KB per stage
-    uint8_t b[STAGES][2 * NB_CHUNK * BK * 2];  // 16 KB per stage
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
-    uint64_t done;
+    uint8_t a16[STAGES][kOpTileBytes];  // bf16 A operand
+    uint8_t b16[STAGES][kOpTileBytes];  // bf16 B operand (as copied)
+    uint8_t a8[STAGES][kATileBytes];    // int8 A tile (as copied)
+    uint64_t full[STAGES];              // bulk copies of the stage landed
+    uint64_t conv[STAGES];              // A converted to bf16
+    uint64_t empty[STAGES];             // MMAs done reading the stage
+    uint64_t acc_full[2];               // accumulator ready for the epilogue
+    uint64_t acc_empty[2];              // epilogue done reading the accumulator
+    uint64_t drain;                     // all MMAs of this CTA completed
     uint32_t tmem_base;
     int abort_flag;
-    int last;
 };
 
 struct GemmParams {
-    const int8_t *W;
-    const float *s;
-    const float *x;
-    float *y;
-    float *part;      // [ks][B][M] partials (ks > 1)
-    int *counters;    // [chunks][M / BM], zero between launches
-    int32_t *rpos;    // optional: ring positions to advance (out_proj)
+    const uint8_t *Wt;   // int8 weight tiles
+    const uint8_t *xb;   // bf16 B tiles [nchunks][KT][16 KB]
+    float *part;         // [tiles][max_seg][64][128] segment partials (unscaled)
+    int *nseg;           // [tiles] segment count, written by each tile's last segment
     int *err;
-    int M, K, B, ks, k_split, conv_k;
+    int M, MT, KT, B, nchunks, U, G, max_seg;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -84,6 +100,12 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -96,36 +118,43 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Waits for the phase of `bar` with the given parity.  Gives up (returns
-// false) after about one second or when another role has aborted.
-__device__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+// Waits for the phase of `bar` with the given parity; false after about one
+// second, or at once when another role has aborted (unless ignore_abort).
+__device__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                          bool ignore_abort = false) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 0) {
-            if (*abort_flag) return false;
+            if (!ignore_abort && *abort_flag) return false;
             if (global_ns() - t0 > kWaitLimitNs) return false;
         }
     }
 }
 
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
-
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor, K-major, no swizzle: core matrices of
-// 8 rows x 16 bytes; `lbo` = byte distance between core matrices along K,
-// `sbo` = byte distance between 8-row groups.  Bits 46..48 hold the fixed
-// value 0b001 of the tcgen05 descriptor format.
+// Shared-memory matrix descriptor, K-major, no swizzle: `lbo` = byte distance
+// between core matrices along K, `sbo` = between 8-row groups; bits 46..48
+// hold the descriptor format's fixed value 0b001.
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
     uint64_t d = 0;
     d |= (uint64_t)((addr >> 4) & 0x3FFFu);
@@ -135,9 +164,9 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
     return d;
 }
 
-// Instruction descriptor of kind::f16: D fp32, A and B bf16, both K-major,
+// kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major,
 // N >> 3 at bits 17..22, M >> 4 at bits 24..28.
-__host__ __device__ constexpr uint32_t instr_desc(int M, int N) {
+__device__ __forceinline__ uint32_t instr_desc(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
            ((uint32_t)(M >> 4) << 24);
 }
@@ -173,14 +202,24 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// byte offset of (row, 8-element K chunk) in a K-major no-swizzle tile
-__device__ __forceinline__ uint32_t core_off(int row, int kc) {
-    return (uint32_t)(row >> 3) * kGroupBytes + (uint32_t)kc * kCoreBytes + (uint32_t)(row & 7) * 16u;
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
 }
 
-// 4 int8 -> 4 bf16 (exact): byte ^ 0x80 placed in the mantissa of 2^23 gives
-// 2^23 + b + 128; subtracting 2^23 + 128 is exact; the result is an integer
-// of magnitude <= 128, exactly representable in bf16.
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+// 4 int8 -> 4 bf16, exact: byte ^ 0x80 in the mantissa of 2^23 is the float
+// 2^23 + b + 128; subtracting 2^23 + 128 is exact and leaves the integer b,
+// which bf16 holds exactly (|b| <= 128).
 __device__ __forceinline__ uint2 i8x4_to_bf16x4(uint32_t w) {
     const uint32_t u = w ^ 0x80808080u;
     const float f0 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)) - 8388736.0f;
@@ -192,206 +231,178 @@ __device__ __forceinline__ uint2 i8x4_to_bf16x4(uint32_t w) {
     return make_uint2(*reinterpret_cast<uint32_t *>(&p0), *reinterpret_cast<uint32_t *>(&p1));
 }
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w)
-                 : "memory");
+__device__ __forceinline__ int unit_start(int c, const GemmParams &p) {
+    return (int)(((unsigned)c * (unsigned)p.U) / (unsigned)p.G);
 }
 
-__global__ void __launch_bounds__(kThreads, 2) gemm_i8_tc_kernel(const GemmParams p) {
+__device__ __forceinline__ int chunk_rows(int chunk, const GemmParams &p) {
+    return min(NB_CHUNK, p.B - chunk * NB_CHUNK);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) gemm_i8_tc_kernel(const GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     GemmSmem &sm = *reinterpret_cast<GemmSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int mt = blockIdx.x, ksi = blockIdx.y, chunk = blockIdx.z;
-    const int m0 = mt * BM;
-    const int b0 = chunk * NB_CHUNK;
-    const int Bc = min(NB_CHUNK, p.B - b0);
-    const int Bpad = (Bc + 7) & ~7;
-    const int N = 2 * Bpad;  // multiple of 16, <= 128
-    const int k_begin = ksi * p.k_split;
-    const int T = p.k_split / BK;
-
-    if (p.rpos != nullptr && mt == 0 && ksi == 0) {  // ring positions advance once per step
-        for (int b = tid; b < Bc; b += kThreads) {
-            int2 q = reinterpret_cast<int2 *>(p.rpos)[b0 + b];
-            q.x = (q.x + 1) % p.conv_k;
-            q.y = (q.y + 1) % (p.conv_k - 1);
-            reinterpret_cast<int2 *>(p.rpos)[b0 + b] = q;
-        }
-    }
+    const int c = blockIdx.x;
+    const int u0 = unit_start(c, p), u1 = unit_start(c + 1, p);
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&sm.full[s], kProducers);
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.conv[s], kConvThreads);
             mbar_init(&sm.empty[s], 1);
         }
-        mbar_init(&sm.done, 1);
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&sm.acc_full[a], 1);
+            mbar_init(&sm.acc_empty[a], kEpiThreads);
+        }
+        mbar_init(&sm.drain, 1);
         sm.abort_flag = 0;
-        sm.last = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 0) {  // TMEM accumulator: 128 lanes x 128 fp32 columns
+    if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(&sm.tmem_base)),
-                     "r"(128)
+                     "r"(kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem_d = sm.tmem_base;
+    const uint32_t tmem = sm.tmem_base;
     volatile int *abort_flag = &sm.abort_flag;
 
-    if (warp < 4) {
-        // ---- A producers: one weight row each, BK int8 per stage ----------
-        const int r = tid;
-        const int8_t *gw = p.W + (size_t)(m0 + r) * p.K + k_begin;
-        int4 cur[BK / 16], nxt[BK / 16];
-#pragma unroll
-        for (int i = 0; i < BK / 16; ++i) cur[i] = __ldcs(reinterpret_cast<const int4 *>(gw) + i);
-        for (int t = 0; t < T; ++t) {
-            const int st = t % STAGES;
-            if (t + 1 < T) {
-#pragma unroll
-                for (int i = 0; i < BK / 16; ++i)
-                    nxt[i] = __ldcs(reinterpret_cast<const int4 *>(gw + (size_t)(t + 1) * BK) + i);
+    if (warp == 0) {
+        // ---- bulk-copy producer ---------------------------------------------
+        if (lane == 0) {
+            int issued = 0;  // stages whose last issued copy may still be in flight
+            for (int u = u0; u < u1; ++u) {
+                const int it = u - u0, st = it % STAGES;
+                if (it >= STAGES && !mbar_wait(&sm.empty[st], ((it / STAGES) - 1) & 1, abort_flag)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                const int tile = u / p.KT, kt = u % p.KT;
+                const int chunk = tile / p.MT, mt = tile % p.MT;
+                const int N = 2 * ((chunk_rows(chunk, p) + 7) & ~7);
+                mbar_arrive_expect_tx(&sm.full[st], kATileBytes + (uint32_t)N * 128u);
+                bulk_g2s(smem_u32(sm.a8[st]), p.Wt + ((size_t)mt * p.KT + kt) * kATileBytes,
+                         kATileBytes, &sm.full[st]);
+                bulk_g2s(smem_u32(sm.b16[st]), p.xb + ((size_t)chunk * p.KT + kt) * kOpTileBytes,
+                         (uint32_t)N * 128u, &sm.full[st]);
+                issued = it + 1;
             }
-            if (t >= STAGES && !mbar_wait(&sm.empty[st], ((t / STAGES) - 1) & 1, abort_flag)) {
-                *abort_flag = 1;
-                break;
+            if (*abort_flag) {  // let every copy still in flight land before exiting
+                for (int it = max(0, issued - STAGES); it < issued; ++it)
+                    mbar_wait(&sm.full[it % STAGES], (it / STAGES) & 1, abort_flag, true);
             }
-            const uint32_t base = smem_u32(sm.a[st]);
+        }
+    } else if (warp == 1) {
+        // ---- MMA issuer -----------------------------------------------------------
+        if (lane == 0) {
+            int it = 0, seg = 0;
+            bool ok = true;
+            for (int u = u0; u < u1 && ok; ++seg) {
+                const int tile = u / p.KT;
+                const int ue = min(u1, (tile + 1) * p.KT);
+                const int chunk = tile / p.MT;
+                const int N = 2 * ((chunk_rows(chunk, p) + 7) & ~7);
+                const uint32_t idesc = instr_desc(BM, N);
+                const int a = seg & 1;
+                if (seg >= 2 && !mbar_wait(&sm.acc_empty[a], ((seg >> 1) - 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t dtm = tmem + (uint32_t)(a * 128);
+                const int useg = u;  // first unit of this segment: overwrite the accumulator
+                for (; u < ue; ++u, ++it) {
+                    const int st = it % STAGES;
+                    if (!mbar_wait(&sm.conv[st], (it / STAGES) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(sm.a16[st]), b0 = smem_u32(sm.b16[st]);
 #pragma unroll
-            for (int i = 0; i < BK / 16; ++i) {  // 16 int8 (k = 16i..16i+15) -> two core rows
-                const uint2 q0 = i8x4_to_bf16x4((uint32_t)cur[i].x);  // k + 0..3
-                const uint2 q1 = i8x4_to_bf16x4((uint32_t)cur[i].y);  // k + 4..7
-                const uint2 q2 = i8x4_to_bf16x4((uint32_t)cur[i].z);  // k + 8..11
-                const uint2 q3 = i8x4_to_bf16x4((uint32_t)cur[i].w);  // k + 12..15
-                st_shared_v4(base + core_off(r, 2 * i), make_uint4(q0.x, q0.y, q1.x, q1.y));
-                st_shared_v4(base + core_off(r, 2 * i + 1), make_uint4(q2.x, q2.y, q3.x, q3.y));
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint64_t ad = smem_desc(a0 + kk * 2 * kCoreBytes, kCoreBytes, kGroupBytes);
+                        const uint64_t bd = smem_desc(b0 + kk * 2 * kCoreBytes, kCoreBytes, kGroupBytes);
+                        mma_bf16(dtm, ad, bd, idesc, (u == useg && kk == 0) ? 0u : 1u);
+                    }
+                    mma_commit(&sm.empty[st]);
+                }
+                if (!ok) break;
+                mma_commit(&sm.acc_full[a]);
             }
-            fence_async_smem();
-            mbar_arrive(&sm.full[st]);
-#pragma unroll
-            for (int i = 0; i < BK / 16; ++i) cur[i] = nxt[i];
+            if (!ok) *abort_flag = 1;
+            mma_commit(&sm.drain);  // arrives once every MMA issued above has completed
+            mbar_wait(&sm.drain, 0, abort_flag, true);
         }
     } else if (warp < 6) {
-        // ---- B producers: x row b -> bf16 hi (row 2b) and lo (row 2b+1) ----
-        const int b = tid - 128;  // 0..63
-        const bool valid = b < Bc;
-        const bool active = b < Bpad;
-        const float *gx = p.x + (size_t)(b0 + (valid ? b : 0)) * p.K + k_begin;
-        for (int t = 0; t < T; ++t) {
-            const int st = t % STAGES;
-            float4 v[BK / 4];
-            if (valid) {
-#pragma unroll
-                for (int i = 0; i < BK / 4; ++i)
-                    v[i] = __ldcg(reinterpret_cast<const float4 *>(gx + (size_t)t * BK) + i);
-            } else {
-#pragma unroll
-                for (int i = 0; i < BK / 4; ++i) v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-            if (t >= STAGES && !mbar_wait(&sm.empty[st], ((t / STAGES) - 1) & 1, abort_flag)) {
+        // ---- int8 -> bf16 converters ------------------------------------------------
+        const int t = tid - 64;  // 0..127
+        for (int u = u0; u < u1; ++u) {
+            const int it = u - u0, st = it % STAGES;
+            if (!mbar_wait(&sm.full[st], (it / STAGES) & 1, abort_flag)) {
                 *abort_flag = 1;
                 break;
             }
-            if (active) {
-                const uint32_t base = smem_u32(sm.b[st]);
+            const uint32_t src = smem_u32(sm.a8[st]), dst = smem_u32(sm.a16[st]);
 #pragma unroll
-                for (int kc = 0; kc < BK / 8; ++kc) {
-                    const float xs[8] = {v[2 * kc].x, v[2 * kc].y, v[2 * kc].z, v[2 * kc].w,
-                                         v[2 * kc + 1].x, v[2 * kc + 1].y, v[2 * kc + 1].z,
-                                         v[2 * kc + 1].w};
-                    uint32_t hi[4], lo[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        __nv_bfloat162 h = __floats2bfloat162_rn(xs[2 * j], xs[2 * j + 1]);
-                        const float2 hf = __bfloat1622float2(h);
-                        __nv_bfloat162 l = __floats2bfloat162_rn(xs[2 * j] - hf.x, xs[2 * j + 1] - hf.y);
-                        hi[j] = *reinterpret_cast<uint32_t *>(&h);
-                        lo[j] = *reinterpret_cast<uint32_t *>(&l);
-                    }
-                    st_shared_v4(base + core_off(2 * b, kc), make_uint4(hi[0], hi[1], hi[2], hi[3]));
-                    st_shared_v4(base + core_off(2 * b + 1, kc), make_uint4(lo[0], lo[1], lo[2], lo[3]));
-                }
+            for (int i = 0; i < 4; ++i) {
+                const int q = t + 128 * i;          // 16-byte chunk of the int8 tile
+                const int row = q >> 2, kp = q & 3;  // row, 16-element part of its 64 k
+                const uint4 w = ld_shared_v4(src + (uint32_t)q * 16u);
+                const uint2 e0 = i8x4_to_bf16x4(w.x), e1 = i8x4_to_bf16x4(w.y);
+                const uint2 e2 = i8x4_to_bf16x4(w.z), e3 = i8x4_to_bf16x4(w.w);
+                const uint32_t off = (uint32_t)(row >> 3) * kGroupBytes + (uint32_t)(row & 7) * 16u;
+                st_shared_v4(dst + off + (uint32_t)(2 * kp) * kCoreBytes, make_uint4(e0.x, e0.y, e1.x, e1.y));
+                st_shared_v4(dst + off + (uint32_t)(2 * kp + 1) * kCoreBytes, make_uint4(e2.x, e2.y, e3.x, e3.y));
             }
             fence_async_smem();
-            mbar_arrive(&sm.full[st]);
+            mbar_arrive(&sm.conv[st]);
         }
-    } else if (lane == 0) {
-        // ---- MMA issuer ---------------------------------------------------------
-        const uint32_t idesc = instr_desc(BM, N);
-        for (int t = 0; t < T; ++t) {
-            const int st = t % STAGES;
-            if (!mbar_wait(&sm.full[st], (t / STAGES) & 1, abort_flag)) {
+    } else {
+        // ---- epilogue: warps 6..9 read TMEM lane quarters 2, 3, 0, 1 --------------
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const SchedView sv{p.U, p.G, p.KT, p.MT, p.max_seg};
+        int seg = 0;
+        for (int u = u0; u < u1; ++seg) {
+            const int tile = u / p.KT;
+            u = min(u1, (tile + 1) * p.KT);
+            const int chunk = tile / p.MT;
+            const int Bc = chunk_rows(chunk, p);
+            const int N = 2 * ((Bc + 7) & ~7);
+            const int a = seg & 1;
+            const int slot = c - sched_cta_of_unit(tile * p.KT, sv);
+            if (quarter == 0 && lane == 0 && u1 >= (tile + 1) * p.KT) p.nseg[tile] = slot + 1;
+            bool ok = mbar_wait(&sm.acc_full[a], (seg >> 1) & 1, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) {
                 *abort_flag = 1;
                 break;
             }
             tc_fence_after();
-            const uint32_t a0 = smem_u32(sm.a[st]), bb0 = smem_u32(sm.b[st]);
+            const uint32_t trow = tmem + (uint32_t)(a * 128) + ((uint32_t)(quarter * 32) << 16);
+            float *pslot = p.part + ((size_t)tile * p.max_seg + slot) * (NB_CHUNK * BM);
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
-                const uint64_t ad = smem_desc(a0 + kk * 2 * kCoreBytes, kCoreBytes, kGroupBytes);
-                const uint64_t bd = smem_desc(bb0 + kk * 2 * kCoreBytes, kCoreBytes, kGroupBytes);
-                mma_bf16(tmem_d, ad, bd, idesc, (t > 0 || kk > 0) ? 1u : 0u);
-            }
-            mma_commit(&sm.empty[st]);  // frees the stage once these MMAs have read it
-        }
-        mma_commit(&sm.done);  // arrives when every MMA issued above has completed
-    }
-
-    // ---- epilogue: warps 0-3 read their 32 TMEM lanes (= weight rows) --------
-    if (warp < 4) {
-        bool ok = mbar_wait(&sm.done, 0, abort_flag) && !*abort_flag;
-        ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld is warp-collective
-        tc_fence_after();
-        const int r = warp * 32 + lane;
-        const int m = m0 + r;
-        const float sc = p.s[m];
-        const uint32_t trow = tmem_d + ((uint32_t)(warp * 32) << 16);
-        if (ok) {
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                if (c * 16 < N) {  // warp-uniform
+            for (int c16 = 0; c16 < 8; ++c16) {
+                if (c16 * 16 < N) {  // warp-uniform
                     float v[16];
-                    tmem_ld16(trow + c * 16, v);
+                    tmem_ld16(trow + c16 * 16, v);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        const int b = c * 8 + j;
-                        if (b < Bc) {
-                            const float acc = v[2 * j] + v[2 * j + 1];
-                            if (p.ks == 1)
-                                p.y[(size_t)(b0 + b) * p.M + m] = sc * acc;
-                            else
-                                p.part[((size_t)ksi * p.B + b0 + b) * p.M + m] = acc;
-                        }
+                        const int b = c16 * 8 + j;
+                        if (b < Bc) pslot[b * BM + r] = v[2 * j] + v[2 * j + 1];
                     }
                 }
             }
-        } else {
-            atomicOr(p.err, 1);
-        }
-        if (p.ks > 1) {
-            __threadfence();
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            if (tid == 0) {
-                const int old = atomicAdd(&p.counters[chunk * gridDim.x + mt], 1);
-                sm.last = (old == p.ks - 1);
-            }
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            if (sm.last) {
-                __threadfence();
-                for (int b = 0; b < Bc; ++b) {
-                    float acc = 0.f;
-                    for (int k = 0; k < p.ks; ++k)
-                        acc += __ldcg(&p.part[((size_t)k * p.B + b0 + b) * p.M + m]);
-                    p.y[(size_t)(b0 + b) * p.M + m] = sc * acc;
-                }
-                if (tid == 0) p.counters[chunk * gridDim.x + mt] = 0;
-            }
+            tc_fence_before();
+            mbar_arrive(&sm.acc_empty[a]);
         }
     }
 
@@ -399,58 +410,153 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_i8_tc_kernel(const GemmParam
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_d), "r"(128)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols)
                      : "memory");
     }
+    if (tid == 0 && sm.abort_flag) atomicOr(p.err, 1);
+}
+
+// Activations fp32 [B][K] -> bf16 B-operand tiles [chunk][kt][16 KB]: rows
+// 2b (hi) and 2b+1 (lo) of sequence b; k >= K and b in [Bc, Bpad) are zero.
+__global__ void pack_b_kernel(const float *__restrict__ x, uint8_t *__restrict__ xb, int B, int K,
+                              int KT) {
+    const int kt = blockIdx.x, chunk = blockIdx.y;
+    const int Bc = min(NB_CHUNK, B - chunk * NB_CHUNK);
+    const int Bpad = (Bc + 7) & ~7;
+    uint8_t *tile = xb + ((size_t)chunk * KT + kt) * kOpTileBytes;
+    for (int idx = blockIdx.z * blockDim.x + threadIdx.x; idx < Bpad * 8; idx += blockDim.x * gridDim.z) {
+        const int b = idx >> 3, kc = idx & 7;
+        const int k0 = kt * BK + kc * 8;
+        float v[8];
+        if (b < Bc && k0 < K) {
+            const float4 *src = reinterpret_cast<const float4 *>(x + (size_t)(chunk * NB_CHUNK + b) * K + k0);
+            const float4 a0 = src[0], a1 = src[1];
+            v[0] = a0.x; v[1] = a0.y; v[2] = a0.z; v[3] = a0.w;
+            v[4] = a1.x; v[5] = a1.y; v[6] = a1.z; v[7] = a1.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = 0.f;
+        }
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+            const float2 hf = __bfloat1622float2(h);
+            __nv_bfloat162 l = __floats2bfloat162_rn(v[2 * j] - hf.x, v[2 * j + 1] - hf.y);
+            hi[j] = *reinterpret_cast<uint32_t *>(&h);
+            lo[j] = *reinterpret_cast<uint32_t *>(&l);
+        }
+        const int rh = 2 * b, rl = 2 * b + 1;
+        *reinterpret_cast<uint4 *>(tile + (rh >> 3) * kGroupBytes + kc * kCoreBytes + (rh & 7) * 16) =
+            make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(tile + (rl >> 3) * kGroupBytes + kc * kCoreBytes + (rl & 7) * 16) =
+            make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+}
+
+// y[b][m] = s[m] * (sum of the tile's segment partials, in slot order)
+// Also advances the ring positions of `rpos` (block 0), once per step.
+__global__ void splitk_reduce_kernel(const float *__restrict__ part, const int *__restrict__ nseg_tab,
+                                     const float *__restrict__ s, float *__restrict__ y,
+                                     SchedView sv, int M, int B, int32_t *__restrict__ rpos,
+                                     int conv_k) {
+    if (rpos != nullptr && blockIdx.x == 0 && blockIdx.y == 0) {
+        for (int b = threadIdx.x; b < B; b += blockDim.x) {
+            int2 q = reinterpret_cast<int2 *>(rpos)[b];
+            q.x = (q.x + 1) % conv_k;
+            q.y = (q.y + 1) % (conv_k - 1);
+            reinterpret_cast<int2 *>(rpos)[b] = q;
+        }
+    }
+    const int tile = blockIdx.x;             // chunk * MT + mt
+    const int chunk = tile / sv.MT, mt = tile % sv.MT;
+    const int Bc = min(NB_CHUNK, B - chunk * NB_CHUNK);
+    const int r = threadIdx.x & (BM - 1);
+    const int b = blockIdx.y * 2 + (threadIdx.x >> 7);
+    const int m = mt * BM + r;
+    if (m >= M || b >= Bc) return;
+    const int nseg = nseg_tab[tile];
+    const float *pt = part + (size_t)tile * sv.max_seg * (NB_CHUNK * BM) + b * BM + r;
+    float acc = 0.f;
+#pragma unroll 4
+    for (int k = 0; k < nseg; ++k) acc += __ldcg(pt + (size_t)k * (NB_CHUNK * BM));
+    y[(size_t)(chunk * NB_CHUNK + b) * M + m] = s[m] * acc;
 }
 
 }  // namespace
 
-bool tc_gemm_supported(int M, int K) { return M % BM == 0 && K % BK == 0 && K >= BK; }
-
-int tc_gemm_splits(int M, int K, int B) {
-    const int tiles = (M / BM) * ((B + NB_CHUNK - 1) / NB_CHUNK);
-    const int target = 2 * num_sms();
-    int ks = 1;
-    while (ks < 8 && tiles * ks * 2 <= target && K % (BK * ks * 2) == 0 && K / (ks * 2) >= 2 * BK)
-        ks *= 2;
-    return ks;
+GemmPlan plan_tc_gemm(int M, int K, int B) {
+    GemmPlan g;
+    // (unit counts stay far below 2^31 / num_sms for every accepted config)
+    g.MT = (M + BM - 1) / BM;
+    g.KT = (K + BK - 1) / BK;
+    g.nchunks = (B + NB_CHUNK - 1) / NB_CHUNK;
+    g.U = g.nchunks * g.MT * g.KT;
+    g.G = std::min(num_sms(), g.U);
+    // segments per tile: a tile of KT units meets at most ceil(KT / min_range) + 1 ranges
+    const int min_range = g.U / g.G;
+    g.max_seg = (g.KT + min_range - 1) / min_range + 1;
+    g.tiles = g.nchunks * g.MT;
+    return g;
 }
 
 size_t tc_gemm_smem_bytes() { return sizeof(GemmSmem) + 1024; }
 
-cudaError_t launch_gemm_i8_tc(const int8_t *W, const float *s, const float *x, float *y,
-                              float *part, int *counters, int *err, int M, int K, int B, int ks,
-                              int32_t *rpos_advance, int conv_k, cudaStream_t st) {
-    static bool attr_set = false;
+cudaError_t launch_pack_b(const float *x, uint8_t *xb, int B, int K, cudaStream_t st) {
+    const int KT = (K + BK - 1) / BK;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)KT, (unsigned)((B + NB_CHUNK - 1) / NB_CHUNK), 4);
+    cfg.blockDim = dim3(128);
+    cfg.stream = st;
+    return cudaLaunchKernelEx(&cfg, pack_b_kernel, x, xb, B, K, KT);
+}
+
+cudaError_t launch_gemm_i8_tc(const uint8_t *Wt, const uint8_t *xb, float *part, int *nseg, int *err,
+                              int M, int K, int B, cudaStream_t st) {
+    static int attr_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
     const size_t smem = tc_gemm_smem_bytes();
-    if (!attr_set) {
+    if (attr_dev != dev) {
         cudaError_t e = cudaFuncSetAttribute(gemm_i8_tc_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        attr_dev = dev;
     }
+    const GemmPlan g = plan_tc_gemm(M, K, B);
     GemmParams p;
-    p.W = W;
-    p.s = s;
-    p.x = x;
-    p.y = y;
+    p.Wt = Wt;
+    p.xb = xb;
     p.part = part;
-    p.counters = counters;
-    p.rpos = rpos_advance;
+    p.nseg = nseg;
     p.err = err;
     p.M = M;
-    p.K = K;
+    p.MT = g.MT;
+    p.KT = g.KT;
     p.B = B;
-    p.ks = ks;
-    p.k_split = K / ks;
-    p.conv_k = conv_k;
+    p.nchunks = g.nchunks;
+    p.U = g.U;
+    p.G = g.G;
+    p.max_seg = g.max_seg;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(M / BM), (unsigned)ks, (unsigned)((B + NB_CHUNK - 1) / NB_CHUNK));
+    cfg.gridDim = dim3((unsigned)g.G);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     return cudaLaunchKernelEx(&cfg, gemm_i8_tc_kernel, p);
+}
+
+cudaError_t launch_splitk_reduce(const float *part, const int *nseg, const float *s, float *y, int M,
+                                 int K, int B, int32_t *rpos_advance, int conv_k, cudaStream_t st) {
+    const GemmPlan g = plan_tc_gemm(M, K, B);
+    const SchedView sv{g.U, g.G, g.KT, g.MT, g.max_seg};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)g.tiles, (unsigned)((std::min(B, NB_CHUNK) + 1) / 2));
+    cfg.blockDim = dim3(2 * BM);
+    cfg.stream = st;
+    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, part, nseg, s, y, sv, M, B, rpos_advance,
+                              conv_k);
 }
 
 }  // namespace dn

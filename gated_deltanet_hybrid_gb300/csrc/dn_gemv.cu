@@ -1,41 +1,99 @@
-// int8 row-scaled GEMV on CUDA cores: y[b][o] = s[o] * sum_k W[o][k] * x[b][k].
+// int8 row-scaled GEMV on the CUDA cores for small batches:
+//   y[b][o] = s[o] * sum_k W[o][k] * x[b][k]
 //
 // The projections of the gated-DeltaNet step are int8 matrices with one fp32
 // scale per output row (page "feat(qwen36): the dense trunk places itself",
 // section "What this adds", item 1; the fused in_proj is "qkv ++ z, one GEMV
-// instead of two").  At small batch the step is a pure weight stream, so the
-// kernel is built around the HBM read of W: one warp per output row, 16-byte
-// loads of 16 int8 weights per lane (a warp covers 512 consecutive bytes of a
-// row per iteration), all of a lane's loads for a row issued before any use,
-// and a fixed xor-shuffle reduction order (bitwise-reproducible results).
-// Each weight is converted once and used for every batch column of the
-// chunk, so W is read from memory once per chunk of NB sequences.
+// instead of two").  At small batch the step is a weight stream: the kernel
+// is built so that every SM keeps about 128 KB of weights in flight.
+//
+// W is stored as contiguous 8 KB tiles of 128 rows x 64 int8 (shared with the
+// tensor-core kernel) and the work is split exactly like the tensor-core
+// projection (stream-K, dn_sched.cuh): one CTA per SM takes a contiguous
+// range of (row tile, k tile) units.  Warp 0 streams the CTA's tiles with
+// 1-D bulk copies (cp.async.bulk) into a 16-deep shared-memory ring; eight
+// compute warps read each tile from shared memory (16 contiguous bytes per
+// lane), convert int8 exactly to fp32 and multiply with the fp32 activations
+// (read through L1), one accumulator per (row, sequence).  At the end of each
+// segment the four lanes of a row are combined in a fixed shuffle order and
+// the unscaled partial goes to its slot, to be summed and scaled by the
+// consumer in slot order (bitwise-reproducible results).
+//
+// Every wait is bounded (about one second of the global timer); on timeout
+// the kernel records an error in `err`, lets its copies land and returns.
+#include <algorithm>
+
 #include "dn_internal.cuh"
+#include "dn_sched.cuh"
 
 namespace dn {
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int NSTAGE = 16;
+constexpr int kCompute = 256;            // compute threads (warps 1..8)
+constexpr int kThreads = 32 + kCompute;  // + producer warp
+constexpr uint32_t kTile = kTileM * kTileK;  // 8 KB
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
-// Exact int8 -> fp32 for the four bytes of a 32-bit word.  Byte b of the
-// word, taken as unsigned u = b ^ 0x80 (= b + 128), is placed in the low
-// mantissa bits of 2^23 (bit pattern 0x4B000000 | u, the float 8388608 + u);
-// subtracting 8388608 + 128 is exact and leaves b.  (IEEE-754 binary32: any
-// integer below 2^24 is exact, and at exponent 2^23 one mantissa unit is 1.)
-__device__ __forceinline__ void i8x4_to_f32(uint32_t w, float &f0, float &f1, float &f2,
-                                            float &f3) {
-    const uint32_t u = w ^ 0x80808080u;
-    f0 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)) - 8388736.0f;
-    f1 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651)) - 8388736.0f;
-    f2 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652)) - 8388736.0f;
-    f3 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653)) - 8388736.0f;
+struct __align__(128) GemvSmem {
+    uint8_t tile[NSTAGE][kTile];
+    uint64_t full[NSTAGE];
+    uint64_t empty[NSTAGE];
+    int abort_flag;
+};
+
+struct GemvParams {
+    const uint8_t *Wt;
+    const float *x;   // [B][K]
+    float *part;      // [tiles][max_seg][64][128]
+    int *nseg;        // [tiles]
+    int *err;
+    SchedView sv;
+    int K, B;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                          bool ignore_abort = false) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (!ignore_abort && *abort_flag) return false;
+            if (global_ns() - t0 > kWaitLimitNs) return false;
+        }
+    }
 }
 
-__device__ __forceinline__ void unpack16(const int4 v, float f[16]) {
-    i8x4_to_f32((uint32_t)v.x, f[0], f[1], f[2], f[3]);
-    i8x4_to_f32((uint32_t)v.y, f[4], f[5], f[6], f[7]);
-    i8x4_to_f32((uint32_t)v.z, f[8], f[9], f[10], f[11]);
-    i8x4_to_f32((uint32_t)v.w, f[12], f[13], f[14], f[15]);
+// Exact int8 -> fp32 for the four bytes of a 32-bit word: byte b taken as
+// u = b ^ 0x80 (= b + 128) is placed in the mantissa of 2^23 (bit pattern
+// 0x4B000000 | u, the float 8388608 + u); subtracting 8388608 + 128 is exact
+// and leaves b (binary32 holds every integer below 2^24 exactly).
+__device__ __forceinline__ void i8x4_to_f32(uint32_t w, float *f) {
+    const uint32_t u = w ^ 0x80808080u;
+    f[0] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)) - 8388736.0f;
+    f[1] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651)) - 8388736.0f;
+    f[2] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652)) - 8388736.0f;
+    f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653)) - 8388736.0f;
 }
 
 __device__ __forceinline__ float dot16(const float w[16], const float *xp) {
@@ -62,92 +120,174 @@ __device__ __forceinline__ float dot16(const float w[16], const float *xp) {
     return t;
 }
 
-// One warp per output row.  Weights of the row are streamed UNROLL 16-byte
-// chunks per lane at a time (loads first, then math).  NB batch columns share
-// each converted weight.
-template <int NB, int UNROLL>
-__global__ void __launch_bounds__(kWarps * 32)
-gemv_i8_kernel(const int8_t *__restrict__ W, const float *__restrict__ s,
-               const float *__restrict__ x, float *__restrict__ y, int M, int K, int B,
-               int32_t *__restrict__ rpos, int conv_k) {
-    if (rpos != nullptr && blockIdx.x == 0) {
-        // ring positions advance once per step, after the core kernel read them
-        for (int b = threadIdx.x; b < B; b += blockDim.x) {
-            int2 p = reinterpret_cast<int2 *>(rpos)[b];
-            p.x = (p.x + 1) % conv_k;
-            p.y = (p.y + 1) % (conv_k - 1);
-            reinterpret_cast<int2 *>(rpos)[b] = p;
+template <int NB>
+__global__ void __launch_bounds__(kThreads, 1) gemv_i8_stream_kernel(const GemvParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    GemvSmem &sm = *reinterpret_cast<GemvSmem *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int c = blockIdx.x;
+    const int u0 = sched_unit_start(c, p.sv), u1 = sched_unit_start(c + 1, p.sv);
+    const int KT = p.sv.KT;
+    if (tid == 0) {
+        for (int s = 0; s < NSTAGE; ++s) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&sm.full[s])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&sm.empty[s])),
+                         "r"(kCompute));
         }
+        sm.abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int stride_rows = gridDim.x * kWarps;
-    for (int row = blockIdx.x * kWarps + warp; row < M; row += stride_rows) {
-        const int8_t *wr = W + (size_t)row * K;
-        const float sc = s[row];
-        for (int b0 = 0; b0 < B; b0 += NB) {
-            float acc[NB];
-#pragma unroll
-            for (int j = 0; j < NB; ++j) acc[j] = 0.f;
-            for (int kb = 0; kb < K; kb += 512 * UNROLL) {
-                int4 wv[UNROLL];
-#pragma unroll
-                for (int u = 0; u < UNROLL; ++u) {
-                    const int k0 = kb + u * 512 + lane * 16;
-                    wv[u] = (k0 < K) ? __ldcs(reinterpret_cast<const int4 *>(wr + k0))
-                                     : make_int4(0, 0, 0, 0);
+    __syncthreads();
+    volatile int *abort_flag = &sm.abort_flag;
+
+    if (warp == 0) {
+        if (tid == 0) {  // ---- producer: bulk copies of the weight tiles ----
+            int issued = 0;
+            for (int u = u0; u < u1; ++u) {
+                const int it = u - u0, st = it % NSTAGE;
+                if (it >= NSTAGE && !mbar_wait(&sm.empty[st], ((it / NSTAGE) - 1) & 1, abort_flag)) {
+                    *abort_flag = 1;
+                    break;
                 }
+                const int tile = u / KT, kt = u % KT;
+                const int mt = tile % p.sv.MT;
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+                                 smem_u32(&sm.full[st])),
+                             "r"(kTile)
+                             : "memory");
+                asm volatile(
+                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                        smem_u32(sm.tile[st])),
+                    "l"(p.Wt + ((size_t)mt * KT + kt) * kTile), "r"(kTile), "r"(smem_u32(&sm.full[st]))
+                    : "memory");
+                issued = it + 1;
+            }
+            if (*abort_flag) {
+                for (int it = issued > NSTAGE ? issued - NSTAGE : 0; it < issued; ++it)
+                    mbar_wait(&sm.full[it % NSTAGE], (it / NSTAGE) & 1, abort_flag, true);
+            }
+        }
+    } else {
+        // ---- compute: thread t takes 16-byte chunks t and t + 256 of each tile:
+        //      rows t/4 and t/4 + 64, k part t % 4 (16 of the tile's 64 k) --------
+        const int t = tid - 32;
+        const int lane = t & 31;
+        const int kp = t & 3;
+        const int ra = t >> 2, rb = ra + 64;
+        float acc[2][NB];
+        int tile_cur = -1;
+        for (int u = u0; u <= u1; ++u) {
+            const int tile = u < u1 ? u / KT : -2;
+            if (tile != tile_cur && tile_cur >= 0) {
+                // end of a segment: combine the 4 lanes of each row, write the partial
 #pragma unroll
-                for (int u = 0; u < UNROLL; ++u) {
-                    const int k0 = kb + u * 512 + lane * 16;
-                    if (k0 < K) {
-                        float wf[16];
-                        unpack16(wv[u], wf);
+                for (int h = 0; h < 2; ++h)
 #pragma unroll
-                        for (int j = 0; j < NB; ++j)
-                            if (b0 + j < B) acc[j] += dot16(wf, x + (size_t)(b0 + j) * K + k0);
+                    for (int j = 0; j < NB; ++j) {
+                        float v = acc[h][j];
+                        v += __shfl_xor_sync(0xffffffffu, v, 1);
+                        v += __shfl_xor_sync(0xffffffffu, v, 2);
+                        acc[h][j] = v;
+                    }
+                const int slot = c - sched_cta_of_unit(tile_cur * KT, p.sv);
+                if (t == 0 && u1 >= (tile_cur + 1) * KT) p.nseg[tile_cur] = slot + 1;
+                if (kp == 0) {
+                    float *ps = p.part + ((size_t)tile_cur * p.sv.max_seg + slot) * (64 * 128);
+#pragma unroll
+                    for (int j = 0; j < NB; ++j)
+                        if (j < p.B) {
+                            ps[j * 128 + ra] = acc[0][j];
+                            ps[j * 128 + rb] = acc[1][j];
+                        }
+                }
+            }
+            if (u == u1) break;
+            if (tile != tile_cur) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int j = 0; j < NB; ++j) acc[h][j] = 0.f;
+                tile_cur = tile;
+            }
+            const int it = u - u0, st = it % NSTAGE;
+            bool ok = mbar_wait(&sm.full[st], (it / NSTAGE) & 1, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) {
+                *abort_flag = 1;
+                break;
+            }
+            const int kt = u % KT;
+            const int k0 = kt * kTileK + kp * 16;
+            const uint4 wa = *reinterpret_cast<const uint4 *>(sm.tile[st] + t * 16);
+            const uint4 wb = *reinterpret_cast<const uint4 *>(sm.tile[st] + (t + kCompute) * 16);
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&sm.empty[st]))
+                         : "memory");
+            if (k0 < p.K) {
+                float fa[16], fb[16];
+                i8x4_to_f32(wa.x, fa);
+                i8x4_to_f32(wa.y, fa + 4);
+                i8x4_to_f32(wa.z, fa + 8);
+                i8x4_to_f32(wa.w, fa + 12);
+                i8x4_to_f32(wb.x, fb);
+                i8x4_to_f32(wb.y, fb + 4);
+                i8x4_to_f32(wb.z, fb + 8);
+                i8x4_to_f32(wb.w, fb + 12);
+#pragma unroll
+                for (int j = 0; j < NB; ++j) {
+                    if (j < p.B) {
+                        const float *xp = p.x + (size_t)j * p.K + k0;
+                        acc[0][j] += dot16(fa, xp);
+                        acc[1][j] += dot16(fb, xp);
                     }
                 }
             }
-#pragma unroll
-            for (int j = 0; j < NB; ++j) {
-                float v = acc[j];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                acc[j] = v;
-            }
-            if (lane == 0) {
-#pragma unroll
-                for (int j = 0; j < NB; ++j)
-                    if (b0 + j < B) y[(size_t)(b0 + j) * M + row] = sc * acc[j];
-            }
         }
+        (void)lane;
     }
+    __syncthreads();
+    if (tid == 0 && sm.abort_flag) atomicOr(p.err, 1);
 }
 
-template <int NB, int UNROLL>
-cudaError_t launch_nb(const int8_t *W, const float *s, const float *x, float *y, int M, int K,
-                      int B, int32_t *rpos, int conv_k, cudaStream_t st) {
+template <int NB>
+cudaError_t launch_nb(const uint8_t *Wt, const float *x, float *part, int *nseg, int *err, int M,
+                      int K, int B, cudaStream_t st) {
+    static int attr_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const size_t smem = sizeof(GemvSmem) + 128;
+    if (attr_dev != dev) {
+        cudaError_t e = cudaFuncSetAttribute(gemv_i8_stream_kernel<NB>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr_dev = dev;
+    }
+    const GemmPlan g = plan_tc_gemm(M, K, B);
+    GemvParams p;
+    p.Wt = Wt;
+    p.x = x;
+    p.part = part;
+    p.nseg = nseg;
+    p.err = err;
+    p.sv = SchedView{g.U, g.G, g.KT, g.MT, g.max_seg};
+    p.K = K;
+    p.B = B;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((M + kWarps - 1) / kWarps));
-    cfg.blockDim = dim3(kWarps * 32);
-    cfg.dynamicSmemBytes = 0;
+    cfg.gridDim = dim3((unsigned)g.G);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    return cudaLaunchKernelEx(&cfg, gemv_i8_kernel<NB, UNROLL>, W, s, x, y, M, K, B, rpos,
-                              conv_k);
+    return cudaLaunchKernelEx(&cfg, gemv_i8_stream_kernel<NB>, p);
 }
 
 }  // namespace
 
-cudaError_t launch_gemv_i8(const int8_t *W, const float *s, const float *x, float *y, int M,
-                           int K, int B, int32_t *rpos_advance, int conv_k, cudaStream_t st) {
-    // unroll so that one lane's loads of a row are in flight together
-    if (B == 1) {
-        if (K >= 2048) return launch_nb<1, 4>(W, s, x, y, M, K, B, rpos_advance, conv_k, st);
-        return launch_nb<1, 1>(W, s, x, y, M, K, B, rpos_advance, conv_k, st);
-    }
-    if (B == 2) return launch_nb<2, 2>(W, s, x, y, M, K, B, rpos_advance, conv_k, st);
-    if (B <= 4) return launch_nb<4, 2>(W, s, x, y, M, K, B, rpos_advance, conv_k, st);
-    return launch_nb<8, 1>(W, s, x, y, M, K, B, rpos_advance, conv_k, st);
+cudaError_t launch_gemv_i8(const uint8_t *Wt, const float *x, float *part, int *nseg, int *err,
+                           int M, int K, int B, cudaStream_t st) {
+    if (B == 1) return launch_nb<1>(Wt, x, part, nseg, err, M, K, B, st);
+    if (B == 2) return launch_nb<2>(Wt, x, part, nseg, err, M, K, B, st);
+    if (B <= 4) return launch_nb<4>(Wt, x, part, nseg, err, M, K, B, st);
+    return launch_nb<8>(Wt, x, part, nseg, err, M, K, B, st);
 }
 
 }  // namespace dn

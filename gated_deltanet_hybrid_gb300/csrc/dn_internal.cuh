@@ -23,7 +23,6 @@ namespace dn {
 //                                             step reads
 //   rpos    i32  [max_batch][2]              {slot of the oldest input in `ring`,
 //                                             ring_pos as seen through the ABI}
-//   qkvz    f32  [max_batch][in_rows]        in_proj output (scratch)
 //   nrm     f32  [max_batch][v_dim]          gated-RMSNorm output (scratch)
 struct Dims {
     int hidden, n_qk, n_v, dk, dv, conv_k, max_batch;
@@ -32,39 +31,67 @@ struct Dims {
 };
 
 struct LayerDev {
-    int8_t *w_in;
+    uint8_t *w_in;  // tiled int8 (see kTileM / kTileK)
     float *s_in, *wconv_t, *w_norm;
-    int8_t *w_out;
+    uint8_t *w_out;  // tiled int8
     float *s_out;
     float *S, *ring;
     int32_t *rpos;
-    float *qkvz, *nrm;
+    float *nrm;
     // staging used by dn_step with host pointers and by the state copies
     float *x_stage, *g_stage, *beta_stage, *out_stage;
     float *ring_stage;     // [max_batch][conv_k-1][conv_ch]
     int32_t *rp_stage;     // [max_batch]
     // tensor-core projections: split-K partials, per-tile arrival counters
     float *part_in, *part_out;
-    int *cnt_in, *cnt_out;
+    int *nseg_in, *nseg_out;  // segments per tile of the last projection launch
+    uint8_t *xb_in;        // packed B-operand tiles of x   [chunks][KT_in][16 KB]
+    uint8_t *xb_out;       // packed B-operand tiles of the gated-norm output [chunks][KT_out][16 KB]
     int *err;              // device-side error word (bounded waits that gave up)
 };
 
-// y[b][o] = s[o] * sum_k W[o][k] * x[b][k] for b < B.  Optionally advances
-// the per-sequence ring positions of `rpos` for b < B (done by block 0).
-cudaError_t launch_gemv_i8(const int8_t *W, const float *s, const float *x, float *y, int M,
-                           int K, int B, int32_t *rpos_advance, int conv_k, cudaStream_t st);
+// Weight tiles used by every projection kernel: W [M][K] int8 is stored as
+// [ceil(M/128)][ceil(K/64)][128 rows][64 int8], zero-padded, one 8 KB
+// contiguous block per (m tile, k tile).
+constexpr int kTileM = 128;
+constexpr int kTileK = 64;
 
-// Tensor-core (tcgen05) version of the same projection for batches >= 8.
-bool tc_gemm_supported(int M, int K);
-int tc_gemm_splits(int M, int K, int B);
-cudaError_t launch_gemm_i8_tc(const int8_t *W, const float *s, const float *x, float *y,
-                              float *part, int *counters, int *err, int M, int K, int B, int ks,
-                              int32_t *rpos_advance, int conv_k, cudaStream_t st);
+// Both projection kernels leave unscaled per-segment partial sums of their
+// stream-K schedule (dn_sched.cuh) in `part`; the consumer sums a tile's
+// slots in slot order and applies the row scale: the core kernel for the
+// in_proj, launch_splitk_reduce for the out_proj.
+//
+// CUDA-core version for batches < kTcMinBatch (fp32 activations x [B][K]).
+cudaError_t launch_gemv_i8(const uint8_t *Wt, const float *x, float *part, int *nseg, int *err,
+                           int M, int K, int B, cudaStream_t st);
+
+// Tensor-core (tcgen05) version for batches >= kTcMinBatch: x arrives packed
+// as bf16 hi/lo B-operand tiles (launch_pack_b, or written so by the core
+// kernel).
+struct GemmPlan {
+    int MT, KT, nchunks, U, G, max_seg, tiles;
+};
+GemmPlan plan_tc_gemm(int M, int K, int B);
+cudaError_t launch_pack_b(const float *x, uint8_t *xb, int B, int K, cudaStream_t st);
+cudaError_t launch_gemm_i8_tc(const uint8_t *Wt, const uint8_t *xb, float *part, int *nseg, int *err,
+                              int M, int K, int B, cudaStream_t st);
+// y = s * (sum of partials); also advances ring positions (rpos_advance != NULL)
+cudaError_t launch_splitk_reduce(const float *part, const int *nseg, const float *s, float *y, int M,
+                                 int K, int B, int32_t *rpos_advance, int conv_k, cudaStream_t st);
 constexpr int kTcMinBatch = 8;
+constexpr size_t kOpTile = 16384;  // bytes of one packed B-operand tile (64 seqs x 64 k, hi+lo)
 
 // The fused conv / L2 / gated-delta / readout / gated-RMSNorm step.
+// The in_proj result is read as the sum of its segment partials (part_in,
+// scaled by s_in).  tc: the gated-norm output is written as packed B-operand
+// tiles (xb_out) for the tensor-core out_proj instead of fp32 rows (nrm).
 cudaError_t launch_dn_core(const Dims &d, const LayerDev &L, int B, const float *g,
-                           const float *beta, cudaStream_t st);
+                           const float *beta, bool tc, cudaStream_t st);
+
+// Persistent bulk-copy-pipelined variant for large batches of 128 x 128 heads.
+bool dn_core_stream_ok(const Dims &d, int B);
+cudaError_t launch_dn_core_stream(const Dims &d, const LayerDev &L, int B, const float *g,
+                                  const float *beta, bool tc, cudaStream_t st);
 
 // ring conversion between the ABI's conv_k-1 slots and the device's conv_k slots
 cudaError_t launch_ring_import(const Dims &d, const LayerDev &L, int seq0, int n,
