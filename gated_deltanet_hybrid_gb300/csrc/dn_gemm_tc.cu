@@ -29,8 +29,11 @@
 // core kernel for the in_proj, splitk_reduce_kernel for the out_proj), so
 // results do not depend on scheduling and no CTA waits on another.
 //
-// Roles: warp 0 issues the bulk copies, warp 1 (one thread) the MMAs, warps
-// 2-5 convert the int8 tile to bf16 in shared memory, warps 6-9 read the
+// A pipeline stage is 128 rows x 128 k (16 KB of int8 weights, one bulk copy:
+// copies this size keep the per-stage hand-off cost small against the HBM
+// time).  Roles: warp 0 issues the bulk copies, warp 1 (one thread) the
+// MMAs, warps 2-5 convert the int8 unit to bf16 in a double-buffered shared
+// operand, warps 6-9 read the
 // accumulators (tcgen05.ld) and write results.  Every wait is bounded (about
 // one second of the global timer): on timeout the kernel records an error in
 // `err`, waits (bounded) for its own copies and MMAs in flight, frees its
@@ -46,8 +49,9 @@ namespace dn {
 namespace {
 
 constexpr int BM = 128;          // weight rows per tile (MMA M)
-constexpr int BK = 64;           // K per unit / pipeline stage
-constexpr int STAGES = 4;
+constexpr int BK = 64;           // k per weight tile
+constexpr int KU = 2;            // k tiles per unit / pipeline stage (128 k)
+constexpr int STAGES = 3;
 constexpr int NB_CHUNK = 64;     // sequences per batch chunk (MMA N <= 128)
 constexpr int kThreads = 320;    // 10 warps
 constexpr int kConvThreads = 128;
@@ -59,13 +63,16 @@ constexpr uint32_t kGroupBytes = (BK / 8) * 128;     // 1024
 constexpr uint32_t kTmemCols = 256;                  // two 128-column accumulators
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
+// A unit (= pipeline stage) is 128 rows x 128 k: two 64-k halves, each laid
+// out like one 64-k tile (core-matrix groups 1024 bytes apart).
 struct __align__(1024) GemmSmem {
-    uint8_t a16[STAGES][kOpTileBytes];  // bf16 A operand
-    uint8_t b16[STAGES][kOpTileBytes];  // bf16 B operand (as copied)
-    uint8_t a8[STAGES][kATileBytes];    // int8 A tile (as copied)
-    uint64_t full[STAGES];              // bulk copies of the stage landed
-    uint64_t conv[STAGES];              // A converted to bf16
-    uint64_t empty[STAGES];             // MMAs done reading the stage
+    uint8_t a16[2][KU * kOpTileBytes];       // bf16 A operand, double-buffered (2 x 32 KB)
+    uint8_t b16[STAGES][KU * kOpTileBytes];  // bf16 B operand as copied (3 x 32 KB)
+    uint8_t a8[STAGES][KU * kATileBytes];    // int8 A as copied (3 x 16 KB)
+    uint64_t full[STAGES];                   // bulk copies of the stage landed
+    uint64_t empty[STAGES];                  // MMAs done reading the stage
+    uint64_t conv[2];                        // A converted to bf16 (per a16 buffer)
+    uint64_t a16_free[2];                    // MMAs done reading the a16 buffer
     uint64_t acc_full[2];               // accumulator ready for the epilogue
     uint64_t acc_empty[2];              // epilogue done reading the accumulator
     uint64_t drain;                     // all MMAs of this CTA completed
@@ -79,7 +86,7 @@ struct GemmParams {
     float *part;         // [tiles][max_seg][64][128] segment partials (unscaled)
     int *nseg;           // [tiles] segment count, written by each tile's last segment
     int *err;
-    int M, MT, KT, B, nchunks, U, G, max_seg;
+    int M, MT, KT, UT, B, nchunks, U, G, max_seg;  // KT: k tiles; UT: units per row tile
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -250,8 +257,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_i8_tc_kernel(const GemmParam
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.conv[s], kConvThreads);
             mbar_init(&sm.empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&sm.conv[a], kConvThreads);
+            mbar_init(&sm.a16_free[a], 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&sm.acc_full[a], 1);
@@ -284,14 +294,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_i8_tc_kernel(const GemmParam
                     *abort_flag = 1;
                     break;
                 }
-                const int tile = u / p.KT, kt = u % p.KT;
+                const int tile = u / p.UT, kt0 = (u % p.UT) * KU;
                 const int chunk = tile / p.MT, mt = tile % p.MT;
+                const int nk = min(KU, p.KT - kt0);
                 const int N = 2 * ((chunk_rows(chunk, p) + 7) & ~7);
-                mbar_arrive_expect_tx(&sm.full[st], kATileBytes + (uint32_t)N * 128u);
-                bulk_g2s(smem_u32(sm.a8[st]), p.Wt + ((size_t)mt * p.KT + kt) * kATileBytes,
-                         kATileBytes, &sm.full[st]);
-                bulk_g2s(smem_u32(sm.b16[st]), p.xb + ((size_t)chunk * p.KT + kt) * kOpTileBytes,
-                         (uint32_t)N * 128u, &sm.full[st]);
+                mbar_arrive_expect_tx(&sm.full[st], (uint32_t)nk * (kATileBytes + (uint32_t)N * 128u));
+                bulk_g2s(smem_u32(sm.a8[st]), p.Wt + ((size_t)mt * p.KT + kt0) * kATileBytes,
+                         (uint32_t)nk * kATileBytes, &sm.full[st]);
+                for (int i = 0; i < nk; ++i)
+                    bulk_g2s(smem_u32(sm.b16[st]) + (uint32_t)i * kOpTileBytes,
+                             p.xb + ((size_t)chunk * p.KT + kt0 + i) * kOpTileBytes, (uint32_t)N * 128u,
+                             &sm.full[st]);
                 issued = it + 1;
             }
             if (*abort_flag) {  // let every copy still in flight land before exiting
@@ -305,8 +318,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_i8_tc_kernel(const GemmParam
             int it = 0, seg = 0;
             bool ok = true;
             for (int u = u0; u < u1 && ok; ++seg) {
-                const int tile = u / p.KT;
-                const int ue = min(u1, (tile + 1) * p.KT);
+                const int tile = u / p.UT;
+                const int ue = min(u1, (tile + 1) * p.UT);
                 const int chunk = tile / p.MT;
                 const int N = 2 * ((chunk_rows(chunk, p) + 7) & ~7);
                 const uint32_t idesc = instr_desc(BM, N);
@@ -319,20 +332,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_i8_tc_kernel(const GemmParam
                 const uint32_t dtm = tmem + (uint32_t)(a * 128);
                 const int useg = u;  // first unit of this segment: overwrite the accumulator
                 for (; u < ue; ++u, ++it) {
-                    const int st = it % STAGES;
-                    if (!mbar_wait(&sm.conv[st], (it / STAGES) & 1, abort_flag)) {
+                    const int st = it % STAGES, ab = it & 1;
+                    if (!mbar_wait(&sm.conv[ab], (it >> 1) & 1, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(sm.a16[st]), b0 = smem_u32(sm.b16[st]);
-#pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t ad = smem_desc(a0 + kk * 2 * kCoreBytes, kCoreBytes, kGroupBytes);
-                        const uint64_t bd = smem_desc(b0 + kk * 2 * kCoreBytes, kCoreBytes, kGroupBytes);
+                    const int nk = min(KU, p.KT - (u % p.UT) * KU);
+                    const uint32_t a0 = smem_u32(sm.a16[ab]), b0 = smem_u32(sm.b16[st]);
+                    for (int kk = 0; kk < nk * (BK / 16); ++kk) {
+                        const uint32_t off = (uint32_t)(kk >> 2) * kOpTileBytes + (uint32_t)(kk & 3) * 2 * kCoreBytes;
+                        const uint64_t ad = smem_desc(a0 + off, kCoreBytes, kGroupBytes);
+                        const uint64_t bd = smem_desc(b0 + off, kCoreBytes, kGroupBytes);
                         mma_bf16(dtm, ad, bd, idesc, (u == useg && kk == 0) ? 0u : 1u);
                     }
                     mma_commit(&sm.empty[st]);
+                    mma_commit(&sm.a16_free[ab]);
                 }
                 if (!ok) break;
                 mma_commit(&sm.acc_full[a]);
@@ -345,41 +360,47 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_i8_tc_kernel(const GemmParam
         // ---- int8 -> bf16 converters ------------------------------------------------
         const int t = tid - 64;  // 0..127
         for (int u = u0; u < u1; ++u) {
-            const int it = u - u0, st = it % STAGES;
-            if (!mbar_wait(&sm.full[st], (it / STAGES) & 1, abort_flag)) {
+            const int it = u - u0, st = it % STAGES, ab = it & 1;
+            if (!mbar_wait(&sm.full[st], (it / STAGES) & 1, abort_flag) ||
+                (it >= 2 && !mbar_wait(&sm.a16_free[ab], ((it >> 1) - 1) & 1, abort_flag))) {
                 *abort_flag = 1;
                 break;
             }
-            const uint32_t src = smem_u32(sm.a8[st]), dst = smem_u32(sm.a16[st]);
+            const int nk = min(KU, p.KT - (u % p.UT) * KU);
+            const uint32_t src = smem_u32(sm.a8[st]), dst = smem_u32(sm.a16[ab]);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int q = t + 128 * i;          // 16-byte chunk of the int8 tile
-                const int row = q >> 2, kp = q & 3;  // row, 16-element part of its 64 k
-                const uint4 w = ld_shared_v4(src + (uint32_t)q * 16u);
-                const uint2 e0 = i8x4_to_bf16x4(w.x), e1 = i8x4_to_bf16x4(w.y);
-                const uint2 e2 = i8x4_to_bf16x4(w.z), e3 = i8x4_to_bf16x4(w.w);
-                const uint32_t off = (uint32_t)(row >> 3) * kGroupBytes + (uint32_t)(row & 7) * 16u;
-                st_shared_v4(dst + off + (uint32_t)(2 * kp) * kCoreBytes, make_uint4(e0.x, e0.y, e1.x, e1.y));
-                st_shared_v4(dst + off + (uint32_t)(2 * kp + 1) * kCoreBytes, make_uint4(e2.x, e2.y, e3.x, e3.y));
+            for (int i = 0; i < 4 * KU; ++i) {
+                const int q = t + 128 * i;  // 16-byte chunk of the int8 unit
+                if (q < nk * 512) {
+                    const int half = q >> 9, qq = q & 511;
+                    const int row = qq >> 2, kp = qq & 3;  // row, 16-element part of its 64 k
+                    const uint4 w = ld_shared_v4(src + (uint32_t)q * 16u);
+                    const uint2 e0 = i8x4_to_bf16x4(w.x), e1 = i8x4_to_bf16x4(w.y);
+                    const uint2 e2 = i8x4_to_bf16x4(w.z), e3 = i8x4_to_bf16x4(w.w);
+                    const uint32_t off = (uint32_t)half * kOpTileBytes + (uint32_t)(row >> 3) * kGroupBytes +
+                                         (uint32_t)(row & 7) * 16u;
+                    st_shared_v4(dst + off + (uint32_t)(2 * kp) * kCoreBytes, make_uint4(e0.x, e0.y, e1.x, e1.y));
+                    st_shared_v4(dst + off + (uint32_t)(2 * kp + 1) * kCoreBytes, make_uint4(e2.x, e2.y, e3.x, e3.y));
+                }
             }
             fence_async_smem();
-            mbar_arrive(&sm.conv[st]);
+            mbar_arrive(&sm.conv[ab]);
         }
     } else {
         // ---- epilogue: warps 6..9 read TMEM lane quarters 2, 3, 0, 1 --------------
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;
-        const SchedView sv{p.U, p.G, p.KT, p.MT, p.max_seg};
+        const SchedView sv{p.U, p.G, p.UT, p.MT, p.max_seg};
         int seg = 0;
         for (int u = u0; u < u1; ++seg) {
-            const int tile = u / p.KT;
-            u = min(u1, (tile + 1) * p.KT);
+            const int tile = u / p.UT;
+            u = min(u1, (tile + 1) * p.UT);
             const int chunk = tile / p.MT;
             const int Bc = chunk_rows(chunk, p);
             const int N = 2 * ((Bc + 7) & ~7);
             const int a = seg & 1;
-            const int slot = c - sched_cta_of_unit(tile * p.KT, sv);
-            if (quarter == 0 && lane == 0 && u1 >= (tile + 1) * p.KT) p.nseg[tile] = slot + 1;
+            const int slot = c - sched_cta_of_unit(tile * p.UT, sv);
+            if (quarter == 0 && lane == 0 && u1 >= (tile + 1) * p.UT) p.nseg[tile] = slot + 1;
             bool ok = mbar_wait(&sm.acc_full[a], (seg >> 1) & 1, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
@@ -490,13 +511,15 @@ GemmPlan plan_tc_gemm(int M, int K, int B) {
     GemmPlan g;
     // (unit counts stay far below 2^31 / num_sms for every accepted config)
     g.MT = (M + BM - 1) / BM;
-    g.KT = (K + BK - 1) / BK;
+    g.KT = (K + kTileK - 1) / kTileK;
+    g.KU = B >= kTcMinBatch ? 2 : 4;
+    g.UT = (g.KT + g.KU - 1) / g.KU;
     g.nchunks = (B + NB_CHUNK - 1) / NB_CHUNK;
-    g.U = g.nchunks * g.MT * g.KT;
+    g.U = g.nchunks * g.MT * g.UT;
     g.G = std::min(num_sms(), g.U);
-    // segments per tile: a tile of KT units meets at most ceil(KT / min_range) + 1 ranges
+    // segments per tile: a tile of UT units meets at most ceil(UT / min_range) + 1 ranges
     const int min_range = g.U / g.G;
-    g.max_seg = (g.KT + min_range - 1) / min_range + 1;
+    g.max_seg = (g.UT + min_range - 1) / min_range + 1;
     g.tiles = g.nchunks * g.MT;
     return g;
 }
@@ -534,6 +557,7 @@ cudaError_t launch_gemm_i8_tc(const uint8_t *Wt, const uint8_t *xb, float *part,
     p.M = M;
     p.MT = g.MT;
     p.KT = g.KT;
+    p.UT = g.UT;
     p.B = B;
     p.nchunks = g.nchunks;
     p.U = g.U;
@@ -550,7 +574,7 @@ cudaError_t launch_gemm_i8_tc(const uint8_t *Wt, const uint8_t *xb, float *part,
 cudaError_t launch_splitk_reduce(const float *part, const int *nseg, const float *s, float *y, int M,
                                  int K, int B, int32_t *rpos_advance, int conv_k, cudaStream_t st) {
     const GemmPlan g = plan_tc_gemm(M, K, B);
-    const SchedView sv{g.U, g.G, g.KT, g.MT, g.max_seg};
+    const SchedView sv{g.U, g.G, g.UT, g.MT, g.max_seg};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)g.tiles, (unsigned)((std::min(B, NB_CHUNK) + 1) / 2));
     cfg.blockDim = dim3(2 * BM);

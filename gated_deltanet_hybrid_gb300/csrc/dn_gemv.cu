@@ -10,11 +10,14 @@
 // W is stored as contiguous 8 KB tiles of 128 rows x 64 int8 (shared with the
 // tensor-core kernel) and the work is split exactly like the tensor-core
 // projection (stream-K, dn_sched.cuh): one CTA per SM takes a contiguous
-// range of (row tile, k tile) units.  Warp 0 streams the CTA's tiles with
-// 1-D bulk copies (cp.async.bulk) into a 16-deep shared-memory ring; eight
-// compute warps read each tile from shared memory (16 contiguous bytes per
-// lane), convert int8 exactly to fp32 and multiply with the fp32 activations
-// (read through L1), one accumulator per (row, sequence).  At the end of each
+// range of units, each 4 consecutive k tiles of one row tile (32 KB; bulk
+// copies this size keep the per-stage hand-off cost small against the HBM
+// time).  Warp 0 streams the CTA's units with 1-D bulk copies
+// (cp.async.bulk) into a 6-deep shared-memory ring; sixteen compute warps
+// read each tile from shared memory (16 contiguous bytes per lane: 16
+// weights of one row), convert int8 exactly to fp32 and multiply with the
+// fp32 activations (read through L1) in four independent FMA chains, one
+// accumulator per (row, sequence).  At the end of each
 // segment the four lanes of a row are combined in a fixed shuffle order and
 // the unscaled partial goes to its slot, to be summed and scaled by the
 // consumer in slot order (bitwise-reproducible results).
@@ -29,14 +32,16 @@
 namespace dn {
 namespace {
 
-constexpr int NSTAGE = 16;
-constexpr int kCompute = 256;            // compute threads (warps 1..8)
+constexpr int KU = 4;                    // 64-wide k tiles per unit: one 32 KB bulk copy
+constexpr int NSTAGE = 6;
+constexpr int kCompute = 512;            // compute threads (warps 1..16), one 16-byte chunk each
 constexpr int kThreads = 32 + kCompute;  // + producer warp
 constexpr uint32_t kTile = kTileM * kTileK;  // 8 KB
+constexpr uint32_t kUnit = KU * kTile;       // 32 KB
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 struct __align__(128) GemvSmem {
-    uint8_t tile[NSTAGE][kTile];
+    uint8_t tile[NSTAGE][kUnit];
     uint64_t full[NSTAGE];
     uint64_t empty[NSTAGE];
     int abort_flag;
@@ -48,8 +53,8 @@ struct GemvParams {
     float *part;      // [tiles][max_seg][64][128]
     int *nseg;        // [tiles]
     int *err;
-    SchedView sv;
-    int K, B;
+    SchedView sv;   // units per row tile in sv.KT
+    int K, B, KTt;  // KTt: 64-wide k tiles per row
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -96,28 +101,26 @@ __device__ __forceinline__ void i8x4_to_f32(uint32_t w, float *f) {
     f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653)) - 8388736.0f;
 }
 
+// 16-term dot product in four interleaved chains of four (fixed order)
 __device__ __forceinline__ float dot16(const float w[16], const float *xp) {
     const float4 a = *reinterpret_cast<const float4 *>(xp);
     const float4 b = *reinterpret_cast<const float4 *>(xp + 4);
     const float4 c = *reinterpret_cast<const float4 *>(xp + 8);
     const float4 d = *reinterpret_cast<const float4 *>(xp + 12);
-    float t = w[0] * a.x;
-    t = fmaf(w[1], a.y, t);
-    t = fmaf(w[2], a.z, t);
-    t = fmaf(w[3], a.w, t);
-    t = fmaf(w[4], b.x, t);
-    t = fmaf(w[5], b.y, t);
-    t = fmaf(w[6], b.z, t);
-    t = fmaf(w[7], b.w, t);
-    t = fmaf(w[8], c.x, t);
-    t = fmaf(w[9], c.y, t);
-    t = fmaf(w[10], c.z, t);
-    t = fmaf(w[11], c.w, t);
-    t = fmaf(w[12], d.x, t);
-    t = fmaf(w[13], d.y, t);
-    t = fmaf(w[14], d.z, t);
-    t = fmaf(w[15], d.w, t);
-    return t;
+    float t0 = w[0] * a.x, t1 = w[1] * a.y, t2 = w[2] * a.z, t3 = w[3] * a.w;
+    t0 = fmaf(w[4], b.x, t0);
+    t1 = fmaf(w[5], b.y, t1);
+    t2 = fmaf(w[6], b.z, t2);
+    t3 = fmaf(w[7], b.w, t3);
+    t0 = fmaf(w[8], c.x, t0);
+    t1 = fmaf(w[9], c.y, t1);
+    t2 = fmaf(w[10], c.z, t2);
+    t3 = fmaf(w[11], c.w, t3);
+    t0 = fmaf(w[12], d.x, t0);
+    t1 = fmaf(w[13], d.y, t1);
+    t2 = fmaf(w[14], d.z, t2);
+    t3 = fmaf(w[15], d.w, t3);
+    return (t0 + t1) + (t2 + t3);
 }
 
 template <int NB>
@@ -150,16 +153,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_i8_stream_kernel(const GemvP
                     *abort_flag = 1;
                     break;
                 }
-                const int tile = u / KT, kt = u % KT;
+                const int tile = u / KT, j = u % KT;
                 const int mt = tile % p.sv.MT;
+                const int kt0 = j * KU, nk = min(KU, p.KTt - kt0);
+                const uint32_t bytes = (uint32_t)nk * kTile;
                 asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
                                  smem_u32(&sm.full[st])),
-                             "r"(kTile)
+                             "r"(bytes)
                              : "memory");
                 asm volatile(
                     "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                         smem_u32(sm.tile[st])),
-                    "l"(p.Wt + ((size_t)mt * KT + kt) * kTile), "r"(kTile), "r"(smem_u32(&sm.full[st]))
+                    "l"(p.Wt + ((size_t)mt * p.KTt + kt0) * kTile), "r"(bytes), "r"(smem_u32(&sm.full[st]))
                     : "memory");
                 issued = it + 1;
             }
@@ -169,45 +174,37 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_i8_stream_kernel(const GemvP
             }
         }
     } else {
-        // ---- compute: thread t takes 16-byte chunks t and t + 256 of each tile:
-        //      rows t/4 and t/4 + 64, k part t % 4 (16 of the tile's 64 k) --------
+        // ---- compute: thread t takes 16-byte chunk t of each 8 KB tile of the
+        //      unit: row t/4, k part t % 4 (16 of the tile's 64 k) ---------------
         const int t = tid - 32;
-        const int lane = t & 31;
         const int kp = t & 3;
-        const int ra = t >> 2, rb = ra + 64;
-        float acc[2][NB];
+        const int r = t >> 2;
+        float acc[NB];
         int tile_cur = -1;
         for (int u = u0; u <= u1; ++u) {
             const int tile = u < u1 ? u / KT : -2;
             if (tile != tile_cur && tile_cur >= 0) {
                 // end of a segment: combine the 4 lanes of each row, write the partial
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
-#pragma unroll
-                    for (int j = 0; j < NB; ++j) {
-                        float v = acc[h][j];
-                        v += __shfl_xor_sync(0xffffffffu, v, 1);
-                        v += __shfl_xor_sync(0xffffffffu, v, 2);
-                        acc[h][j] = v;
-                    }
+                for (int j = 0; j < NB; ++j) {
+                    float v = acc[j];
+                    v += __shfl_xor_sync(0xffffffffu, v, 1);
+                    v += __shfl_xor_sync(0xffffffffu, v, 2);
+                    acc[j] = v;
+                }
                 const int slot = c - sched_cta_of_unit(tile_cur * KT, p.sv);
                 if (t == 0 && u1 >= (tile_cur + 1) * KT) p.nseg[tile_cur] = slot + 1;
                 if (kp == 0) {
                     float *ps = p.part + ((size_t)tile_cur * p.sv.max_seg + slot) * (64 * 128);
 #pragma unroll
                     for (int j = 0; j < NB; ++j)
-                        if (j < p.B) {
-                            ps[j * 128 + ra] = acc[0][j];
-                            ps[j * 128 + rb] = acc[1][j];
-                        }
+                        if (j < p.B) ps[j * 128 + r] = acc[j];
                 }
             }
             if (u == u1) break;
             if (tile != tile_cur) {
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
-#pragma unroll
-                    for (int j = 0; j < NB; ++j) acc[h][j] = 0.f;
+                for (int j = 0; j < NB; ++j) acc[j] = 0.f;
                 tile_cur = tile;
             }
             const int it = u - u0, st = it % NSTAGE;
@@ -217,33 +214,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_i8_stream_kernel(const GemvP
                 *abort_flag = 1;
                 break;
             }
-            const int kt = u % KT;
-            const int k0 = kt * kTileK + kp * 16;
-            const uint4 wa = *reinterpret_cast<const uint4 *>(sm.tile[st] + t * 16);
-            const uint4 wb = *reinterpret_cast<const uint4 *>(sm.tile[st] + (t + kCompute) * 16);
+            const int kt0 = (u % KT) * KU, nk = min(KU, p.KTt - kt0);
+            uint4 wv[KU];
+#pragma unroll
+            for (int i = 0; i < KU; ++i)
+                if (i < nk) wv[i] = *reinterpret_cast<const uint4 *>(sm.tile[st] + i * kTile + t * 16);
             asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&sm.empty[st]))
                          : "memory");
-            if (k0 < p.K) {
-                float fa[16], fb[16];
-                i8x4_to_f32(wa.x, fa);
-                i8x4_to_f32(wa.y, fa + 4);
-                i8x4_to_f32(wa.z, fa + 8);
-                i8x4_to_f32(wa.w, fa + 12);
-                i8x4_to_f32(wb.x, fb);
-                i8x4_to_f32(wb.y, fb + 4);
-                i8x4_to_f32(wb.z, fb + 8);
-                i8x4_to_f32(wb.w, fb + 12);
 #pragma unroll
-                for (int j = 0; j < NB; ++j) {
-                    if (j < p.B) {
-                        const float *xp = p.x + (size_t)j * p.K + k0;
-                        acc[0][j] += dot16(fa, xp);
-                        acc[1][j] += dot16(fb, xp);
-                    }
+            for (int i = 0; i < KU; ++i) {
+                const int k0 = (kt0 + i) * kTileK + kp * 16;
+                if (i < nk && k0 < p.K) {
+                    float fa[16];
+                    i8x4_to_f32(wv[i].x, fa);
+                    i8x4_to_f32(wv[i].y, fa + 4);
+                    i8x4_to_f32(wv[i].z, fa + 8);
+                    i8x4_to_f32(wv[i].w, fa + 12);
+#pragma unroll
+                    for (int jb = 0; jb < NB; ++jb)
+                        if (jb < p.B) acc[jb] += dot16(fa, p.x + (size_t)jb * p.K + k0);
                 }
             }
         }
-        (void)lane;
     }
     __syncthreads();
     if (tid == 0 && sm.abort_flag) atomicOr(p.err, 1);
@@ -269,9 +261,10 @@ cudaError_t launch_nb(const uint8_t *Wt, const float *x, float *part, int *nseg,
     p.part = part;
     p.nseg = nseg;
     p.err = err;
-    p.sv = SchedView{g.U, g.G, g.KT, g.MT, g.max_seg};
+    p.sv = SchedView{g.U, g.G, g.UT, g.MT, g.max_seg};
     p.K = K;
     p.B = B;
+    p.KTt = g.KT;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)g.G);
     cfg.blockDim = dim3(kThreads);

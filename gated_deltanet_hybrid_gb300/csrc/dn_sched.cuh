@@ -1,8 +1,9 @@
 // Stream-K schedule of the tensor-core projections, shared by the kernels
 // that produce split-tile partials and the kernels that consume them.
 //
-// A unit is one (batch chunk, 128-row tile, 64-wide k tile); units are
-// numbered tile-major (u = tile * KT + kt, tile = chunk * MT + mt).  CTA c of
+// A unit is one (batch chunk, 128-row tile, run of KU 64-wide k tiles); units
+// are numbered tile-major (u = tile * KT + j, tile = chunk * MT + mt, where KT
+// here counts units per row tile).  CTA c of
 // G takes units [c*U/G, (c+1)*U/G).  The part of a tile's KT units that one
 // CTA covers is a segment; segment `slot` of a tile is the one done by CTA
 // (first CTA of the tile) + slot.  A tile's partial sums live at
