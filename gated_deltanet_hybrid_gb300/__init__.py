@@ -22,6 +22,7 @@ from .abi import (  # noqa: F401
     dn_device_bytes,
     dn_get_state,
     dn_profile_next_step,
+    dn_proj_i8_noalloc,
     dn_set_state,
     dn_step,
     load_library,

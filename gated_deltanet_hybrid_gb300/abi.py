@@ -26,7 +26,8 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdn.so")
 
 #: every call the header declares, in declaration order
 ABI_SYMBOLS = ("dn_create", "dn_set_state", "dn_get_state", "dn_step", "dn_destroy",
-               "dn_debug_fail_next", "dn_profile_next_step", "dn_device_bytes", "dn_strerror")
+               "dn_debug_fail_next", "dn_profile_next_step", "dn_proj_i8_noalloc",
+               "dn_device_bytes", "dn_strerror")
 
 
 class DNError(RuntimeError):
@@ -76,6 +77,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dn_debug_fail_next.restype = i32
     lib.dn_profile_next_step.argtypes = [vp, ctypes.POINTER(ctypes.c_void_p)]
     lib.dn_profile_next_step.restype = i32
+    lib.dn_proj_i8_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp]
+    lib.dn_proj_i8_noalloc.restype = i32
     lib.dn_device_bytes.argtypes = []
     lib.dn_device_bytes.restype = ctypes.c_int64
     lib.dn_strerror.argtypes = [i32]
@@ -203,6 +206,22 @@ def dn_profile_next_step(layer, events, check: bool = True) -> int:
         return _check("dn_profile_next_step", lib.dn_profile_next_step(layer, None), check)
     arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
     return _check("dn_profile_next_step", lib.dn_profile_next_step(layer, arr), check)
+
+
+def dn_proj_i8_noalloc(W, s, x, y, stream=None, check: bool = True) -> int:
+    """y = s * (W x) for W int8 [M][K], s [M], x [B][K], y [B][M], all CUDA
+    tensors; the library allocates nothing for the call (its scratch is a
+    static device array)."""
+    lib = load_library()
+    pw, kw = _ptr(W, "int8")
+    ps, ks = _ptr(s, "float32")
+    px, kx = _ptr(x, "float32")
+    py, ky = _ptr(y, "float32")
+    if _same_kind(kw, ks, kx, ky) != DN_PTR_DEVICE:
+        raise TypeError("dn_proj_i8_noalloc takes device tensors")
+    M, K = int(W.shape[0]), int(W.shape[1])
+    rc = lib.dn_proj_i8_noalloc(pw, ps, px, py, M, K, int(x.shape[0]), _stream_of(stream, DN_PTR_DEVICE))
+    return _check("dn_proj_i8_noalloc", rc, check)
 
 
 def dn_device_bytes() -> int:

@@ -174,6 +174,37 @@ int dn_debug_fail_next(dn_layer *layer, int code);
  */
 int dn_profile_next_step(dn_layer *layer, void *const *events);
 
+/*
+ * dn_proj_i8_noalloc — the int8 row-scaled projection used inside dn_step,
+ * offered on its own for callers that must not allocate device memory:
+ *   y[b][o] = s[o] * sum_i W[o][i] * x[b][i],  b < B, o < M
+ * The pages have no counterpart of this call; it exists for code that runs
+ * where it does not own the device allocator (a plug-in inside another
+ * runtime's memory pool, a loop with a memory budget fixed in advance) and
+ * so can call neither cudaMalloc nor dn_create.  Its scratch (split-K
+ * partial sums) lives in one static device array of the library, about
+ * 4 MiB, that every GPU which loads the library holds until the process
+ * exits; the call itself allocates nothing.
+ *   W  int8 [M][K] row-major, device, 16-byte aligned
+ *   s  [M] row scales, device
+ *   x  [B][K] activations, device, 16-byte aligned
+ *   y  [B][M] output, device (written)
+ * Limits: 1 <= B <= 8, 1 <= M <= 16384, 16 <= K <= 16384, K a multiple of
+ * 16, and the split-K scratch of the shape must fit the static array (it
+ * does for every M, K within the limits on a 152-SM GPU); anything else
+ * returns DN_EINVAL before any device work.
+ * Work is enqueued on `stream` (NULL: the legacy default stream) and the
+ * call returns without synchronising.  The first call on a device looks up
+ * the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture.  Every call on a
+ * device shares the one array: nothing in it needs to start at zero (a call
+ * writes every scratch value it reads before reading it), but calls whose
+ * work overlaps on the GPU (other streams, other threads) race on it.
+ * Errors: DN_EINVAL, DN_ECUDA (launch failure).
+ */
+int dn_proj_i8_noalloc(const int8_t *W, const float *s, const float *x, float *y, int M, int K,
+                       int B, void *stream);
+
 /* dn_device_bytes — device bytes currently held by all live layers of this
  * process (leak accounting: 0 once every layer is destroyed). */
 int64_t dn_device_bytes(void);
