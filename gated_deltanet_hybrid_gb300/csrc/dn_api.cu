@@ -200,6 +200,7 @@ DN_API int dn_create(const dn_config *cfg, const dn_weights *w, void *stream, dn
     ALLOC(L.nseg_out, tiles_out * 4);
     ALLOC(L.xb_in, xb_bytes_in);
     ALLOC(L.xb_out, xb_bytes_out);
+    ALLOC(L.prep_rec, MB * d.n_v * dn::prep_record_len(d) * 4);
     ALLOC(L.err, 4);
 #undef ALLOC
     if (rc != DN_OK) {

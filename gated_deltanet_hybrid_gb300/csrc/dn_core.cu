@@ -98,6 +98,8 @@ __global__ void __launch_bounds__(kThreads, 2) dn_core_kernel(const CoreParams p
     //         DJ v channels of this slice; the ring takes the new inputs ----
     const int dpos = p.rpos[2 * b];
     const int K = p.conv_k;
+    pdl_wait();  // the in_proj partials come from the previous kernel
+    pdl_trigger();
     int wslot = dpos + K - 1;
     if (wslot >= K) wslot -= K;
     float *rb = p.ring + (size_t)b * K * p.conv_ch;
@@ -255,14 +257,17 @@ cudaError_t launch_core(const CoreParams &cp, int js, int n_v, int B, cudaStream
     cfg.gridDim = dim3((unsigned)js, (unsigned)n_v, (unsigned)B);
     cfg.blockDim = dim3(kThreads);
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (js > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)js;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)js;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
         return cudaLaunchKernelEx(&cfg, dn_core_kernel<DK, DJ, true>, cp);
     }
     return cudaLaunchKernelEx(&cfg, dn_core_kernel<DK, DJ, false>, cp);

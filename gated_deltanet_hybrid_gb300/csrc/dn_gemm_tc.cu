@@ -32,9 +32,11 @@
 // A pipeline stage is 128 rows x 128 k (16 KB of int8 weights, one bulk copy:
 // copies this size keep the per-stage hand-off cost small against the HBM
 // time).  Roles: warp 0 issues the bulk copies, warp 1 (one thread) the
-// MMAs, warps 2-5 convert the int8 unit to bf16 in a double-buffered shared
-// operand, warps 6-9 read the
-// accumulators (tcgen05.ld) and write results.  Every wait is bounded (about
+// MMAs, warps 2-9 convert the int8 unit to bf16 in a double-buffered shared
+// operand, warps 10-13 read the accumulators (tcgen05.ld) and write results.
+// The weight copies of the first stages go out before the kernel waits for
+// the previous kernel of the step (programmatic dependent launch): weights
+// are read-only, the activations and the partial buffers are not.  Every wait is bounded (about
 // one second of the global timer): on timeout the kernel records an error in
 // `err`, waits (bounded) for its own copies and MMAs in flight, frees its
 // tensor memory and returns.
@@ -53,8 +55,8 @@ constexpr int BK = 64;           // k per weight tile
 constexpr int KU = 2;            // k tiles per unit / pipeline stage (128 k)
 constexpr int STAGES = 3;
 constexpr int NB_CHUNK = 64;     // sequences per batch chunk (MMA N <= 128)
-constexpr int kThreads = 320;    // 10 warps
-constexpr int kConvThreads = 128;
+constexpr int kThreads = 448;    // 14 warps
+constexpr int kConvThreads = 256;
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kATileBytes = BM * BK;            // 8 KB int8
 constexpr uint32_t kOpTileBytes = 128 * BK * 2;      // 16 KB bf16
@@ -224,18 +226,21 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
     return v;
 }
 
-// 4 int8 -> 4 bf16, exact: byte ^ 0x80 in the mantissa of 2^23 is the float
-// 2^23 + b + 128; subtracting 2^23 + 128 is exact and leaves the integer b,
-// which bf16 holds exactly (|b| <= 128).
+// 4 int8 -> 4 bf16, exact, without float conversions: 0x43 above the low
+// 7 bits of a byte is the bf16 128 + (b & 127); 0x43 above its sign bit
+// (b & 0x80) is the bf16 128 or 256.  Their difference is the signed byte
+// b = (b & 127) - (b & 128), an integer of at most 8 significant bits that
+// bf16 holds exactly, so the packed subtraction is exact.
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+    __nv_bfloat162 r = __hsub2(*reinterpret_cast<__nv_bfloat162 *>(&a),
+                               *reinterpret_cast<__nv_bfloat162 *>(&b));
+    return *reinterpret_cast<uint32_t *>(&r);
+}
 __device__ __forceinline__ uint2 i8x4_to_bf16x4(uint32_t w) {
-    const uint32_t u = w ^ 0x80808080u;
-    const float f0 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)) - 8388736.0f;
-    const float f1 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651)) - 8388736.0f;
-    const float f2 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652)) - 8388736.0f;
-    const float f3 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653)) - 8388736.0f;
-    __nv_bfloat162 p0 = __floats2bfloat162_rn(f0, f1);
-    __nv_bfloat162 p1 = __floats2bfloat162_rn(f2, f3);
-    return make_uint2(*reinterpret_cast<uint32_t *>(&p0), *reinterpret_cast<uint32_t *>(&p1));
+    const uint32_t mag = w & 0x7F7F7F7Fu, sgn = w & 0x80808080u;
+    const uint32_t a01 = __byte_perm(mag, 0x43u, 0x4140), a23 = __byte_perm(mag, 0x43u, 0x4342);
+    const uint32_t s01 = __byte_perm(sgn, 0x43u, 0x4140), s23 = __byte_perm(sgn, 0x43u, 0x4342);
+    return make_uint2(bf16x2_sub(a01, s01), bf16x2_sub(a23, s23));
 }
 
 __device__ __forceinline__ int unit_start(int c, const GemmParams &p) {
@@ -287,25 +292,41 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_i8_tc_kernel(const GemmParam
     if (warp == 0) {
         // ---- bulk-copy producer ---------------------------------------------
         if (lane == 0) {
-            int issued = 0;  // stages whose last issued copy may still be in flight
-            for (int u = u0; u < u1; ++u) {
-                const int it = u - u0, st = it % STAGES;
-                if (it >= STAGES && !mbar_wait(&sm.empty[st], ((it / STAGES) - 1) & 1, abort_flag)) {
-                    *abort_flag = 1;
-                    break;
-                }
+            // weights of the first stages before waiting for the previous kernel
+            const int n_pre = min(STAGES, u1 - u0);
+            for (int it = 0; it < n_pre; ++it) {
+                const int u = u0 + it;
                 const int tile = u / p.UT, kt0 = (u % p.UT) * KU;
                 const int chunk = tile / p.MT, mt = tile % p.MT;
                 const int nk = min(KU, p.KT - kt0);
                 const int N = 2 * ((chunk_rows(chunk, p) + 7) & ~7);
-                mbar_arrive_expect_tx(&sm.full[st], (uint32_t)nk * (kATileBytes + (uint32_t)N * 128u));
-                bulk_g2s(smem_u32(sm.a8[st]), p.Wt + ((size_t)mt * p.KT + kt0) * kATileBytes,
-                         (uint32_t)nk * kATileBytes, &sm.full[st]);
+                mbar_arrive_expect_tx(&sm.full[it], (uint32_t)nk * (kATileBytes + (uint32_t)N * 128u));
+                bulk_g2s(smem_u32(sm.a8[it]), p.Wt + ((size_t)mt * p.KT + kt0) * kATileBytes,
+                         (uint32_t)nk * kATileBytes, &sm.full[it]);
+            }
+            pdl_wait();
+            pdl_trigger();
+            int issued = n_pre;  // stages whose last issued copy may still be in flight
+            for (int u = u0; u < u1; ++u) {
+                const int it = u - u0, st = it % STAGES;
+                const int tile = u / p.UT, kt0 = (u % p.UT) * KU;
+                const int chunk = tile / p.MT, mt = tile % p.MT;
+                const int nk = min(KU, p.KT - kt0);
+                const int N = 2 * ((chunk_rows(chunk, p) + 7) & ~7);
+                if (it >= n_pre) {
+                    if (!mbar_wait(&sm.empty[st], ((it / STAGES) - 1) & 1, abort_flag)) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&sm.full[st], (uint32_t)nk * (kATileBytes + (uint32_t)N * 128u));
+                    bulk_g2s(smem_u32(sm.a8[st]), p.Wt + ((size_t)mt * p.KT + kt0) * kATileBytes,
+                             (uint32_t)nk * kATileBytes, &sm.full[st]);
+                    issued = it + 1;
+                }
                 for (int i = 0; i < nk; ++i)
                     bulk_g2s(smem_u32(sm.b16[st]) + (uint32_t)i * kOpTileBytes,
                              p.xb + ((size_t)chunk * p.KT + kt0 + i) * kOpTileBytes, (uint32_t)N * 128u,
                              &sm.full[st]);
-                issued = it + 1;
             }
             if (*abort_flag) {  // let every copy still in flight land before exiting
                 for (int it = max(0, issued - STAGES); it < issued; ++it)
@@ -356,9 +377,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_i8_tc_kernel(const GemmParam
             mma_commit(&sm.drain);  // arrives once every MMA issued above has completed
             mbar_wait(&sm.drain, 0, abort_flag, true);
         }
-    } else if (warp < 6) {
+    } else if (warp < 10) {
         // ---- int8 -> bf16 converters ------------------------------------------------
-        const int t = tid - 64;  // 0..127
+        const int t = tid - 64;  // 0..255
         for (int u = u0; u < u1; ++u) {
             const int it = u - u0, st = it % STAGES, ab = it & 1;
             if (!mbar_wait(&sm.full[st], (it / STAGES) & 1, abort_flag) ||
@@ -369,8 +390,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_i8_tc_kernel(const GemmParam
             const int nk = min(KU, p.KT - (u % p.UT) * KU);
             const uint32_t src = smem_u32(sm.a8[st]), dst = smem_u32(sm.a16[ab]);
 #pragma unroll
-            for (int i = 0; i < 4 * KU; ++i) {
-                const int q = t + 128 * i;  // 16-byte chunk of the int8 unit
+            for (int i = 0; i < 2 * KU; ++i) {
+                const int q = t + kConvThreads * i;  // 16-byte chunk of the int8 unit
                 if (q < nk * 512) {
                     const int half = q >> 9, qq = q & 511;
                     const int row = qq >> 2, kp = qq & 3;  // row, 16-element part of its 64 k
@@ -387,7 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_i8_tc_kernel(const GemmParam
             mbar_arrive(&sm.conv[ab]);
         }
     } else {
-        // ---- epilogue: warps 6..9 read TMEM lane quarters 2, 3, 0, 1 --------------
+        // ---- epilogue: warps 10..13 read TMEM lane quarters 2, 3, 0, 1 ------------
+        pdl_wait();  // the partial buffers may still be read by the previous kernel
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;
         const SchedView sv{p.U, p.G, p.UT, p.MT, p.max_seg};
@@ -442,6 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_i8_tc_kernel(const GemmParam
 // 2b (hi) and 2b+1 (lo) of sequence b; k >= K and b in [Bc, Bpad) are zero.
 __global__ void pack_b_kernel(const float *__restrict__ x, uint8_t *__restrict__ xb, int B, int K,
                               int KT) {
+    pdl_wait();
+    pdl_trigger();
     const int kt = blockIdx.x, chunk = blockIdx.y;
     const int Bc = min(NB_CHUNK, B - chunk * NB_CHUNK);
     const int Bpad = (Bc + 7) & ~7;
@@ -482,6 +506,8 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ part, const int *
                                      const float *__restrict__ s, float *__restrict__ y,
                                      SchedView sv, int M, int B, int32_t *__restrict__ rpos,
                                      int conv_k) {
+    pdl_wait();
+    pdl_trigger();
     if (rpos != nullptr && blockIdx.x == 0 && blockIdx.y == 0) {
         for (int b = threadIdx.x; b < B; b += blockDim.x) {
             int2 q = reinterpret_cast<int2 *>(rpos)[b];
@@ -532,6 +558,8 @@ cudaError_t launch_pack_b(const float *x, uint8_t *xb, int B, int K, cudaStream_
     cfg.gridDim = dim3((unsigned)KT, (unsigned)((B + NB_CHUNK - 1) / NB_CHUNK), 4);
     cfg.blockDim = dim3(128);
     cfg.stream = st;
+    PdlAttr pdl;
+    pdl.apply(cfg);
     return cudaLaunchKernelEx(&cfg, pack_b_kernel, x, xb, B, K, KT);
 }
 
@@ -568,6 +596,8 @@ cudaError_t launch_gemm_i8_tc(const uint8_t *Wt, const uint8_t *xb, float *part,
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
+    PdlAttr pdl;
+    pdl.apply(cfg);
     return cudaLaunchKernelEx(&cfg, gemm_i8_tc_kernel, p);
 }
 
@@ -579,6 +609,8 @@ cudaError_t launch_splitk_reduce(const float *part, const int *nseg, const float
     cfg.gridDim = dim3((unsigned)g.tiles, (unsigned)((std::min(B, NB_CHUNK) + 1) / 2));
     cfg.blockDim = dim3(2 * BM);
     cfg.stream = st;
+    PdlAttr pdl;
+    pdl.apply(cfg);
     return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, part, nseg, s, y, sv, M, B, rpos_advance,
                               conv_k);
 }

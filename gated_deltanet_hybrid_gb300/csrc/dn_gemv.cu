@@ -176,6 +176,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_i8_stream_kernel(const GemvP
     } else {
         // ---- compute: thread t takes 16-byte chunk t of each 8 KB tile of the
         //      unit: row t/4, k part t % 4 (16 of the tile's 64 k) ---------------
+        pdl_wait();  // x and the partial buffers: after the previous kernel
+        if (tid == 32) pdl_trigger();
         const int t = tid - 32;
         const int kp = t & 3;
         const int r = t >> 2;
@@ -270,6 +272,8 @@ cudaError_t launch_nb(const uint8_t *Wt, const float *x, float *part, int *nseg,
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
+    PdlAttr pdl;
+    pdl.apply(cfg);
     return cudaLaunchKernelEx(&cfg, gemv_i8_stream_kernel<NB>, p);
 }
 

@@ -47,6 +47,7 @@ struct LayerDev {
     int *nseg_in, *nseg_out;  // segments per tile of the last projection launch
     uint8_t *xb_in;        // packed B-operand tiles of x   [chunks][KT_in][16 KB]
     uint8_t *xb_out;       // packed B-operand tiles of the gated-norm output [chunks][KT_out][16 KB]
+    float *prep_rec;       // [max_batch][n_v][2*dk + 2*dv + 4] records for the persistent state kernel
     int *err;              // device-side error word (bounded waits that gave up)
 };
 
@@ -91,7 +92,13 @@ constexpr size_t kOpTile = 16384;  // bytes of one packed B-operand tile (64 seq
 cudaError_t launch_dn_core(const Dims &d, const LayerDev &L, int B, const float *g,
                            const float *beta, bool tc, cudaStream_t st);
 
-// Persistent bulk-copy-pipelined variant for large batches of 128 x 128 heads.
+// Per-(sequence, head) conv / norm / gate records for the persistent kernel.
+int prep_record_len(const Dims &d);
+cudaError_t launch_dn_prep(const Dims &d, const LayerDev &L, int B, const float *g,
+                           const float *beta, cudaStream_t st);
+
+// Persistent bulk-copy-pipelined variant for large batches of 128 x 128 heads
+// (launches dn_prep first).
 bool dn_core_stream_ok(const Dims &d, int B);
 cudaError_t launch_dn_core_stream(const Dims &d, const LayerDev &L, int B, const float *g,
                                   const float *beta, bool tc, cudaStream_t st);
@@ -103,5 +110,26 @@ cudaError_t launch_ring_export(const Dims &d, const LayerDev &L, int seq0, int n
                                cudaStream_t st);
 
 int num_sms();
+
+// Programmatic dependent launch.  Every kernel of a step is launched with
+// the programmatic-serialization attribute (with_pdl), so it may start while
+// the kernel before it is still running.  A kernel may only read read-only
+// data (weights, the recurrent state when the previous kernel does not touch
+// it) before pdl_wait(), which returns once the previous kernel has
+// completed and its writes are visible; it signals pdl_trigger() only after
+// its own pdl_wait(), so at most two kernels of the chain overlap.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+struct PdlAttr {
+    cudaLaunchAttribute a[1];
+    void apply(cudaLaunchConfig_t &cfg) {
+        a[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        a[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = a;
+        cfg.numAttrs = 1;
+    }
+};
 
 }  // namespace dn
