@@ -74,7 +74,9 @@ std::vector<uint8_t> tile_weights(const int8_t *W, int M, int K) {
         const int mt = m / dn::kTileM, r = m % dn::kTileM;
         for (int k = 0; k < K; ++k) {
             const int kt = k / dn::kTileK, kk = k % dn::kTileK;
-            t[(((size_t)mt * KT + kt) * dn::kTileM + r) * dn::kTileK + kk] = (uint8_t)W[(size_t)m * K + k];
+            // [mt][kt][k part (16 k)][row][16 B]
+            t[((size_t)mt * KT + kt) * dn::kTileM * dn::kTileK + (size_t)(kk >> 4) * dn::kTileM * 16 + r * 16 +
+              (kk & 15)] = (uint8_t)W[(size_t)m * K + k];
         }
     }
     return t;

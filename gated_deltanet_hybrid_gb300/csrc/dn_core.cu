@@ -245,8 +245,8 @@ __global__ void __launch_bounds__(kThreads, 2) dn_core_kernel(const CoreParams p
             uint8_t *tile = p.xb_out + ((size_t)(b >> 6) * p.kt_out + (k >> 6)) * kOpTile;
             const int kc = (k & 63) >> 3, e = k & 7;
             const int rh = 2 * (b & 63), rl = rh + 1;
-            *reinterpret_cast<__nv_bfloat16 *>(tile + (rh >> 3) * 1024 + kc * 128 + (rh & 7) * 16 + e * 2) = hi;
-            *reinterpret_cast<__nv_bfloat16 *>(tile + (rl >> 3) * 1024 + kc * 128 + (rl & 7) * 16 + e * 2) = lo;
+            *reinterpret_cast<__nv_bfloat16 *>(tile + op_chunk_offset(rh, kc) + e * 2) = hi;
+            *reinterpret_cast<__nv_bfloat16 *>(tile + op_chunk_offset(rl, kc) + e * 2) = lo;
         }
     }
 }

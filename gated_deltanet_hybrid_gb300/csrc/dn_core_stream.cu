@@ -240,8 +240,8 @@ __global__ void __launch_bounds__(NT, 1) dn_core_stream_kernel(const StreamParam
                 uint8_t *ot = p.xb_out + ((size_t)(b >> 6) * p.kt_out + (k >> 6)) * kOpTile;
                 const int kc = (k & 63) >> 3, e = k & 7;
                 const int rh = 2 * (b & 63), rl = rh + 1;
-                *reinterpret_cast<__nv_bfloat16 *>(ot + (rh >> 3) * 1024 + kc * 128 + (rh & 7) * 16 + e * 2) = hi;
-                *reinterpret_cast<__nv_bfloat16 *>(ot + (rl >> 3) * 1024 + kc * 128 + (rl & 7) * 16 + e * 2) = lo;
+                *reinterpret_cast<__nv_bfloat16 *>(ot + op_chunk_offset(rh, kc) + e * 2) = hi;
+                *reinterpret_cast<__nv_bfloat16 *>(ot + op_chunk_offset(rl, kc) + e * 2) = lo;
             }
         }
         // (red, delta and ssq_o are next written after the next item's first barrier)

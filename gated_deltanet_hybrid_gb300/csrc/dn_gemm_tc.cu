@@ -13,11 +13,15 @@
 // and the epilogue adds accumulator columns 2b and 2b+1.
 //
 // Layouts.  The layer stores W as contiguous 8 KB tiles [m tile][k tile]
-// [128 rows][64 int8] and the activations as 16 KB tiles [batch chunk][k tile]
-// holding 128 B-operand rows of 64 bf16 in the MMA's canonical K-major layout
-// (8-row x 16-byte core matrices; 8-row groups 1024 bytes apart).  So every
-// pipeline stage is two 1-D bulk copies (cp.async.bulk, completed on an
-// mbarrier), and the k tiles of a row tile stream through HBM sequentially.
+// (128 rows x 64 int8 in four 16-k parts, dn_internal.cuh) and the
+// activations as 16 KB tiles [batch chunk][k tile] holding 128 B-operand
+// rows of 64 bf16 in the 128-byte swizzled K-major layout (op_chunk_offset).
+// So every pipeline stage is two 1-D bulk copies (cp.async.bulk, completed
+// on an mbarrier), and the k tiles of a row tile stream through HBM
+// sequentially.  The converted weights never go back to shared memory: the
+// converters store them into tensor memory (tcgen05.st), and the MMA takes
+// its A operand from there, so shared memory only carries the copies, the
+// converters' int8 reads and the MMA's B reads.
 //
 // Work split (stream-K).  A unit is one (batch chunk, m tile, k tile).  The
 // grid has one CTA per SM; CTA c takes the contiguous unit range
@@ -25,21 +29,23 @@
 // tile count.  A range covers the tail of one m tile and the head of the next
 // (a "segment" each); two TMEM accumulators alternate between segments.
 // Every segment's partial sums go to a slot of a partial buffer (schedule in
-// dn_sched.cuh); the consumer sums a tile's slots in slot order (the fused
+// dn_sched.cuh); the consumer sums a tile's slots in slot order (the prep or
 // core kernel for the in_proj, splitk_reduce_kernel for the out_proj), so
 // results do not depend on scheduling and no CTA waits on another.
 //
 // A pipeline stage is 128 rows x 128 k (16 KB of int8 weights, one bulk copy:
 // copies this size keep the per-stage hand-off cost small against the HBM
 // time).  Roles: warp 0 issues the bulk copies, warp 1 (one thread) the
-// MMAs, warps 2-9 convert the int8 unit to bf16 in a double-buffered shared
-// operand, warps 10-13 read the accumulators (tcgen05.ld) and write results.
-// The weight copies of the first stages go out before the kernel waits for
-// the previous kernel of the step (programmatic dependent launch): weights
-// are read-only, the activations and the partial buffers are not.  Every wait is bounded (about
-// one second of the global timer): on timeout the kernel records an error in
-// `err`, waits (bounded) for its own copies and MMAs in flight, frees its
-// tensor memory and returns.
+// MMAs, warps 2-9 convert the int8 unit to bf16 into one of two tensor-memory
+// A buffers (warp w owns lane quarter w % 4 and k tile (w - 2) / 4 of the
+// unit: one row per lane), warps 10-13 read the accumulators (tcgen05.ld) and
+// write results.  Tensor memory: accumulators in columns 0-255, A buffers in
+// 256-383.  The weight copies of the first stages go out before the kernel
+// waits for the previous kernel of the step (programmatic dependent launch):
+// weights are read-only, the activations and the partial buffers are not.
+// Every wait is bounded (about one second of the global timer): on timeout
+// the kernel records an error in `err`, waits (bounded) for its own copies
+// and MMAs in flight, frees its tensor memory and returns.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -53,28 +59,26 @@ namespace {
 constexpr int BM = 128;          // weight rows per tile (MMA M)
 constexpr int BK = 64;           // k per weight tile
 constexpr int KU = 2;            // k tiles per unit / pipeline stage (128 k)
-constexpr int STAGES = 3;
+constexpr int STAGES = 4;
 constexpr int NB_CHUNK = 64;     // sequences per batch chunk (MMA N <= 128)
 constexpr int kThreads = 448;    // 14 warps
 constexpr int kConvThreads = 256;
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kATileBytes = BM * BK;            // 8 KB int8
 constexpr uint32_t kOpTileBytes = 128 * BK * 2;      // 16 KB bf16
-constexpr uint32_t kCoreBytes = 128;
-constexpr uint32_t kGroupBytes = (BK / 8) * 128;     // 1024
-constexpr uint32_t kTmemCols = 256;                  // two 128-column accumulators
+constexpr uint32_t kTmemCols = 512;                  // 2 accumulators x 128 + 2 A buffers x 64
+constexpr uint32_t kTmemA = 256;                     // first column of the A buffers
+constexpr uint32_t kACols = KU * BK / 2;             // 64: bf16 pairs of a 128-k unit
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
-// A unit (= pipeline stage) is 128 rows x 128 k: two 64-k halves, each laid
-// out like one 64-k tile (core-matrix groups 1024 bytes apart).
+// A unit (= pipeline stage) is 128 rows x 128 k: two 64-k tiles.
 struct __align__(1024) GemmSmem {
-    uint8_t a16[2][KU * kOpTileBytes];       // bf16 A operand, double-buffered (2 x 32 KB)
-    uint8_t b16[STAGES][KU * kOpTileBytes];  // bf16 B operand as copied (3 x 32 KB)
-    uint8_t a8[STAGES][KU * kATileBytes];    // int8 A as copied (3 x 16 KB)
+    uint8_t b16[STAGES][KU * kOpTileBytes];  // bf16 B operand as copied (4 x 32 KB)
+    uint8_t a8[STAGES][KU * kATileBytes];    // int8 A as copied (4 x 16 KB)
     uint64_t full[STAGES];                   // bulk copies of the stage landed
     uint64_t empty[STAGES];                  // MMAs done reading the stage
-    uint64_t conv[2];                        // A converted to bf16 (per a16 buffer)
-    uint64_t a16_free[2];                    // MMAs done reading the a16 buffer
+    uint64_t conv[2];                        // A converted into tensor-memory buffer 0 / 1
+    uint64_t a_free[2];                      // MMAs done reading tensor-memory A buffer 0 / 1
     uint64_t acc_full[2];               // accumulator ready for the epilogue
     uint64_t acc_empty[2];              // epilogue done reading the accumulator
     uint64_t drain;                     // all MMAs of this CTA completed
@@ -151,9 +155,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         : "memory");
 }
 
-__device__ __forceinline__ void fence_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -161,15 +162,21 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor, K-major, no swizzle: `lbo` = byte distance
-// between core matrices along K, `sbo` = between 8-row groups; bits 46..48
-// hold the descriptor format's fixed value 0b001.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+// Shared-memory matrix descriptor for the 128-byte swizzled K-major layout
+// (bits 46..48 hold the descriptor format's fixed value 0b001): rows of 64 bf16
+// (128 bytes) stored contiguously, 8-row groups 1024 bytes apart, and within
+// each 1024-byte group the 16-byte chunk c of row r stored at chunk position
+// c ^ (r & 7).  The leading offset is unused in this mode; a K step of 16
+// elements inside the 128-byte row is a 32-byte advance of the start address
+// (the hardware applies the XOR to the computed addresses), so groups must be
+// 1024-byte aligned.  Layout-type field (bits 61..63) = 2.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
     uint64_t d = 0;
     d |= (uint64_t)((addr >> 4) & 0x3FFFu);
-    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024u >> 4) << 32;
     d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
     return d;
 }
 
@@ -180,13 +187,15 @@ __device__ __forceinline__ uint32_t instr_desc(int M, int N) {
            ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
+// D (tensor memory) (+)= A (tensor memory, lane = row, 32-bit column = two
+// consecutive k) x B (shared memory descriptor)^T
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -211,19 +220,19 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w)
-                 : "memory");
-}
-
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
+// 32 consecutive 32-bit columns of this thread's tensor-memory lane, then
+// wait until the stores are done
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t v[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+        "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
+        "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // 4 int8 -> 4 bf16, exact, without float conversions: 0x43 above the low
@@ -266,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_i8_tc_kernel(const GemmParam
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&sm.conv[a], kConvThreads);
-            mbar_init(&sm.a16_free[a], 1);
+            mbar_init(&sm.a_free[a], 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&sm.acc_full[a], 1);
@@ -360,15 +369,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_i8_tc_kernel(const GemmParam
                     }
                     tc_fence_after();
                     const int nk = min(KU, p.KT - (u % p.UT) * KU);
-                    const uint32_t a0 = smem_u32(sm.a16[ab]), b0 = smem_u32(sm.b16[st]);
+                    const uint32_t ta = tmem + kTmemA + (uint32_t)ab * kACols, b0 = smem_u32(sm.b16[st]);
                     for (int kk = 0; kk < nk * (BK / 16); ++kk) {
-                        const uint32_t off = (uint32_t)(kk >> 2) * kOpTileBytes + (uint32_t)(kk & 3) * 2 * kCoreBytes;
-                        const uint64_t ad = smem_desc(a0 + off, kCoreBytes, kGroupBytes);
-                        const uint64_t bd = smem_desc(b0 + off, kCoreBytes, kGroupBytes);
-                        mma_bf16(dtm, ad, bd, idesc, (u == useg && kk == 0) ? 0u : 1u);
+                        // K step of 16: 8 tensor-memory columns of A, 32 bytes of B's rows
+                        const uint64_t bd = smem_desc_sw128(b0 + (uint32_t)(kk >> 2) * kOpTileBytes +
+                                                            (uint32_t)(kk & 3) * 32u);
+                        mma_bf16_ts(dtm, ta + (uint32_t)kk * 8u, bd, idesc, (u == useg && kk == 0) ? 0u : 1u);
                     }
                     mma_commit(&sm.empty[st]);
-                    mma_commit(&sm.a16_free[ab]);
+                    mma_commit(&sm.a_free[ab]);
                 }
                 if (!ok) break;
                 mma_commit(&sm.acc_full[a]);
@@ -378,33 +387,42 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_i8_tc_kernel(const GemmParam
             mbar_wait(&sm.drain, 0, abort_flag, true);
         }
     } else if (warp < 10) {
-        // ---- int8 -> bf16 converters ------------------------------------------------
-        const int t = tid - 64;  // 0..255
+        // ---- int8 -> bf16 converters: lane = row of the unit's k tile kh ---------
+        const int quarter = warp & 3, kh = (warp - 2) >> 2;
+        const int row = quarter * 32 + lane;
+        const uint32_t tlane = (uint32_t)(quarter * 32) << 16;
         for (int u = u0; u < u1; ++u) {
             const int it = u - u0, st = it % STAGES, ab = it & 1;
             if (!mbar_wait(&sm.full[st], (it / STAGES) & 1, abort_flag) ||
-                (it >= 2 && !mbar_wait(&sm.a16_free[ab], ((it >> 1) - 1) & 1, abort_flag))) {
+                (it >= 2 && !mbar_wait(&sm.a_free[ab], ((it >> 1) - 1) & 1, abort_flag))) {
                 *abort_flag = 1;
                 break;
             }
             const int nk = min(KU, p.KT - (u % p.UT) * KU);
-            const uint32_t src = smem_u32(sm.a8[st]), dst = smem_u32(sm.a16[ab]);
+            if (kh < nk) {  // warp-uniform
+                // the row's 4 k parts: 16 bytes each, 2 KB apart (lanes read 512
+                // contiguous bytes per part)
+                const uint8_t *src = sm.a8[st] + kh * kATileBytes + row * 16;
+                uint4 w[4];
 #pragma unroll
-            for (int i = 0; i < 2 * KU; ++i) {
-                const int q = t + kConvThreads * i;  // 16-byte chunk of the int8 unit
-                if (q < nk * 512) {
-                    const int half = q >> 9, qq = q & 511;
-                    const int row = qq >> 2, kp = qq & 3;  // row, 16-element part of its 64 k
-                    const uint4 w = ld_shared_v4(src + (uint32_t)q * 16u);
-                    const uint2 e0 = i8x4_to_bf16x4(w.x), e1 = i8x4_to_bf16x4(w.y);
-                    const uint2 e2 = i8x4_to_bf16x4(w.z), e3 = i8x4_to_bf16x4(w.w);
-                    const uint32_t off = (uint32_t)half * kOpTileBytes + (uint32_t)(row >> 3) * kGroupBytes +
-                                         (uint32_t)(row & 7) * 16u;
-                    st_shared_v4(dst + off + (uint32_t)(2 * kp) * kCoreBytes, make_uint4(e0.x, e0.y, e1.x, e1.y));
-                    st_shared_v4(dst + off + (uint32_t)(2 * kp + 1) * kCoreBytes, make_uint4(e2.x, e2.y, e3.x, e3.y));
+                for (int kp = 0; kp < 4; ++kp) w[kp] = *reinterpret_cast<const uint4 *>(src + kp * 2048);
+                uint32_t v[32];  // bf16 pairs (k even, k odd) of the row's 64 k, in k order
+#pragma unroll
+                for (int kp = 0; kp < 4; ++kp) {
+                    const uint2 e0 = i8x4_to_bf16x4(w[kp].x), e1 = i8x4_to_bf16x4(w[kp].y);
+                    const uint2 e2 = i8x4_to_bf16x4(w[kp].z), e3 = i8x4_to_bf16x4(w[kp].w);
+                    v[kp * 8 + 0] = e0.x;
+                    v[kp * 8 + 1] = e0.y;
+                    v[kp * 8 + 2] = e1.x;
+                    v[kp * 8 + 3] = e1.y;
+                    v[kp * 8 + 4] = e2.x;
+                    v[kp * 8 + 5] = e2.y;
+                    v[kp * 8 + 6] = e3.x;
+                    v[kp * 8 + 7] = e3.y;
                 }
+                tmem_st32(tmem + tlane + kTmemA + (uint32_t)ab * kACols + (uint32_t)kh * 32u, v);
             }
-            fence_async_smem();
+            tc_fence_before();
             mbar_arrive(&sm.conv[ab]);
         }
     } else {
@@ -493,10 +511,8 @@ __global__ void pack_b_kernel(const float *__restrict__ x, uint8_t *__restrict__
             lo[j] = *reinterpret_cast<uint32_t *>(&l);
         }
         const int rh = 2 * b, rl = 2 * b + 1;
-        *reinterpret_cast<uint4 *>(tile + (rh >> 3) * kGroupBytes + kc * kCoreBytes + (rh & 7) * 16) =
-            make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4 *>(tile + (rl >> 3) * kGroupBytes + kc * kCoreBytes + (rl & 7) * 16) =
-            make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        *reinterpret_cast<uint4 *>(tile + op_chunk_offset(rh, kc)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(tile + op_chunk_offset(rl, kc)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
 }
 

@@ -7,20 +7,20 @@
 // instead of two").  At small batch the step is a weight stream: the kernel
 // is built so that every SM keeps about 128 KB of weights in flight.
 //
-// W is stored as contiguous 8 KB tiles of 128 rows x 64 int8 (shared with the
-// tensor-core kernel) and the work is split exactly like the tensor-core
+// W is stored as contiguous 8 KB tiles of 128 rows x 64 int8 in four 16-k
+// parts (dn_internal.cuh; shared with the tensor-core kernel) and the work is split exactly like the tensor-core
 // projection (stream-K, dn_sched.cuh): one CTA per SM takes a contiguous
 // range of units, each 4 consecutive k tiles of one row tile (32 KB; bulk
 // copies this size keep the per-stage hand-off cost small against the HBM
 // time).  Warp 0 streams the CTA's units with 1-D bulk copies
 // (cp.async.bulk) into a 6-deep shared-memory ring; sixteen compute warps
 // read each tile from shared memory (16 contiguous bytes per lane: 16
-// weights of one row), convert int8 exactly to fp32 and multiply with the
-// fp32 activations (read through L1) in four independent FMA chains, one
-// accumulator per (row, sequence).  At the end of each
-// segment the four lanes of a row are combined in a fixed shuffle order and
-// the unscaled partial goes to its slot, to be summed and scaled by the
-// consumer in slot order (bitwise-reproducible results).
+// weights of one row; a warp takes 8 rows x 4 k parts), convert int8 exactly
+// to fp32 and multiply with the fp32 activations (read through L1) in four
+// independent FMA chains, one accumulator per (row, sequence).  At the end
+// of each segment the four lanes of a row (8 apart) are combined in a fixed
+// shuffle order and the unscaled partial goes to its slot, to be summed and
+// scaled by the consumer in slot order (bitwise-reproducible results).
 //
 // Every wait is bounded (about one second of the global timer); on timeout
 // the kernel records an error in `err`, lets its copies land and returns.
@@ -174,13 +174,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_i8_stream_kernel(const GemvP
             }
         }
     } else {
-        // ---- compute: thread t takes 16-byte chunk t of each 8 KB tile of the
-        //      unit: row t/4, k part t % 4 (16 of the tile's 64 k) ---------------
+        // ---- compute: lane l of compute warp w takes k part l/8 (16 of the
+        //      tile's 64 k) of row 8w + l%8 of each 8 KB tile of the unit ---------
         pdl_wait();  // x and the partial buffers: after the previous kernel
         if (tid == 32) pdl_trigger();
         const int t = tid - 32;
-        const int kp = t & 3;
-        const int r = t >> 2;
+        const int kp = (t >> 3) & 3;
+        const int r = (t >> 5) * 8 + (t & 7);
         float acc[NB];
         int tile_cur = -1;
         for (int u = u0; u <= u1; ++u) {
@@ -190,8 +190,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_i8_stream_kernel(const GemvP
 #pragma unroll
                 for (int j = 0; j < NB; ++j) {
                     float v = acc[j];
-                    v += __shfl_xor_sync(0xffffffffu, v, 1);
-                    v += __shfl_xor_sync(0xffffffffu, v, 2);
+                    v += __shfl_xor_sync(0xffffffffu, v, 8);
+                    v += __shfl_xor_sync(0xffffffffu, v, 16);
                     acc[j] = v;
                 }
                 const int slot = c - sched_cta_of_unit(tile_cur * KT, p.sv);
@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_i8_stream_kernel(const GemvP
             uint4 wv[KU];
 #pragma unroll
             for (int i = 0; i < KU; ++i)
-                if (i < nk) wv[i] = *reinterpret_cast<const uint4 *>(sm.tile[st] + i * kTile + t * 16);
+                if (i < nk) wv[i] = *reinterpret_cast<const uint4 *>(sm.tile[st] + i * kTile + kp * 2048 + r * 16);
             asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&sm.empty[st]))
                          : "memory");
 #pragma unroll

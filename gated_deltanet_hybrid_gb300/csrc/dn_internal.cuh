@@ -52,8 +52,11 @@ struct LayerDev {
 };
 
 // Weight tiles used by every projection kernel: W [M][K] int8 is stored as
-// [ceil(M/128)][ceil(K/64)][128 rows][64 int8], zero-padded, one 8 KB
-// contiguous block per (m tile, k tile).
+// [ceil(M/128)][ceil(K/64)][4 k parts][128 rows][16 int8], zero-padded, one
+// 8 KB contiguous block per (m tile, k tile); k part p holds k 16p..16p+15 of
+// the tile.  A warp reading 16 bytes per lane for 32 consecutive rows of one
+// k part (or 8 rows x 4 parts, 8 lanes per part) touches 512 contiguous
+// bytes per part, so shared-memory reads of a tile are free of bank conflicts.
 constexpr int kTileM = 128;
 constexpr int kTileK = 64;
 
@@ -84,6 +87,14 @@ cudaError_t launch_splitk_reduce(const float *part, const int *nseg, const float
                                  int K, int B, int32_t *rpos_advance, int conv_k, cudaStream_t st);
 constexpr int kTcMinBatch = 8;
 constexpr size_t kOpTile = 16384;  // bytes of one packed B-operand tile (64 seqs x 64 k, hi+lo)
+// Byte offset, inside a packed B-operand tile (128 operand rows x 64 bf16;
+// row 2b = hi, row 2b+1 = lo of sequence b), of the 16-byte chunk holding
+// k 8*kc .. 8*kc+7 of operand row `row`.  The tile uses the 128-byte swizzled
+// K-major layout: each row's 128 bytes contiguous, 8-row groups 1024 bytes
+// apart, chunk kc of row r at chunk position kc ^ (r & 7).
+__host__ __device__ __forceinline__ uint32_t op_chunk_offset(int row, int kc) {
+    return (uint32_t)(row >> 3) * 1024u + (uint32_t)(row & 7) * 128u + ((uint32_t)(kc ^ (row & 7)) << 4);
+}
 
 // The fused conv / L2 / gated-delta / readout / gated-RMSNorm step.
 // The in_proj result is read as the sum of its segment partials (part_in,
