@@ -36,11 +36,12 @@
 // A pipeline stage is 128 rows x 128 k (16 KB of int8 weights, one bulk copy:
 // copies this size keep the per-stage hand-off cost small against the HBM
 // time).  Roles: warp 0 issues the bulk copies, warp 1 (one thread) the
-// MMAs, warps 2-9 convert the int8 unit to bf16 into one of two tensor-memory
-// A buffers (warp w owns lane quarter w % 4 and k tile (w - 2) / 4 of the
-// unit: one row per lane), warps 10-13 read the accumulators (tcgen05.ld) and
-// write results.  Tensor memory: accumulators in columns 0-255, A buffers in
-// 256-383.  The weight copies of the first stages go out before the kernel
+// MMAs, warps 2-17 convert the int8 unit to bf16 into one of four
+// tensor-memory A buffers (warp w owns lane quarter w % 4 and 32 k of the
+// unit: one row per lane), warps 18-21 read the accumulators (tcgen05.ld) and
+// write results.  Tensor memory (all 512 columns): accumulators in columns
+// 0-255, A buffers in 256-511, so conversion runs up to three units ahead of
+// the MMAs.  The weight copies of the first stages go out before the kernel
 // waits for the previous kernel of the step (programmatic dependent launch):
 // weights are read-only, the activations and the partial buffers are not.
 // Every wait is bounded (about one second of the global timer): on timeout
@@ -61,15 +62,22 @@ constexpr int BK = 64;           // k per weight tile
 constexpr int KU = 2;            // k tiles per unit / pipeline stage (128 k)
 constexpr int STAGES = 4;
 constexpr int NB_CHUNK = 64;     // sequences per batch chunk (MMA N <= 128)
-constexpr int kThreads = 448;    // 14 warps
-constexpr int kConvThreads = 256;
+constexpr int kConvWarps = 16;
+constexpr int kThreads = 32 * (2 + kConvWarps + 4);  // 22 warps
+constexpr int kConvThreads = 32 * kConvWarps;
+constexpr int kEpiWarp0 = 2 + kConvWarps;
+constexpr int NABUF = 4;                             // tensor-memory A buffers
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kATileBytes = BM * BK;            // 8 KB int8
 constexpr uint32_t kOpTileBytes = 128 * BK * 2;      // 16 KB bf16
-constexpr uint32_t kTmemCols = 512;                  // 2 accumulators x 128 + 2 A buffers x 64
+constexpr uint32_t kTmemCols = 512;                  // 2 accumulators x 128 + 4 A buffers x 64
 constexpr uint32_t kTmemA = 256;                     // first column of the A buffers
 constexpr uint32_t kACols = KU * BK / 2;             // 64: bf16 pairs of a 128-k unit
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
+// A waiting thread is suspended until the phase completes or this many ns
+// pass, so waiting warps leave the issue slots to the working ones (the
+// single MMA-issuing thread above all).
+constexpr uint32_t kSuspendHintNs = 20000;
 
 // A unit (= pipeline stage) is 128 rows x 128 k: two 64-k tiles.
 struct __align__(1024) GemmSmem {
@@ -77,8 +85,8 @@ struct __align__(1024) GemmSmem {
     uint8_t a8[STAGES][KU * kATileBytes];    // int8 A as copied (4 x 16 KB)
     uint64_t full[STAGES];                   // bulk copies of the stage landed
     uint64_t empty[STAGES];                  // MMAs done reading the stage
-    uint64_t conv[2];                        // A converted into tensor-memory buffer 0 / 1
-    uint64_t a_free[2];                      // MMAs done reading tensor-memory A buffer 0 / 1
+    uint64_t conv[NABUF];                    // A converted into tensor-memory buffer i
+    uint64_t a_free[NABUF];                  // MMAs done reading tensor-memory A buffer i
     uint64_t acc_full[2];               // accumulator ready for the epilogue
     uint64_t acc_empty[2];              // epilogue done reading the accumulator
     uint64_t drain;                     // all MMAs of this CTA completed
@@ -123,10 +131,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
         : "memory");
     return ok != 0;
 }
@@ -187,15 +195,24 @@ __device__ __forceinline__ uint32_t instr_desc(int M, int N) {
            ((uint32_t)(M >> 4) << 24);
 }
 
-// D (tensor memory) (+)= A (tensor memory, lane = row, 32-bit column = two
-// consecutive k) x B (shared memory descriptor)^T
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                            uint32_t idesc, uint32_t accumulate) {
+// Four K steps of 16: D (tensor memory) (+)= A (tensor memory, lane = row,
+// 32-bit column = two consecutive k; 8 columns per step) x B (shared-memory
+// descriptor, 32 bytes further per step)^T.  The first step overwrites D
+// when `accumulate` is 0.  One asm block with precomputed operands: for
+// 128 x 128 x 16 steps the issuing thread's own instruction count, not the
+// tensor core, otherwise sets the pace.
+__device__ __forceinline__ void mma_bf16_ts_x4(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        "setp.eq.b32 q, %4, %4;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %6, %3, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %3, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %10, %3, q;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(a_tmem + 8u), "l"(bdesc + 2u),
+        "r"(a_tmem + 16u), "l"(bdesc + 4u), "r"(a_tmem + 24u), "l"(bdesc + 6u)
         : "memory");
 }
 
@@ -220,17 +237,14 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// 32 consecutive 32-bit columns of this thread's tensor-memory lane, then
+// 16 consecutive 32-bit columns of this thread's tensor-memory lane, then
 // wait until the stores are done
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t v[32]) {
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t v[16]) {
     asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
         "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
-        "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
-        "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
         : "memory");
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -273,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_i8_tc_kernel(const GemmParam
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], 1);
         }
-        for (int a = 0; a < 2; ++a) {
+        for (int a = 0; a < NABUF; ++a) {
             mbar_init(&sm.conv[a], kConvThreads);
             mbar_init(&sm.a_free[a], 1);
         }
@@ -362,20 +376,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_i8_tc_kernel(const GemmParam
                 const uint32_t dtm = tmem + (uint32_t)(a * 128);
                 const int useg = u;  // first unit of this segment: overwrite the accumulator
                 for (; u < ue; ++u, ++it) {
-                    const int st = it % STAGES, ab = it & 1;
-                    if (!mbar_wait(&sm.conv[ab], (it >> 1) & 1, abort_flag)) {
+                    const int st = it % STAGES, ab = it % NABUF;
+                    if (!mbar_wait(&sm.conv[ab], (it / NABUF) & 1, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const int nk = min(KU, p.KT - (u % p.UT) * KU);
-                    const uint32_t ta = tmem + kTmemA + (uint32_t)ab * kACols, b0 = smem_u32(sm.b16[st]);
-                    for (int kk = 0; kk < nk * (BK / 16); ++kk) {
-                        // K step of 16: 8 tensor-memory columns of A, 32 bytes of B's rows
-                        const uint64_t bd = smem_desc_sw128(b0 + (uint32_t)(kk >> 2) * kOpTileBytes +
-                                                            (uint32_t)(kk & 3) * 32u);
-                        mma_bf16_ts(dtm, ta + (uint32_t)kk * 8u, bd, idesc, (u == useg && kk == 0) ? 0u : 1u);
-                    }
+                    // K steps of 16: 8 tensor-memory columns of A and 32 bytes of
+                    // B's rows (+2 in the descriptor's address field) each; the
+                    // second 64-k tile's B starts 16 KB (+1024) further
+                    const uint32_t ta = tmem + kTmemA + (uint32_t)ab * kACols;
+                    const uint64_t bd = smem_desc_sw128(smem_u32(sm.b16[st]));
+                    mma_bf16_ts_x4(dtm, ta, bd, idesc, u == useg ? 0u : 1u);
+                    if ((u % p.UT) * KU + 1 < p.KT) mma_bf16_ts_x4(dtm, ta + 32u, bd + 1024u, idesc, 1u);
                     mma_commit(&sm.empty[st]);
                     mma_commit(&sm.a_free[ab]);
                 }
@@ -386,47 +399,43 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_i8_tc_kernel(const GemmParam
             mma_commit(&sm.drain);  // arrives once every MMA issued above has completed
             mbar_wait(&sm.drain, 0, abort_flag, true);
         }
-    } else if (warp < 10) {
-        // ---- int8 -> bf16 converters: lane = row of the unit's k tile kh ---------
-        const int quarter = warp & 3, kh = (warp - 2) >> 2;
+    } else if (warp < kEpiWarp0) {
+        // ---- int8 -> bf16 converters: lane = row; warp group g = (w - 2) / 4
+        //      takes k parts 2(g&1), 2(g&1)+1 of the unit's k tile g/2 -------------
+        const int quarter = warp & 3, g = (warp - 2) >> 2, kh = g >> 1, kq = g & 1;
         const int row = quarter * 32 + lane;
         const uint32_t tlane = (uint32_t)(quarter * 32) << 16;
         for (int u = u0; u < u1; ++u) {
-            const int it = u - u0, st = it % STAGES, ab = it & 1;
+            const int it = u - u0, st = it % STAGES, ab = it % NABUF;
             if (!mbar_wait(&sm.full[st], (it / STAGES) & 1, abort_flag) ||
-                (it >= 2 && !mbar_wait(&sm.a_free[ab], ((it >> 1) - 1) & 1, abort_flag))) {
+                (it >= NABUF && !mbar_wait(&sm.a_free[ab], ((it / NABUF) - 1) & 1, abort_flag))) {
                 *abort_flag = 1;
                 break;
             }
             const int nk = min(KU, p.KT - (u % p.UT) * KU);
             if (kh < nk) {  // warp-uniform
-                // the row's 4 k parts: 16 bytes each, 2 KB apart (lanes read 512
-                // contiguous bytes per part)
-                const uint8_t *src = sm.a8[st] + kh * kATileBytes + row * 16;
-                uint4 w[4];
-#pragma unroll
-                for (int kp = 0; kp < 4; ++kp) w[kp] = *reinterpret_cast<const uint4 *>(src + kp * 2048);
-                uint32_t v[32];  // bf16 pairs (k even, k odd) of the row's 64 k, in k order
-#pragma unroll
-                for (int kp = 0; kp < 4; ++kp) {
-                    const uint2 e0 = i8x4_to_bf16x4(w[kp].x), e1 = i8x4_to_bf16x4(w[kp].y);
-                    const uint2 e2 = i8x4_to_bf16x4(w[kp].z), e3 = i8x4_to_bf16x4(w[kp].w);
-                    v[kp * 8 + 0] = e0.x;
-                    v[kp * 8 + 1] = e0.y;
-                    v[kp * 8 + 2] = e1.x;
-                    v[kp * 8 + 3] = e1.y;
-                    v[kp * 8 + 4] = e2.x;
-                    v[kp * 8 + 5] = e2.y;
-                    v[kp * 8 + 6] = e3.x;
-                    v[kp * 8 + 7] = e3.y;
-                }
-                tmem_st32(tmem + tlane + kTmemA + (uint32_t)ab * kACols + (uint32_t)kh * 32u, v);
+                // 16 bytes of each of the row's two k parts, 2 KB apart (the lanes
+                // read 512 contiguous bytes per part)
+                const uint8_t *src = sm.a8[st] + kh * kATileBytes + (2 * kq) * 2048 + row * 16;
+                const uint4 w0 = *reinterpret_cast<const uint4 *>(src);
+                const uint4 w1 = *reinterpret_cast<const uint4 *>(src + 2048);
+                uint32_t v[16];  // bf16 pairs (k even, k odd) of the row's 32 k, in k order
+                uint2 e;
+                e = i8x4_to_bf16x4(w0.x); v[0] = e.x; v[1] = e.y;
+                e = i8x4_to_bf16x4(w0.y); v[2] = e.x; v[3] = e.y;
+                e = i8x4_to_bf16x4(w0.z); v[4] = e.x; v[5] = e.y;
+                e = i8x4_to_bf16x4(w0.w); v[6] = e.x; v[7] = e.y;
+                e = i8x4_to_bf16x4(w1.x); v[8] = e.x; v[9] = e.y;
+                e = i8x4_to_bf16x4(w1.y); v[10] = e.x; v[11] = e.y;
+                e = i8x4_to_bf16x4(w1.z); v[12] = e.x; v[13] = e.y;
+                e = i8x4_to_bf16x4(w1.w); v[14] = e.x; v[15] = e.y;
+                tmem_st16(tmem + tlane + kTmemA + (uint32_t)ab * kACols + (uint32_t)(kh * 32 + kq * 16), v);
             }
             tc_fence_before();
             mbar_arrive(&sm.conv[ab]);
         }
     } else {
-        // ---- epilogue: warps 10..13 read TMEM lane quarters 2, 3, 0, 1 ------------
+        // ---- epilogue: warps 18..21 read TMEM lane quarters 2, 3, 0, 1 ------------
         pdl_wait();  // the partial buffers may still be read by the previous kernel
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;
