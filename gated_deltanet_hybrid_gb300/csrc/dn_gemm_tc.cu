@@ -33,17 +33,21 @@
 // core kernel for the in_proj, splitk_reduce_kernel for the out_proj), so
 // results do not depend on scheduling and no CTA waits on another.
 //
-// A pipeline stage is 128 rows x 128 k (16 KB of int8 weights, one bulk copy:
-// copies this size keep the per-stage hand-off cost small against the HBM
-// time).  Roles: warp 0 issues the bulk copies, warp 1 (one thread) the
-// MMAs, warps 2-17 convert the int8 unit to bf16 into one of four
-// tensor-memory A buffers (warp w owns lane quarter w % 4 and 32 k of the
-// unit: one row per lane), warps 18-21 read the accumulators (tcgen05.ld) and
-// write results.  Tensor memory (all 512 columns): accumulators in columns
-// 0-255, A buffers in 256-511, so conversion runs up to three units ahead of
-// the MMAs.  The weight copies of the first stages go out before the kernel
-// waits for the previous kernel of the step (programmatic dependent launch):
-// weights are read-only, the activations and the partial buffers are not.
+// A unit is 128 rows x 128 k (16 KB of int8 weights, one bulk copy: copies
+// this size keep the per-copy hand-off cost small against the HBM time).
+// Weights and activations stream through separate shared-memory rings: the
+// converters free a weight stage as soon as they hold its bytes in
+// registers, so up to six weight copies are in flight per SM however long
+// the MMAs of a unit take; activation stages are freed by the MMAs.
+// Roles: warp 0 copies weights, warp 22 copies activations, warp 1 (one
+// thread) issues the MMAs, warps 2-17 convert the int8 unit to bf16 into one
+// of four tensor-memory A buffers (warp w owns lane quarter w % 4 and 32 k of
+// the unit: one row per lane), warps 18-21 read the accumulators
+// (tcgen05.ld) and write results.  Tensor memory (all 512 columns):
+// accumulators in columns 0-255, A buffers in 256-511, so conversion runs up
+// to three units ahead of the MMAs.  The weight producer does not wait for
+// the previous kernel of the step (programmatic dependent launch): weights
+// are read-only, the activations and the partial buffers are not.
 // Every wait is bounded (about one second of the global timer): on timeout
 // the kernel records an error in `err`, waits (bounded) for its own copies
 // and MMAs in flight, frees its tensor memory and returns.
@@ -59,37 +63,42 @@ namespace {
 
 constexpr int BM = 128;          // weight rows per tile (MMA M)
 constexpr int BK = 64;           // k per weight tile
-constexpr int KU = 2;            // k tiles per unit / pipeline stage (128 k)
-constexpr int STAGES = 4;
+constexpr int KU = 2;            // k tiles per unit (128 k)
+constexpr int AST = 3;           // int8 weight stages (2 row tiles x 16 KB)
+constexpr int BST = 3;           // bf16 activation stages (32 KB)
 constexpr int NB_CHUNK = 64;     // sequences per batch chunk (MMA N <= 128)
 constexpr int kConvWarps = 16;
-constexpr int kThreads = 32 * (2 + kConvWarps + 4);  // 22 warps
-constexpr int kConvThreads = 32 * kConvWarps;
+constexpr int kEpiWarps = 8;
 constexpr int kEpiWarp0 = 2 + kConvWarps;
-constexpr int NABUF = 4;                             // tensor-memory A buffers
-constexpr int kEpiThreads = 128;
+constexpr int kBProdWarp = kEpiWarp0 + kEpiWarps;
+constexpr int kThreads = 32 * (kBProdWarp + 1);      // 27 warps
+constexpr int NABUF = 2;                             // tensor-memory A buffers (one pair unit each)
 constexpr uint32_t kATileBytes = BM * BK;            // 8 KB int8
+constexpr uint32_t kAUnitBytes = KU * kATileBytes;   // 16 KB: one row tile of a unit
 constexpr uint32_t kOpTileBytes = 128 * BK * 2;      // 16 KB bf16
-constexpr uint32_t kTmemCols = 512;                  // 2 accumulators x 128 + 4 A buffers x 64
+constexpr uint32_t kTmemCols = 512;                  // 2 accumulators x 128 + 2 A buffers x 128
 constexpr uint32_t kTmemA = 256;                     // first column of the A buffers
-constexpr uint32_t kACols = KU * BK / 2;             // 64: bf16 pairs of a 128-k unit
+constexpr uint32_t kACols = 2 * KU * BK / 2;         // 128: bf16 pairs of two 128-k row tiles
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 // A waiting thread is suspended until the phase completes or this many ns
 // pass, so waiting warps leave the issue slots to the working ones (the
 // single MMA-issuing thread above all).
 constexpr uint32_t kSuspendHintNs = 20000;
 
-// A unit (= pipeline stage) is 128 rows x 128 k: two 64-k tiles.
+// A unit is 2 row tiles x 128 k: 2 x 16 KB of int8 weights and one 32 KB
+// activation tile that both row tiles use.
 struct __align__(1024) GemmSmem {
-    uint8_t b16[STAGES][KU * kOpTileBytes];  // bf16 B operand as copied (4 x 32 KB)
-    uint8_t a8[STAGES][KU * kATileBytes];    // int8 A as copied (4 x 16 KB)
-    uint64_t full[STAGES];                   // bulk copies of the stage landed
-    uint64_t empty[STAGES];                  // MMAs done reading the stage
-    uint64_t conv[NABUF];                    // A converted into tensor-memory buffer i
+    uint8_t b16[BST][KU * kOpTileBytes];     // bf16 B operand as copied (3 x 32 KB)
+    uint8_t a8[AST][2][kAUnitBytes];         // int8 A as copied (3 x 2 x 16 KB)
+    uint64_t a_full[AST];                    // weight copies of the stage landed
+    uint64_t a_empty[AST];                   // converters done reading the stage (one arrival per warp)
+    uint64_t b_full[BST];                    // activation copies of the stage landed
+    uint64_t b_empty[BST];                   // MMAs done reading the stage
+    uint64_t conv[NABUF];                    // A converted into tensor-memory buffer i (one arrival per converter warp)
     uint64_t a_free[NABUF];                  // MMAs done reading tensor-memory A buffer i
-    uint64_t acc_full[2];               // accumulator ready for the epilogue
-    uint64_t acc_empty[2];              // epilogue done reading the accumulator
-    uint64_t drain;                     // all MMAs of this CTA completed
+    uint64_t acc_full;                       // accumulators ready for the epilogue
+    uint64_t acc_empty;                      // epilogue done reading the accumulators (one arrival per warp)
+    uint64_t drain;                          // all MMAs of this CTA completed
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -100,7 +109,8 @@ struct GemmParams {
     float *part;         // [tiles][max_seg][64][128] segment partials (unscaled)
     int *nseg;           // [tiles] segment count, written by each tile's last segment
     int *err;
-    int M, MT, KT, UT, B, nchunks, U, G, max_seg;  // KT: k tiles; UT: units per row tile
+    int M, MT, MP, TP, KT, UT, B, nchunks, U, G, max_seg;  // MP row-tile groups of TP (1 or 2) tiles;
+                                                          // KT: k tiles; UT: units per group
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -237,14 +247,17 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// 16 consecutive 32-bit columns of this thread's tensor-memory lane, then
+// 32 consecutive 32-bit columns of this thread's tensor-memory lane, then
 // wait until the stores are done
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t v[16]) {
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t v[32]) {
     asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
         "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+        "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
+        "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
         : "memory");
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -283,18 +296,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_i8_tc_kernel(const GemmParam
     const int u0 = unit_start(c, p), u1 = unit_start(c + 1, p);
 
     if (tid == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.empty[s], 1);
+        for (int s = 0; s < AST; ++s) {
+            mbar_init(&sm.a_full[s], 1);
+            mbar_init(&sm.a_empty[s], kConvWarps);
+        }
+        for (int s = 0; s < BST; ++s) {
+            mbar_init(&sm.b_full[s], 1);
+            mbar_init(&sm.b_empty[s], 1);
         }
         for (int a = 0; a < NABUF; ++a) {
-            mbar_init(&sm.conv[a], kConvThreads);
+            mbar_init(&sm.conv[a], kConvWarps);
             mbar_init(&sm.a_free[a], 1);
         }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(&sm.acc_full[a], 1);
-            mbar_init(&sm.acc_empty[a], kEpiThreads);
-        }
+        mbar_init(&sm.acc_full, 1);
+        mbar_init(&sm.acc_empty, kEpiWarps);
         mbar_init(&sm.drain, 1);
         sm.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -312,48 +327,58 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_i8_tc_kernel(const GemmParam
     const uint32_t tmem = sm.tmem_base;
     volatile int *abort_flag = &sm.abort_flag;
 
+    // unit u: row-tile pair pi = u / UT (pi = chunk * MP + pair: tiles 2 pair,
+    // 2 pair + 1), k tiles (u % UT) * KU ...
     if (warp == 0) {
-        // ---- bulk-copy producer ---------------------------------------------
+        // ---- weight producer: read-only data, so it runs ahead of the previous
+        //      kernel of the step (no wait on it) ------------------------------
         if (lane == 0) {
-            // weights of the first stages before waiting for the previous kernel
-            const int n_pre = min(STAGES, u1 - u0);
-            for (int it = 0; it < n_pre; ++it) {
-                const int u = u0 + it;
-                const int tile = u / p.UT, kt0 = (u % p.UT) * KU;
-                const int chunk = tile / p.MT, mt = tile % p.MT;
-                const int nk = min(KU, p.KT - kt0);
-                const int N = 2 * ((chunk_rows(chunk, p) + 7) & ~7);
-                mbar_arrive_expect_tx(&sm.full[it], (uint32_t)nk * (kATileBytes + (uint32_t)N * 128u));
-                bulk_g2s(smem_u32(sm.a8[it]), p.Wt + ((size_t)mt * p.KT + kt0) * kATileBytes,
-                         (uint32_t)nk * kATileBytes, &sm.full[it]);
-            }
-            pdl_wait();
-            pdl_trigger();
-            int issued = n_pre;  // stages whose last issued copy may still be in flight
+            int issued = 0;  // copies issued; the last AST may still be in flight
             for (int u = u0; u < u1; ++u) {
-                const int it = u - u0, st = it % STAGES;
-                const int tile = u / p.UT, kt0 = (u % p.UT) * KU;
-                const int chunk = tile / p.MT, mt = tile % p.MT;
+                const int it = u - u0, sa = it % AST;
+                const int pi = u / p.UT, kt0 = (u % p.UT) * KU;
+                const int mt0 = p.TP * (pi % p.MP), ntl = min(p.TP, p.MT - mt0);
                 const int nk = min(KU, p.KT - kt0);
-                const int N = 2 * ((chunk_rows(chunk, p) + 7) & ~7);
-                if (it >= n_pre) {
-                    if (!mbar_wait(&sm.empty[st], ((it / STAGES) - 1) & 1, abort_flag)) {
-                        *abort_flag = 1;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&sm.full[st], (uint32_t)nk * (kATileBytes + (uint32_t)N * 128u));
-                    bulk_g2s(smem_u32(sm.a8[st]), p.Wt + ((size_t)mt * p.KT + kt0) * kATileBytes,
-                             (uint32_t)nk * kATileBytes, &sm.full[st]);
-                    issued = it + 1;
+                if (it >= AST && !mbar_wait(&sm.a_empty[sa], ((it / AST) - 1) & 1, abort_flag)) {
+                    *abort_flag = 1;
+                    break;
                 }
-                for (int i = 0; i < nk; ++i)
-                    bulk_g2s(smem_u32(sm.b16[st]) + (uint32_t)i * kOpTileBytes,
-                             p.xb + ((size_t)chunk * p.KT + kt0 + i) * kOpTileBytes, (uint32_t)N * 128u,
-                             &sm.full[st]);
+                mbar_arrive_expect_tx(&sm.a_full[sa], (uint32_t)(ntl * nk) * kATileBytes);
+                for (int tp = 0; tp < ntl; ++tp)
+                    bulk_g2s(smem_u32(sm.a8[sa][tp]), p.Wt + ((size_t)(mt0 + tp) * p.KT + kt0) * kATileBytes,
+                             (uint32_t)nk * kATileBytes, &sm.a_full[sa]);
+                issued = it + 1;
             }
             if (*abort_flag) {  // let every copy still in flight land before exiting
-                for (int it = max(0, issued - STAGES); it < issued; ++it)
-                    mbar_wait(&sm.full[it % STAGES], (it / STAGES) & 1, abort_flag, true);
+                for (int it = max(0, issued - AST); it < issued; ++it)
+                    mbar_wait(&sm.a_full[it % AST], (it / AST) & 1, abort_flag, true);
+            }
+        }
+    } else if (warp == kBProdWarp) {
+        // ---- activation producer: after the previous kernel (which may write them)
+        if (lane == 0) {
+            pdl_wait();
+            pdl_trigger();
+            int issued = 0;
+            for (int u = u0; u < u1; ++u) {
+                const int it = u - u0, sb = it % BST;
+                const int chunk = (u / p.UT) / p.MP, kt0 = (u % p.UT) * KU;
+                const int nk = min(KU, p.KT - kt0);
+                const int N = 2 * ((chunk_rows(chunk, p) + 7) & ~7);
+                if (it >= BST && !mbar_wait(&sm.b_empty[sb], ((it / BST) - 1) & 1, abort_flag)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                mbar_arrive_expect_tx(&sm.b_full[sb], (uint32_t)nk * (uint32_t)N * 128u);
+                for (int i = 0; i < nk; ++i)
+                    bulk_g2s(smem_u32(sm.b16[sb]) + (uint32_t)i * kOpTileBytes,
+                             p.xb + ((size_t)chunk * p.KT + kt0 + i) * kOpTileBytes, (uint32_t)N * 128u,
+                             &sm.b_full[sb]);
+                issued = it + 1;
+            }
+            if (*abort_flag) {
+                for (int it = max(0, issued - BST); it < issued; ++it)
+                    mbar_wait(&sm.b_full[it % BST], (it / BST) & 1, abort_flag, true);
             }
         }
     } else if (warp == 1) {
@@ -362,38 +387,45 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_i8_tc_kernel(const GemmParam
             int it = 0, seg = 0;
             bool ok = true;
             for (int u = u0; u < u1 && ok; ++seg) {
-                const int tile = u / p.UT;
-                const int ue = min(u1, (tile + 1) * p.UT);
-                const int chunk = tile / p.MT;
+                const int pi = u / p.UT;
+                const int ue = min(u1, (pi + 1) * p.UT);
+                const int chunk = pi / p.MP, mt0 = p.TP * (pi % p.MP), ntl = min(p.TP, p.MT - mt0);
                 const int N = 2 * ((chunk_rows(chunk, p) + 7) & ~7);
                 const uint32_t idesc = instr_desc(BM, N);
-                const int a = seg & 1;
-                if (seg >= 2 && !mbar_wait(&sm.acc_empty[a], ((seg >> 1) - 1) & 1, abort_flag)) {
+                // the accumulators are free once the epilogue has read the last segment's
+                if (seg >= 1 && !mbar_wait(&sm.acc_empty, (seg - 1) & 1, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t dtm = tmem + (uint32_t)(a * 128);
-                const int useg = u;  // first unit of this segment: overwrite the accumulator
+                const int useg = u;  // first unit of this segment: overwrite the accumulators
                 for (; u < ue; ++u, ++it) {
-                    const int st = it % STAGES, ab = it % NABUF;
-                    if (!mbar_wait(&sm.conv[ab], (it / NABUF) & 1, abort_flag)) {
+                    const int sb = it % BST, ab = it % NABUF;
+                    if (!mbar_wait(&sm.conv[ab], (it / NABUF) & 1, abort_flag) ||
+                        !mbar_wait(&sm.b_full[sb], (it / BST) & 1, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     // K steps of 16: 8 tensor-memory columns of A and 32 bytes of
                     // B's rows (+2 in the descriptor's address field) each; the
-                    // second 64-k tile's B starts 16 KB (+1024) further
+                    // second 64-k tile's B starts 16 KB (+1024) further.  Row tile
+                    // tp of the pair: accumulator columns 128 tp, A columns 64 tp.
                     const uint32_t ta = tmem + kTmemA + (uint32_t)ab * kACols;
-                    const uint64_t bd = smem_desc_sw128(smem_u32(sm.b16[st]));
-                    mma_bf16_ts_x4(dtm, ta, bd, idesc, u == useg ? 0u : 1u);
-                    if ((u % p.UT) * KU + 1 < p.KT) mma_bf16_ts_x4(dtm, ta + 32u, bd + 1024u, idesc, 1u);
-                    mma_commit(&sm.empty[st]);
+                    const uint64_t bd = smem_desc_sw128(smem_u32(sm.b16[sb]));
+                    const bool two_k = (u % p.UT) * KU + 1 < p.KT;
+                    const uint32_t acc0 = u == useg ? 0u : 1u;
+                    mma_bf16_ts_x4(tmem, ta, bd, idesc, acc0);
+                    if (two_k) mma_bf16_ts_x4(tmem, ta + 32u, bd + 1024u, idesc, 1u);
+                    if (ntl == 2) {
+                        mma_bf16_ts_x4(tmem + 128u, ta + 64u, bd, idesc, acc0);
+                        if (two_k) mma_bf16_ts_x4(tmem + 128u, ta + 96u, bd + 1024u, idesc, 1u);
+                    }
+                    mma_commit(&sm.b_empty[sb]);
                     mma_commit(&sm.a_free[ab]);
                 }
                 if (!ok) break;
-                mma_commit(&sm.acc_full[a]);
+                mma_commit(&sm.acc_full);
             }
             if (!ok) *abort_flag = 1;
             mma_commit(&sm.drain);  // arrives once every MMA issued above has completed
@@ -401,78 +433,101 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_i8_tc_kernel(const GemmParam
         }
     } else if (warp < kEpiWarp0) {
         // ---- int8 -> bf16 converters: lane = row; warp group g = (w - 2) / 4
-        //      takes k parts 2(g&1), 2(g&1)+1 of the unit's k tile g/2 -------------
-        const int quarter = warp & 3, g = (warp - 2) >> 2, kh = g >> 1, kq = g & 1;
+        //      takes k tile g % 2 of row tile g / 2 of the pair ---------------------
+        const int quarter = warp & 3, g = (warp - 2) >> 2, tp = g >> 1, kh = g & 1;
         const int row = quarter * 32 + lane;
         const uint32_t tlane = (uint32_t)(quarter * 32) << 16;
         for (int u = u0; u < u1; ++u) {
-            const int it = u - u0, st = it % STAGES, ab = it % NABUF;
-            if (!mbar_wait(&sm.full[st], (it / STAGES) & 1, abort_flag) ||
+            const int it = u - u0, sa = it % AST, ab = it % NABUF;
+            if (!mbar_wait(&sm.a_full[sa], (it / AST) & 1, abort_flag) ||
                 (it >= NABUF && !mbar_wait(&sm.a_free[ab], ((it / NABUF) - 1) & 1, abort_flag))) {
                 *abort_flag = 1;
                 break;
             }
-            const int nk = min(KU, p.KT - (u % p.UT) * KU);
-            if (kh < nk) {  // warp-uniform
-                // 16 bytes of each of the row's two k parts, 2 KB apart (the lanes
-                // read 512 contiguous bytes per part)
-                const uint8_t *src = sm.a8[st] + kh * kATileBytes + (2 * kq) * 2048 + row * 16;
-                const uint4 w0 = *reinterpret_cast<const uint4 *>(src);
-                const uint4 w1 = *reinterpret_cast<const uint4 *>(src + 2048);
-                uint32_t v[16];  // bf16 pairs (k even, k odd) of the row's 32 k, in k order
-                uint2 e;
-                e = i8x4_to_bf16x4(w0.x); v[0] = e.x; v[1] = e.y;
-                e = i8x4_to_bf16x4(w0.y); v[2] = e.x; v[3] = e.y;
-                e = i8x4_to_bf16x4(w0.z); v[4] = e.x; v[5] = e.y;
-                e = i8x4_to_bf16x4(w0.w); v[6] = e.x; v[7] = e.y;
-                e = i8x4_to_bf16x4(w1.x); v[8] = e.x; v[9] = e.y;
-                e = i8x4_to_bf16x4(w1.y); v[10] = e.x; v[11] = e.y;
-                e = i8x4_to_bf16x4(w1.z); v[12] = e.x; v[13] = e.y;
-                e = i8x4_to_bf16x4(w1.w); v[14] = e.x; v[15] = e.y;
-                tmem_st16(tmem + tlane + kTmemA + (uint32_t)ab * kACols + (uint32_t)(kh * 32 + kq * 16), v);
+            const int mt0 = p.TP * ((u / p.UT) % p.MP);
+            const bool mine = tp < min(p.TP, p.MT - mt0) && kh < min(KU, p.KT - (u % p.UT) * KU);  // warp-uniform
+            uint4 w[4];
+#pragma unroll
+            for (int kp = 0; kp < 4; ++kp) w[kp] = make_uint4(0, 0, 0, 0);
+            if (mine) {
+                // the row's 4 k parts: 16 bytes each, 2 KB apart (the lanes read 512
+                // contiguous bytes per part)
+                const uint8_t *src = sm.a8[sa][tp] + kh * kATileBytes + row * 16;
+#pragma unroll
+                for (int kp = 0; kp < 4; ++kp) w[kp] = *reinterpret_cast<const uint4 *>(src + kp * 2048);
             }
+            // the weight stage is free once every warp has its bytes in registers
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.a_empty[sa]);
+            if (mine) {
+                uint32_t v[32];  // bf16 pairs (k even, k odd) of the row's 64 k, in k order
+#pragma unroll
+                for (int kp = 0; kp < 4; ++kp) {
+                    uint2 e;
+                    e = i8x4_to_bf16x4(w[kp].x);
+                    v[kp * 8 + 0] = e.x;
+                    v[kp * 8 + 1] = e.y;
+                    e = i8x4_to_bf16x4(w[kp].y);
+                    v[kp * 8 + 2] = e.x;
+                    v[kp * 8 + 3] = e.y;
+                    e = i8x4_to_bf16x4(w[kp].z);
+                    v[kp * 8 + 4] = e.x;
+                    v[kp * 8 + 5] = e.y;
+                    e = i8x4_to_bf16x4(w[kp].w);
+                    v[kp * 8 + 6] = e.x;
+                    v[kp * 8 + 7] = e.y;
+                }
+                tmem_st32(tmem + tlane + kTmemA + (uint32_t)ab * kACols + (uint32_t)(tp * 64 + kh * 32), v);
+            }
+            // one arrival per warp: every lane's stores are complete (wait::st)
+            // and fenced before the warp converges and lane 0 arrives
             tc_fence_before();
-            mbar_arrive(&sm.conv[ab]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.conv[ab]);
         }
     } else {
-        // ---- epilogue: warps 18..21 read TMEM lane quarters 2, 3, 0, 1 ------------
+        // ---- epilogue: warps 18..25; warp w reads lane quarter w % 4 of the
+        //      accumulator of row tile (w - 18) / 4 --------------------------------
         pdl_wait();  // the partial buffers may still be read by the previous kernel
-        const int quarter = warp & 3;
+        const int quarter = warp & 3, tp = (warp - kEpiWarp0) >> 2;
         const int r = quarter * 32 + lane;
-        const SchedView sv{p.U, p.G, p.UT, p.MT, p.max_seg};
+        const SchedView sv{p.U, p.G, p.UT, p.MP, p.max_seg};
         int seg = 0;
         for (int u = u0; u < u1; ++seg) {
-            const int tile = u / p.UT;
-            u = min(u1, (tile + 1) * p.UT);
-            const int chunk = tile / p.MT;
+            const int pi = u / p.UT;
+            u = min(u1, (pi + 1) * p.UT);
+            const int chunk = pi / p.MP, mt0 = p.TP * (pi % p.MP), ntl = min(p.TP, p.MT - mt0);
             const int Bc = chunk_rows(chunk, p);
             const int N = 2 * ((Bc + 7) & ~7);
-            const int a = seg & 1;
-            const int slot = c - sched_cta_of_unit(tile * p.UT, sv);
-            if (quarter == 0 && lane == 0 && u1 >= (tile + 1) * p.UT) p.nseg[tile] = slot + 1;
-            bool ok = mbar_wait(&sm.acc_full[a], (seg >> 1) & 1, abort_flag);
+            const int slot = c - sched_cta_of_unit(pi * p.UT, sv);
+            bool ok = mbar_wait(&sm.acc_full, seg & 1, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
                 *abort_flag = 1;
                 break;
             }
             tc_fence_after();
-            const uint32_t trow = tmem + (uint32_t)(a * 128) + ((uint32_t)(quarter * 32) << 16);
-            float *pslot = p.part + ((size_t)tile * p.max_seg + slot) * (NB_CHUNK * BM);
+            if (tp < ntl) {
+                const int tile = chunk * p.MT + mt0 + tp;
+                if (quarter == 0 && lane == 0 && u1 >= (pi + 1) * p.UT) p.nseg[tile] = slot + 1;
+                const uint32_t trow = tmem + (uint32_t)(tp * 128) + ((uint32_t)(quarter * 32) << 16);
+                float *pslot = p.part + ((size_t)tile * p.max_seg + slot) * (NB_CHUNK * BM);
 #pragma unroll
-            for (int c16 = 0; c16 < 8; ++c16) {
-                if (c16 * 16 < N) {  // warp-uniform
-                    float v[16];
-                    tmem_ld16(trow + c16 * 16, v);
+                for (int c16 = 0; c16 < 8; ++c16) {
+                    if (c16 * 16 < N) {  // warp-uniform
+                        float v[16];
+                        tmem_ld16(trow + c16 * 16, v);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int b = c16 * 8 + j;
-                        if (b < Bc) pslot[b * BM + r] = v[2 * j] + v[2 * j + 1];
+                        for (int j = 0; j < 8; ++j) {
+                            const int b = c16 * 8 + j;
+                            if (b < Bc) pslot[b * BM + r] = v[2 * j] + v[2 * j + 1];
+                        }
                     }
                 }
             }
             tc_fence_before();
-            mbar_arrive(&sm.acc_empty[a]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.acc_empty);
         }
     }
 
@@ -563,12 +618,17 @@ GemmPlan plan_tc_gemm(int M, int K, int B) {
     // (unit counts stay far below 2^31 / num_sms for every accepted config)
     g.MT = (M + BM - 1) / BM;
     g.KT = (K + kTileK - 1) / kTileK;
-    g.KU = B >= kTcMinBatch ? 2 : 4;
+    g.KU = B >= kTcMinBatch ? KU : 4;
     g.UT = (g.KT + g.KU - 1) / g.KU;
     g.nchunks = (B + NB_CHUNK - 1) / NB_CHUNK;
-    g.U = g.nchunks * g.MT * g.UT;
+    // tensor-core units cover a pair of row tiles (the activation operand is
+    // then read once per two weight tiles) when that still leaves every SM
+    // several units; otherwise, and for the CUDA-core kernel, one row tile
+    g.TP = (B >= kTcMinBatch && g.nchunks * ((g.MT + 1) / 2) * g.UT >= 4 * num_sms()) ? 2 : 1;
+    g.MP = (g.MT + g.TP - 1) / g.TP;
+    g.U = g.nchunks * g.MP * g.UT;
     g.G = std::min(num_sms(), g.U);
-    // segments per tile: a tile of UT units meets at most ceil(UT / min_range) + 1 ranges
+    // segments per tile (pair): UT units meet at most ceil(UT / min_range) + 1 ranges
     const int min_range = g.U / g.G;
     g.max_seg = (g.UT + min_range - 1) / min_range + 1;
     g.tiles = g.nchunks * g.MT;
@@ -609,6 +669,8 @@ cudaError_t launch_gemm_i8_tc(const uint8_t *Wt, const uint8_t *xb, float *part,
     p.err = err;
     p.M = M;
     p.MT = g.MT;
+    p.MP = g.MP;
+    p.TP = g.TP;
     p.KT = g.KT;
     p.UT = g.UT;
     p.B = B;

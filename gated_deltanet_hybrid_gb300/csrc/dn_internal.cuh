@@ -72,11 +72,13 @@ cudaError_t launch_gemv_i8(const uint8_t *Wt, const float *x, float *part, int *
 // Tensor-core (tcgen05) version for batches >= kTcMinBatch: x arrives packed
 // as bf16 hi/lo B-operand tiles (launch_pack_b, or written so by the core
 // kernel).
-// A schedule unit is KU consecutive 64-wide k tiles of one 128-row tile (one
-// bulk copy of KU * 8 KB weights): 4 for the CUDA-core kernel, 2 for the
-// tensor-core kernel.  UT = units per row tile.
+// A schedule unit is KU consecutive 64-wide k tiles of one 128-row tile (the
+// CUDA-core kernel, KU = 4) or of a pair of row tiles that share the
+// activation operand (the tensor-core kernel, KU = 2, when there are enough
+// units).  MP = row-tile groups of TP tiles, UT = units per group; partial
+// sums are kept per row tile (MT tiles, up to max_seg segment slots each).
 struct GemmPlan {
-    int MT, KT, KU, UT, nchunks, U, G, max_seg, tiles;
+    int MT, TP, MP, KT, KU, UT, nchunks, U, G, max_seg, tiles;
 };
 GemmPlan plan_tc_gemm(int M, int K, int B);
 cudaError_t launch_pack_b(const float *x, uint8_t *xb, int B, int K, cudaStream_t st);
