@@ -46,7 +46,11 @@ from gated_deltanet_hybrid_gb300.inputs import (SHAPE_35B, WORKLOADS, DNConfig, 
 
 METRIC = "DeltaNet layer-steps/s and achieved HBM GB/s (% of roofline) at batch 1 and 64"
 UNIT = "layer-steps/s"
-KERNELS = ("in_proj", "dn_core", "out_proj")
+KERNELS = ("in_proj", "dn_state", "out_proj")
+# stage -> (first, last) index of the five events dn_profile_next_step records
+# (events 1 -> 2 bracket a separate preparation kernel, which this library
+# does not launch: the state kernel builds its inputs itself)
+STAGE_EVENTS = {"in_proj": (0, 1), "dn_state": (1, 3), "out_proj": (3, 4)}
 
 
 # --------------------------------------------------------------------- bytes
@@ -62,14 +66,21 @@ def step_bytes(cfg: DNConfig, B: int) -> int:
 
 
 def kernel_bytes(cfg: DNConfig, B: int) -> dict[str, int]:
-    """Algorithmic bytes of each kernel of the step (its unique inputs and
-    outputs, scratch included, since it is that kernel's real traffic)."""
+    """Algorithmic bytes of each stage of the step (its unique inputs and
+    outputs; an intermediate result counts once as the producer's output and
+    once as the consumer's input, since both move it).
+
+    in_proj: W_in, s_in, x in, the projection out.  dn_state: the projection
+    in, the ring's conv_k-1 history slots in and the new slot out, the conv
+    weights, the gates, the state read and written, the gated-norm output
+    out, the norm weight.  out_proj: W_out, s_out, its input in, the layer
+    output out."""
     k1 = cfg.in_rows * cfg.hidden + cfg.in_rows * 4 + B * (cfg.hidden + cfg.in_rows) * 4
-    core_seq = (2 * cfg.n_v_heads * cfg.dk * cfg.dv * 4 + (cfg.conv_k - 1) * cfg.conv_ch * 4
-                + cfg.conv_ch * 4 + cfg.in_rows * 4 + cfg.v_dim * 4 + 2 * cfg.n_v_heads * 4)
-    k2 = B * core_seq + cfg.conv_ch * cfg.conv_k * 4 + cfg.dv * 4
+    ks = (B * (cfg.in_rows * 4 + (cfg.conv_k - 1) * cfg.conv_ch * 4 + cfg.conv_ch * 4
+               + 2 * cfg.n_v_heads * 4 + 2 * cfg.n_v_heads * cfg.dk * cfg.dv * 4 + cfg.v_dim * 4)
+          + cfg.conv_ch * cfg.conv_k * 4 + cfg.dv * 4)
     k3 = cfg.hidden * cfg.v_dim + cfg.hidden * 4 + B * (cfg.v_dim + cfg.hidden) * 4
-    return {"in_proj": k1, "dn_core": k2, "out_proj": k3}
+    return {"in_proj": k1, "dn_state": ks, "out_proj": k3}
 
 
 def load_peaks() -> tuple[float, str]:
@@ -240,7 +251,7 @@ def bench_gpu(cfg, B, init_std, steps, warmup, n_layers, seed, use_graph, dist_c
         except Exception as e:  # capture not possible: time eager launches
             print(f"[bench] graph capture failed ({e}); timing eager launches", file=sys.stderr)
             graph = None
-    launches_per_step = 3
+    launches_per_step = abi.dn_step_kernels(layers[0], B)
 
     # ---- timed region ----
     def run_region():
@@ -269,7 +280,7 @@ def bench_gpu(cfg, B, init_std, steps, warmup, n_layers, seed, use_graph, dist_c
 
     # ---- per-kernel device times (CUDA events between the kernels) ----
     n_prof = min(steps, 2048)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_prof)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_prof)]
     for es in evs:  # torch creates the CUDA event on first record
         for e in es:
             e.record(stream)
@@ -284,8 +295,9 @@ def bench_gpu(cfg, B, init_std, steps, warmup, n_layers, seed, use_graph, dist_c
     torch.cuda.synchronize()
     per_kernel = {k: 0.0 for k in KERNELS}
     for e in evs:
-        for j, k in enumerate(KERNELS):
-            per_kernel[k] += e[j].elapsed_time(e[j + 1])
+        for k in KERNELS:
+            a, z = STAGE_EVENTS[k]
+            per_kernel[k] += e[a].elapsed_time(e[z])
     per_kernel = {k: v / n_prof for k, v in per_kernel.items()}
 
     # ---- end to end through the ABI with host buffers ----

@@ -27,7 +27,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdn.so")
 #: every call the header declares, in declaration order
 ABI_SYMBOLS = ("dn_create", "dn_set_state", "dn_get_state", "dn_step", "dn_destroy",
                "dn_debug_fail_next", "dn_profile_next_step", "dn_proj_i8_noalloc",
-               "dn_device_bytes", "dn_strerror")
+               "dn_device_bytes", "dn_step_kernels", "dn_strerror")
 
 
 class DNError(RuntimeError):
@@ -79,6 +79,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dn_profile_next_step.restype = i32
     lib.dn_proj_i8_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp]
     lib.dn_proj_i8_noalloc.restype = i32
+    lib.dn_step_kernels.argtypes = [vp, i32]
+    lib.dn_step_kernels.restype = i32
     lib.dn_device_bytes.argtypes = []
     lib.dn_device_bytes.restype = ctypes.c_int64
     lib.dn_strerror.argtypes = [i32]
@@ -200,11 +202,13 @@ def dn_debug_fail_next(layer, code: int, check: bool = True) -> int:
 
 
 def dn_profile_next_step(layer, events, check: bool = True) -> int:
-    """events: four torch.cuda.Event(enable_timing=True) (or None to cancel)."""
+    """events: five torch.cuda.Event(enable_timing=True) (or None to cancel)."""
     lib = load_library()
     if events is None:
         return _check("dn_profile_next_step", lib.dn_profile_next_step(layer, None), check)
-    arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    if len(events) != 5:
+        raise ValueError("dn_profile_next_step takes five events")
+    arr = (ctypes.c_void_p * 5)(*[ctypes.c_void_p(e.cuda_event) for e in events])
     return _check("dn_profile_next_step", lib.dn_profile_next_step(layer, arr), check)
 
 
@@ -222,6 +226,11 @@ def dn_proj_i8_noalloc(W, s, x, y, stream=None, check: bool = True) -> int:
     M, K = int(W.shape[0]), int(W.shape[1])
     rc = lib.dn_proj_i8_noalloc(pw, ps, px, py, M, K, int(x.shape[0]), _stream_of(stream, DN_PTR_DEVICE))
     return _check("dn_proj_i8_noalloc", rc, check)
+
+
+def dn_step_kernels(layer, batch: int) -> int:
+    """Kernels one dn_step of `batch` sequences launches (0 if out of range)."""
+    return int(load_library().dn_step_kernels(layer, int(batch)))
 
 
 def dn_device_bytes() -> int:

@@ -21,7 +21,7 @@ struct dn_layer {
     int device;
     int failed;
     int fail_next;
-    cudaEvent_t prof[4];  // one-shot per-kernel events for the next step
+    cudaEvent_t prof[5];  // one-shot per-stage events for the next step
     int prof_armed;
     size_t bytes;
     std::vector<void *> allocs;
@@ -202,7 +202,6 @@ DN_API int dn_create(const dn_config *cfg, const dn_weights *w, void *stream, dn
     ALLOC(L.nseg_out, tiles_out * 4);
     ALLOC(L.xb_in, xb_bytes_in);
     ALLOC(L.xb_out, xb_bytes_out);
-    ALLOC(L.prep_rec, MB * d.n_v * dn::prep_record_len(d) * 4);
     ALLOC(L.err, 4);
 #undef ALLOC
     if (rc != DN_OK) {
@@ -264,12 +263,19 @@ DN_API int dn_profile_next_step(dn_layer *l, void *const *events) {
         l->prof_armed = 0;
         return DN_OK;
     }
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 5; ++i) {
         if (events[i] == nullptr) return DN_EINVAL;
         l->prof[i] = (cudaEvent_t)events[i];
     }
     l->prof_armed = 1;
     return DN_OK;
+}
+
+DN_API int dn_step_kernels(const dn_layer *l, int batch) {
+    if (l == nullptr || batch < 1 || batch > l->d.max_batch) return 0;
+    const bool tc = batch >= dn::kTcMinBatch;
+    const int in_proj = tc ? 2 : 1;                                // (pack) + projection
+    return in_proj + 1 + 1 + 1;  // state kernel, out projection, reduction
 }
 
 DN_API int dn_set_state(dn_layer *l, int seq0, int n, const float *S, const float *ring,
@@ -371,11 +377,12 @@ DN_API int dn_step(dn_layer *l, int batch, const float *x, const float *g, const
                                      batch, st));
     }
     if (prof) DN_TRY(l, cudaEventRecord(l->prof[1], st));
+    if (prof) DN_TRY(l, cudaEventRecord(l->prof[2], st));  // no separate preparation kernel
     if (dn::dn_core_stream_ok(d, batch))
         DN_TRY(l, dn::launch_dn_core_stream(d, L, batch, gd, bd, tc, st));
     else
         DN_TRY(l, dn::launch_dn_core(d, L, batch, gd, bd, tc, st));
-    if (prof) DN_TRY(l, cudaEventRecord(l->prof[2], st));
+    if (prof) DN_TRY(l, cudaEventRecord(l->prof[3], st));
     if (tc)
         DN_TRY(l, dn::launch_gemm_i8_tc(L.w_out, L.xb_out, L.part_out, L.nseg_out, L.err, d.hidden,
                                         d.v_dim, batch, st));
@@ -384,7 +391,7 @@ DN_API int dn_step(dn_layer *l, int batch, const float *x, const float *g, const
                                      d.v_dim, batch, st));
     DN_TRY(l, dn::launch_splitk_reduce(L.part_out, L.nseg_out, L.s_out, od, d.hidden, d.v_dim, batch,
                                        L.rpos, d.conv_k, st));
-    if (prof) DN_TRY(l, cudaEventRecord(l->prof[3], st));
+    if (prof) DN_TRY(l, cudaEventRecord(l->prof[4], st));
     if (ptr_kind == DN_PTR_HOST) {
         DN_TRY(l, cudaMemcpyAsync(out, L.out_stage, (size_t)batch * d.hidden * 4, cudaMemcpyDeviceToHost, st));
         DN_TRY(l, cudaStreamSynchronize(st));

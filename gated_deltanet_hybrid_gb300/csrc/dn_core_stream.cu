@@ -1,23 +1,33 @@
-// Persistent, bulk-copy-pipelined state kernel for large batches (one
-// 128 x 128 state tile per (sequence, value head)).
+// Persistent, bulk-copy-pipelined kernel for large batches of 128 x 128
+// heads: the whole part of the page's step ("qwen36: run the DeltaNet layer
+// end to end on the card (Q36_DN_GPU=1)", section "What the PR does")
+// between the in_proj and the out_proj - causal conv + SiLU with the ring
+// advancing, the L2 norms of q and k, the decay, the delta against the
+// decayed state, the write-back, out = q^T S over the updated state, and
+// the gated RMSNorm with silu(z) - for one (sequence, value head) item at a
+// time.  Organised for HBM streaming:
 //
-// It runs the recurrence of the page's step ("qwen36: run the DeltaNet layer
-// end to end on the card (Q36_DN_GPU=1)", section "What the PR does": the
-// decay, the delta against the decayed state, the write-back, out = q^T S
-// over the updated state) and the gated RMSNorm with silu(z), on the
-// per-(sequence, head) records that dn_prep_kernel wrote (normalised q and k,
-// v, silu(z), exp(g), beta).  Organised for HBM streaming:
-//
-//  * one CTA per SM walks a contiguous range of (sequence, head) items;
-//  * each item's 64 KB state tile and its 2 KB record arrive by two
-//    cp.async.bulk copies on one mbarrier into a 3-deep shared-memory ring;
-//    the tile is updated in place by 16 warps (each thread keeps its 32
-//    values in registers between the decay/delta pass and the write-back /
-//    readout pass) and leaves by one bulk store; the loads of item i+2 are
-//    issued as soon as the store of item i-1 has been read out of shared
-//    memory.
-//  * the first two state tiles are fetched before the kernel waits for
-//    dn_prep_kernel (programmatic dependent launch), the records after.
+//  * one CTA per SM walks a contiguous range of items (b-major);
+//  * each item's 64 KB state tile arrives by one cp.async.bulk copy on an
+//    mbarrier into a 3-deep shared-memory ring, is updated in place by 16
+//    warps (each thread keeps its 32 values in registers between the
+//    decay/delta pass and the write-back/readout pass) and leaves by one bulk
+//    store; the load of item j+2 is issued as soon as the store of item j-1
+//    has been read out of shared memory;
+//  * the item's inputs - its q and k rows (of its q/k head), its v and z rows,
+//    one per thread (512 = 4 x 128 rows) - are built on the fly: the in_proj
+//    output of a row is the sum of its segment partials in slot order
+//    (dn_sched.cuh) times the row scale; q, k, v go through the conv over the
+//    ring (K-1 history slots read, the newest written) and SiLU, z through
+//    SiLU; q and k are L2-normalised with fp32 warp sums combined in a fixed
+//    order.  The CTA's segment counts and ring positions are read once into
+//    shared memory, so an item's loads (partials, ring history, row scale and
+//    conv weights) depend on nothing else and are issued one item ahead (as
+//    volatile loads, so that the compiler keeps them there): their latency
+//    hides behind the previous item's tile;
+//  * the first two state tiles are fetched before the kernel waits for the
+//    in_proj kernel (programmatic dependent launch): the state is not written
+//    by it, the partials are.
 //
 // Every wait is bounded (about one second); on timeout the kernel records an
 // error in `err`, waits (bounded) for its own bulk copies and returns.
@@ -26,39 +36,52 @@
 #include <algorithm>
 
 #include "dn_internal.cuh"
+#include "dn_sched.cuh"
 
 namespace dn {
 namespace {
 
 constexpr int D = 128;               // dk = dv
-constexpr int NT = 512;              // threads
+constexpr int NT = 512;              // threads: one input row of the item each
 constexpr int STAGES = 3;
 constexpr uint32_t kTileBytes = D * D * 4;
-constexpr int REC = 4 * D + 4;       // record floats: q^ | k^ | v | silu(z) | exp(g), beta, 0, 0
-constexpr uint32_t kRecBytes = REC * 4;
 constexpr int LPR = D / 4;           // 32 lanes across a row (float4 each)
 constexpr int RPP = NT / LPR;        // 16 rows per pass
 constexpr int NP = D / RPP;          // 8 float4 per thread
+constexpr int PV = 6;                // partial slots fetched ahead (more are read on the spot)
+constexpr int kMaxMT = 256;          // in_proj row tiles (in_rows <= 32768)
+constexpr int kMaxSeqCta = 64;       // sequences one CTA's item range may touch
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 struct StreamParams {
-    const float *rec;      // [B][n_v][REC]
+    const float *part_in;  // in_proj segment partials
+    const int *nseg_in;
+    const float *s_in;
+    float *ring;           // [max_batch][conv_k][conv_ch]
+    const int32_t *rpos;   // [max_batch][2]
+    const float *wconv_t;  // [conv_k][conv_ch]
+    const float *g, *beta; // [B][n_v]
     const float *w_norm;   // [dv]
     float *S;              // [max_batch][n_v][128][128]
     float *nrm;            // fp32 output rows, or
     uint8_t *xb_out;       // packed bf16 hi/lo B-operand tiles
     int *err;
-    int n_v, v_dim, kt_out, items;
-    float norm_eps;
+    int MT, max_seg;       // in_proj row tiles and segment slots per tile
+    int n_v, group, conv_ch, qk_dim, v_dim, kt_out, items;
+    float l2_eps, q_scale, norm_eps;
 };
 
 struct __align__(128) StreamSmem {
     float tile[STAGES][D * D];  // 3 x 64 KB
-    float rec[STAGES][REC];     // 3 x 2064 B
+    float rec[2][4 * D];        // the item's q^ | k^ | v | silu(z), double-buffered
+    float gate[2][2];           // exp(g), beta
     float red[RPP][D];          // 8 KB
     float delta[D];
     float ssq_o[4];
+    float ssq_qk[2][8];         // warp sums of squares (warps 0-3 q, 4-7 k), double-buffered
     float wn[D];                // gated-RMSNorm weight
+    int nseg[2][kMaxMT];        // in_proj segment counts of the CTA's (up to 2) batch chunks
+    int dpos[kMaxSeqCta];       // ring positions of the CTA's sequences
     uint64_t full[STAGES];
 };
 
@@ -89,22 +112,16 @@ __device__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
         if ((it & 63u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
     }
 }
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-// the item's state tile and record, on the stage's barrier
+// the item's state tile, on the stage's barrier
 __device__ __forceinline__ void load_tile(StreamSmem &sm, int st, const StreamParams &p, int item) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(&sm.full[st])),
-                 "r"(kTileBytes + kRecBytes)
+                 "r"(kTileBytes)
                  : "memory");
-    bulk_g2s(sm.tile[st], p.S + (size_t)item * (D * D), kTileBytes, &sm.full[st]);
-}
-__device__ __forceinline__ void load_rec(StreamSmem &sm, int st, const StreamParams &p, int item) {
-    bulk_g2s(sm.rec[st], p.rec + (size_t)item * REC, kRecBytes, &sm.full[st]);
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(sm.tile[st])),
+        "l"(p.S + (size_t)item * (D * D)), "r"(kTileBytes), "r"(smem_u32(&sm.full[st]))
+        : "memory");
 }
 __device__ __forceinline__ void store_tile(float *dst, const float *src) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
@@ -117,7 +134,109 @@ __device__ __forceinline__ float warp_sum(float v) {
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
 }
+// silu(a) = a / (1 + e^-a) with the hardware exponential and divide
+// (__expf, __fdividef: a few ulp, far inside the step's tolerance; for
+// a -> -inf the divisor overflows and the quotient is 0, silu's limit)
+__device__ __forceinline__ float silu_f(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
 
+// This thread's input row of item (b, h): region 0 q, 1 k, 2 v, 3 z (thread
+// t serves row t % 128 of region t / 128).
+struct RowRef {
+    int b, c;          // sequence, in_proj row
+    bool conv, ring_w; // goes through the conv; this item writes its ring slot
+};
+__device__ __forceinline__ RowRef row_of(const StreamParams &p, int b, int h, int t) {
+    RowRef r;
+    r.b = b;
+    const int hq = h / p.group;
+    const int region = t >> 7, o = t & (D - 1);
+    r.c = region == 0 ? hq * D + o
+        : region == 1 ? p.qk_dim + hq * D + o
+        : region == 2 ? 2 * p.qk_dim + h * D + o
+                      : p.conv_ch + h * D + o;
+    r.conv = region < 3;
+    // q and k rows are shared by the value heads of a q/k head: the first writes
+    r.ring_w = region == 2 || (region < 2 && h % p.group == 0);
+    return r;
+}
+
+__device__ __forceinline__ float ld_cg(const float *ptr) {
+    float v;
+    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(ptr));
+    return v;
+}
+__device__ __forceinline__ float ld_nc(const float *ptr) {
+    float v;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(ptr));
+    return v;
+}
+
+// One item ahead: the row's first PV segment partials, its ring history,
+// scale and conv weights, and the item's gates.  Every load is
+// unconditional, from an address that is valid whatever the row (slots past
+// the segment count and the conv inputs of z rows are masked where they are
+// used), because a select on a value still in flight would wait for it here.
+template <int KC>
+struct Ahead {
+    float pv[PV], hist[KC - 1], sc, wc[KC], gv, bv;
+};
+
+template <int KC>
+__device__ __forceinline__ void load_ahead(const StreamParams &p, const StreamSmem &sm, int b0, int b, int h,
+                                           int t, Ahead<KC> &a) {
+    const RowRef r = row_of(p, b, h, t);
+    const int item = b * p.n_v + h;
+    const int ptile = (r.b >> 6) * p.MT + (r.c >> 7);
+    const float *pp = p.part_in + (size_t)ptile * p.max_seg * (64 * D) + (r.b & 63) * D + (r.c & (D - 1));
+#pragma unroll
+    for (int k = 0; k < PV; ++k)  // slots past max_seg fall back to slot 0
+        a.pv[k] = ld_cg(pp + (size_t)(k < p.max_seg ? k : 0) * (64 * D));
+    const int cr = r.conv ? r.c : 0;  // z rows read channel 0's ring and weights
+    const float *rb = p.ring + (size_t)r.b * KC * p.conv_ch + cr;
+    int slot = sm.dpos[r.b - b0];
+#pragma unroll
+    for (int m = 0; m < KC - 1; ++m) {  // oldest input first
+        a.hist[m] = ld_cg(rb + (size_t)slot * p.conv_ch);
+        if (++slot == KC) slot = 0;
+    }
+    a.sc = ld_nc(p.s_in + r.c);
+#pragma unroll
+    for (int m = 0; m < KC; ++m) a.wc[m] = ld_nc(p.wconv_t + (size_t)m * p.conv_ch + cr);
+    a.gv = ld_cg(p.g + item);  // [B][n_v] = item order
+    a.bv = ld_cg(p.beta + item);
+}
+
+// The row's in_proj output, conv + SiLU (z: SiLU only); the ring slot of the
+// new input is written by the item that owns the row.
+template <int KC>
+__device__ __forceinline__ float build_input(const StreamParams &p, const StreamSmem &sm, int b0, int chunk0,
+                                             int b, int h, int t, const Ahead<KC> &a) {
+    const RowRef r = row_of(p, b, h, t);
+    const int ns = sm.nseg[(r.b >> 6) - chunk0][r.c >> 7];
+    float acc = 0.f;
+#pragma unroll
+    for (int k = 0; k < PV; ++k)
+        if (k < ns) acc += a.pv[k];  // slot order
+    if (ns > PV) {
+        const int ptile = (r.b >> 6) * p.MT + (r.c >> 7);
+        const float *pp = p.part_in + (size_t)ptile * p.max_seg * (64 * D) + (r.b & 63) * D + (r.c & (D - 1));
+        for (int k = PV; k < ns; ++k) acc += __ldcg(pp + (size_t)k * (64 * D));
+    }
+    const float xv = a.sc * acc;
+    if (!r.conv) return silu_f(xv);
+    float cv = 0.f;
+#pragma unroll
+    for (int m = 0; m < KC - 1; ++m) cv = fmaf(a.wc[m], a.hist[m], cv);
+    cv = fmaf(a.wc[KC - 1], xv, cv);
+    if (r.ring_w) {
+        int ws = sm.dpos[r.b - b0] + KC - 1;  // the oldest slot, not read by this step
+        if (ws >= KC) ws -= KC;
+        p.ring[((size_t)r.b * KC + ws) * p.conv_ch + r.c] = xv;
+    }
+    return silu_f(cv);
+}
+
+template <int KC>
 __global__ void __launch_bounds__(NT, 1) dn_core_stream_kernel(const StreamParams p) {
     extern __shared__ uint8_t smem_raw[];
     StreamSmem &sm = *reinterpret_cast<StreamSmem *>(
@@ -134,31 +253,66 @@ __global__ void __launch_bounds__(NT, 1) dn_core_stream_kernel(const StreamParam
     }
     if (t < D) sm.wn[t] = p.w_norm[t];
     __syncthreads();
-    int issued = 0;  // (thread 0) item loads issued so far
-    if (t == 0) {
-        // the state tiles do not depend on the previous kernel (dn_prep_kernel):
-        // fetch them before waiting for it, the records after
+    int issued = 0;  // (thread 0) tile loads issued so far
+    if (t == 0)
         for (int j = 0; j < 2 && j < n_items; ++j, ++issued) load_tile(sm, j, p, i0 + j);
-        pdl_wait();
-        pdl_trigger();
-        for (int j = 0; j < issued; ++j) load_rec(sm, j, p, i0 + j);
-    } else {
-        pdl_wait();
+    // the state is not written by the in_proj kernel, its partials are
+    pdl_wait();
+    if (t == 0) pdl_trigger();
+    // the segment counts of the CTA's batch chunks and its sequences' ring positions
+    const int b0 = i0 / p.n_v, chunk0 = b0 >> 6;
+    const int nseq = n_items > 0 ? (i1 - 1) / p.n_v - b0 + 1 : 0;
+    const int nchunk = n_items > 0 ? (((i1 - 1) / p.n_v) >> 6) - chunk0 + 1 : 0;
+    for (int i = t; i < nchunk * p.MT; i += NT) {
+        const int ci = i / p.MT, mt = i - ci * p.MT;
+        sm.nseg[ci][mt] = p.nseg_in[(chunk0 + ci) * p.MT + mt];
     }
+    for (int i = t; i < nseq; i += NT) sm.dpos[i] = p.rpos[2 * (b0 + i)];
+    __syncthreads();
+
+    Ahead<KC> ac;  // item j
+    if (n_items > 0) load_ahead(p, sm, b0, i0 / p.n_v, i0 % p.n_v, t, ac);
 
     const int c4 = t % LPR, r0 = t / LPR;
     bool failed = false;
     for (int j = 0; j < n_items; ++j) {
         const int item = i0 + j;
-        const int b = item / p.n_v, h = item % p.n_v;
-        const int st = j % STAGES;
+        const int b = item / p.n_v, h = item - b * p.n_v;
+        const int st = j % STAGES, rbuf = j & 1;
+
+        // ---- the item's q^, k^, v, silu(z), gates; loads for the next items ----
+        const float u = build_input(p, sm, b0, chunk0, b, h, t, ac);
+        const float gv = ac.gv, bv = ac.bv;
+        if (j + 1 < n_items) {
+            const bool wrap = h + 1 == p.n_v;
+            load_ahead(p, sm, b0, wrap ? b + 1 : b, wrap ? 0 : h + 1, t, ac);
+        }
+        if (warp < 8) {  // q (warps 0-3) and k (warps 4-7): sums of squares
+            const float sq = warp_sum(u * u);
+            if (lane == 0) sm.ssq_qk[rbuf][warp] = sq;
+        }
+        __syncthreads();
+        float val = u;
+        if (t < 2 * D) {
+            const float *ssq = sm.ssq_qk[rbuf] + (t >> 7) * 4;
+            val = u * (1.0f / sqrtf(((ssq[0] + ssq[1]) + (ssq[2] + ssq[3])) + p.l2_eps)) *
+                  (t < D ? p.q_scale : 1.0f);
+        }
+        sm.rec[rbuf][t] = val;
+        if (t == 0) {
+            sm.gate[rbuf][0] = expf(gv);
+            sm.gate[rbuf][1] = bv;
+        }
+
+        // ---- the state tile --------------------------------------------------
         const bool landed = mbar_wait(&sm.full[st], (j / STAGES) & 1);
         if (!__syncthreads_and(landed)) {
             failed = true;
             break;
         }
-        const float *rq = sm.rec[st], *rk = rq + D, *rv = rq + 2 * D, *rz = rq + 3 * D;
-        const float eg = rq[4 * D], bt = rq[4 * D + 1];
+        const float *rq = sm.rec[rbuf], *rk = rq + D, *rv = rq + 2 * D, *rz = rq + 3 * D;
+        const float eg = sm.gate[rbuf][0], bt = sm.gate[rbuf][1];
+
         float *tile = sm.tile[st];
 
         // decay, then what the decayed state predicts for k
@@ -214,7 +368,6 @@ __global__ void __launch_bounds__(NT, 1) dn_core_stream_kernel(const StreamParam
             asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
             if (j + 2 < n_items) {
                 load_tile(sm, (j + 2) % STAGES, p, item + 2);
-                load_rec(sm, (j + 2) % STAGES, p, item + 2);
                 issued = j + 3;
             }
         }
@@ -244,7 +397,8 @@ __global__ void __launch_bounds__(NT, 1) dn_core_stream_kernel(const StreamParam
                 *reinterpret_cast<__nv_bfloat16 *>(ot + op_chunk_offset(rl, kc) + e * 2) = lo;
             }
         }
-        // (red, delta and ssq_o are next written after the next item's first barrier)
+        // (red, delta, ssq_* and the other record buffer are next written after
+        // a barrier of the next item)
     }
     if (t == 0) {
         if (failed) atomicOr(p.err, 1);
@@ -256,49 +410,71 @@ __global__ void __launch_bounds__(NT, 1) dn_core_stream_kernel(const StreamParam
     __syncthreads();
 }
 
-}  // namespace
-
-bool dn_core_stream_ok(const Dims &d, int B) {
-    return d.dk == D && d.dv == D && (long)B * d.n_v >= 2L * num_sms();
-}
-
-size_t dn_core_stream_smem() { return sizeof(StreamSmem) + 128; }
-
-cudaError_t launch_dn_core_stream(const Dims &d, const LayerDev &L, int B, const float *g,
-                                  const float *beta, bool tc, cudaStream_t st) {
+template <int KC>
+cudaError_t launch_kc(const StreamParams &p, cudaStream_t st) {
     static int attr_dev = -1;
     int dev = 0;
     cudaGetDevice(&dev);
+    const size_t smem = sizeof(StreamSmem) + 128;
     if (attr_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(dn_core_stream_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)dn_core_stream_smem());
+        cudaError_t e = cudaFuncSetAttribute(dn_core_stream_kernel<KC>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         attr_dev = dev;
     }
-    // conv, ring, norms and gates of every (sequence, head) first
-    cudaError_t e = launch_dn_prep(d, L, B, g, beta, st);
-    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)std::min(num_sms(), p.items));
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    PdlAttr pdl;
+    pdl.apply(cfg);
+    return cudaLaunchKernelEx(&cfg, dn_core_stream_kernel<KC>, p);
+}
+
+}  // namespace
+
+bool dn_core_stream_ok(const Dims &d, int B) {
+    const long items = (long)B * d.n_v, per_cta = (items + num_sms() - 1) / num_sms();
+    return d.dk == D && d.dv == D && d.conv_k <= 4 && items >= 2L * num_sms() &&
+           (d.in_rows + kTileM - 1) / kTileM <= kMaxMT && per_cta / d.n_v + 2 <= kMaxSeqCta;
+}
+
+cudaError_t launch_dn_core_stream(const Dims &d, const LayerDev &L, int B, const float *g,
+                                  const float *beta, bool tc, cudaStream_t st) {
     StreamParams p;
-    p.rec = L.prep_rec;
+    p.part_in = L.part_in;
+    p.nseg_in = L.nseg_in;
+    p.s_in = L.s_in;
+    p.ring = L.ring;
+    p.rpos = L.rpos;
+    p.wconv_t = L.wconv_t;
+    p.g = g;
+    p.beta = beta;
     p.w_norm = L.w_norm;
     p.S = L.S;
     p.nrm = L.nrm;
     p.xb_out = tc ? L.xb_out : nullptr;
     p.err = L.err;
+    const GemmPlan gp = plan_tc_gemm(d.in_rows, d.hidden, B);
+    p.MT = gp.MT;
+    p.max_seg = gp.max_seg;
     p.n_v = d.n_v;
+    p.group = d.n_v / d.n_qk;
+    p.conv_ch = d.conv_ch;
+    p.qk_dim = d.qk_dim;
     p.v_dim = d.v_dim;
     p.kt_out = (d.v_dim + kTileK - 1) / kTileK;
     p.items = B * d.n_v;
+    p.l2_eps = d.l2_eps;
+    p.q_scale = d.q_scale;
     p.norm_eps = d.norm_eps;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)std::min(num_sms(), p.items));
-    cfg.blockDim = dim3(NT);
-    cfg.dynamicSmemBytes = dn_core_stream_smem();
-    cfg.stream = st;
-    PdlAttr pdl;
-    pdl.apply(cfg);
-    return cudaLaunchKernelEx(&cfg, dn_core_stream_kernel, p);
+    switch (d.conv_k) {
+        case 2: return launch_kc<2>(p, st);
+        case 3: return launch_kc<3>(p, st);
+        case 4: return launch_kc<4>(p, st);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace dn

@@ -29,8 +29,8 @@
 // tile count.  A range covers the tail of one m tile and the head of the next
 // (a "segment" each); two TMEM accumulators alternate between segments.
 // Every segment's partial sums go to a slot of a partial buffer (schedule in
-// dn_sched.cuh); the consumer sums a tile's slots in slot order (the prep or
-// core kernel for the in_proj, splitk_reduce_kernel for the out_proj), so
+// dn_sched.cuh); the consumer sums a tile's slots in slot order (the state
+// kernel for the in_proj, splitk_reduce_kernel for the out_proj), so
 // results do not depend on scheduling and no CTA waits on another.
 //
 // A unit is 128 rows x 128 k (16 KB of int8 weights, one bulk copy: copies

@@ -47,7 +47,6 @@ struct LayerDev {
     int *nseg_in, *nseg_out;  // segments per tile of the last projection launch
     uint8_t *xb_in;        // packed B-operand tiles of x   [chunks][KT_in][16 KB]
     uint8_t *xb_out;       // packed B-operand tiles of the gated-norm output [chunks][KT_out][16 KB]
-    float *prep_rec;       // [max_batch][n_v][2*dk + 2*dv + 4] records for the persistent state kernel
     int *err;              // device-side error word (bounded waits that gave up)
 };
 
@@ -105,13 +104,8 @@ __host__ __device__ __forceinline__ uint32_t op_chunk_offset(int row, int kc) {
 cudaError_t launch_dn_core(const Dims &d, const LayerDev &L, int B, const float *g,
                            const float *beta, bool tc, cudaStream_t st);
 
-// Per-(sequence, head) conv / norm / gate records for the persistent kernel.
-int prep_record_len(const Dims &d);
-cudaError_t launch_dn_prep(const Dims &d, const LayerDev &L, int B, const float *g,
-                           const float *beta, cudaStream_t st);
-
-// Persistent bulk-copy-pipelined variant for large batches of 128 x 128 heads
-// (launches dn_prep first).
+// Persistent bulk-copy-pipelined variant of the same step for large batches
+// of 128 x 128 heads (conv_k <= 4).
 bool dn_core_stream_ok(const Dims &d, int B);
 cudaError_t launch_dn_core_stream(const Dims &d, const LayerDev &L, int B, const float *g,
                                   const float *beta, bool tc, cudaStream_t st);

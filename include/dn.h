@@ -165,14 +165,24 @@ int dn_debug_fail_next(dn_layer *layer, int code);
 
 /*
  * dn_profile_next_step — instrumentation for benchmarks: the next dn_step on
- * this layer records events[0] on its stream before its first kernel,
- * events[1] after the in_proj GEMV, events[2] after the fused conv /
- * recurrence / gated-norm kernel and events[3] after the out_proj GEMV, so
- * that cudaEventElapsedTime gives each kernel's device time.  `events` points
- * to four cudaEvent_t created by the caller (timing enabled); it is used by
- * that one dn_step call only (one-shot).  NULL cancels.  Errors: DN_EINVAL.
+ * this layer records, on its stream, events[0] before its first kernel,
+ * events[1] after the in_proj (activation packing + projection),
+ * events[2] after the per-sequence preparation kernel (conv, norms, gates;
+ * recorded right after events[1] when the step fuses it into the state
+ * kernel), events[3] after the state kernel (recurrence, readout, gated
+ * norm) and events[4] after the out_proj (projection + reduction), so that
+ * cudaEventElapsedTime gives each stage's device time.  `events` points to
+ * five cudaEvent_t created by the caller (timing enabled); it is used by that
+ * one dn_step call only (one-shot).  NULL cancels.  Errors: DN_EINVAL.
  */
 int dn_profile_next_step(dn_layer *layer, void *const *events);
+
+/*
+ * dn_step_kernels — the number of kernels one dn_step of `batch` sequences
+ * launches on this layer (for launch accounting in benchmarks); 0 when
+ * `batch` is out of range.  Not part of the page's layer: instrumentation.
+ */
+int dn_step_kernels(const dn_layer *layer, int batch);
 
 /*
  * dn_proj_i8_noalloc — the int8 row-scaled projection used inside dn_step,

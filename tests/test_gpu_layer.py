@@ -221,3 +221,53 @@ def test_checkpoint_resume_is_bitwise():
     finally:
         full.destroy()
         first.destroy()
+
+
+def test_two_runs_are_bitwise_identical_on_the_tensor_core_path():
+    """Batch 16 of the 35B shape takes the tensor-core projections and the
+    persistent state kernel; the stream-K partials are summed in slot order,
+    so two runs agree bit for bit."""
+    wl = custom_workload("det16", SHAPE_35B, batch=16, steps=4, seed=19, init_std=0.02)
+    outs, states = [], []
+    for _ in range(2):
+        stream = WorkloadStream(wl)
+        layer = GpuLayer.create(wl.cfg, stream.weights[0], 16, stream.states[0])
+        try:
+            assert abi.dn_step_kernels(layer.handle, 16) == 5  # pack, GEMM, state, GEMM, reduce
+            outs.append(_run(layer, stream, 4, 16))
+            states.append(layer.get_state())
+        finally:
+            layer.destroy()
+    for a, b in zip(outs[0], outs[1]):
+        assert np.array_equal(a, b)
+    assert np.array_equal(states[0].S, states[1].S)
+
+
+def test_profiled_step_records_five_stage_events_and_changes_nothing():
+    torch = _torch()
+    wl = custom_workload("prof", SHAPE_35B, batch=16, steps=2, seed=23, init_std=0.02)
+    s1, s2 = WorkloadStream(wl), WorkloadStream(wl)
+    a = GpuLayer.create(wl.cfg, s1.weights[0], 16, s1.states[0])
+    b = GpuLayer.create(wl.cfg, s2.weights[0], 16, s2.states[0])
+    try:
+        assert abi.dn_step_kernels(a.handle, 1) == 4
+        assert abi.dn_step_kernels(a.handle, 17) == 0
+        with pytest.raises(ValueError):
+            abi.dn_profile_next_step(a.handle, [torch.cuda.Event(enable_timing=True)] * 4)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        for e in evs:  # torch creates the CUDA event on first record
+            e.record()
+        abi.dn_profile_next_step(a.handle, evs)
+        x, gates = s1.next_step()
+        s2.next_step()
+        xd, gd, bd, od = _dev_inputs(x, *gates[0])
+        abi.dn_step(a.handle, 16, xd, gd, bd, od)
+        xd2, gd2, bd2, od2 = _dev_inputs(x, *gates[0])
+        abi.dn_step(b.handle, 16, xd2, gd2, bd2, od2)
+        torch.cuda.synchronize()
+        times = [evs[i].elapsed_time(evs[i + 1]) for i in range(4)]
+        assert all(t >= 0.0 for t in times) and sum(times) > 0.0
+        assert np.array_equal(od.cpu().numpy(), od2.cpu().numpy())
+    finally:
+        a.destroy()
+        b.destroy()
