@@ -25,7 +25,7 @@ DN_PTR_DEVICE = 1
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdn.so")
 
 #: every call the header declares, in declaration order
-ABI_SYMBOLS = ("dn_create", "dn_set_state", "dn_get_state", "dn_step", "dn_destroy",
+ABI_SYMBOLS = ("dn_create", "dn_set_state", "dn_get_state", "dn_step", "dn_stack_step", "dn_destroy",
                "dn_debug_fail_next", "dn_profile_next_step", "dn_proj_i8_noalloc",
                "dn_device_bytes", "dn_step_kernels", "dn_strerror")
 
@@ -71,6 +71,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dn_get_state.restype = i32
     lib.dn_step.argtypes = [vp, i32, f32p, f32p, f32p, f32p, i32, vp]
     lib.dn_step.restype = i32
+    lib.dn_stack_step.argtypes = [ctypes.POINTER(vp), i32, i32, f32p, f32p, f32p, ctypes.c_float, vp]
+    lib.dn_stack_step.restype = i32
     lib.dn_destroy.argtypes = [vp]
     lib.dn_destroy.restype = None
     lib.dn_debug_fail_next.argtypes = [vp, i32]
@@ -191,6 +193,20 @@ def dn_step(layer, batch: int, x, g, beta, out, stream=None, check: bool = True)
     kind = _same_kind(kx, kg, kb, ko)
     rc = lib.dn_step(layer, int(batch), px, pg, pb, po, kind, _stream_of(stream, kind))
     return _check("dn_step", rc, check)
+
+
+def dn_stack_step(layers, batch: int, h, g, beta, eps: float = 1e-6, stream=None, check: bool = True) -> int:
+    """One token through a stack of layers (device tensors only): h [B][hidden]
+    is read and overwritten, g/beta [n_layers][B][n_v_heads]."""
+    lib = load_library()
+    ph, kh = _ptr(h, "float32")
+    pg, kg = _ptr(g, "float32")
+    pb, kb = _ptr(beta, "float32")
+    if _same_kind(kh, kg, kb) != DN_PTR_DEVICE:
+        raise TypeError("dn_stack_step takes device tensors")
+    arr = (ctypes.c_void_p * len(layers))(*[ctypes.c_void_p(getattr(l, "value", l)) for l in layers])
+    rc = lib.dn_stack_step(arr, len(layers), int(batch), ph, pg, pb, float(eps), _stream_of(stream, DN_PTR_DEVICE))
+    return _check("dn_stack_step", rc, check)
 
 
 def dn_destroy(layer) -> None:

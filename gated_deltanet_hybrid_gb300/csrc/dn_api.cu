@@ -177,12 +177,12 @@ DN_API int dn_create(const dn_config *cfg, const dn_weights *w, void *stream, dn
     ALLOC(L.out_stage, MB * d.hidden * 4);
     ALLOC(L.ring_stage, MB * (d.conv_k - 1) * d.conv_ch * 4);
     ALLOC(L.rp_stage, MB * 4);
-    // projections: the largest segment-partial buffer over all batch sizes
-    // the layer accepts; packed activations for the tensor-core path
+    // projections: the largest segment-partial buffer over every batch size
+    // the layer accepts (the schedule, hence the segment count, depends on
+    // the batch); packed activations for the tensor-core path
     const size_t chunks = (MB + 63) / 64;
     size_t part_in = 0, part_out = 0, tiles_in = 0, tiles_out = 0, xb_bytes_in = 0, xb_bytes_out = 0;
-    for (size_t ch = 1; ch <= chunks; ++ch) {
-        const int b = (int)std::min<size_t>(ch * 64, MB);
+    for (int b = 1; b <= (int)MB; ++b) {
         const dn::GemmPlan gi = dn::plan_tc_gemm(d.in_rows, d.hidden, b);
         const dn::GemmPlan go = dn::plan_tc_gemm(d.hidden, d.v_dim, b);
         part_in = std::max(part_in, (size_t)gi.tiles * gi.max_seg * 64 * 128);
@@ -276,6 +276,39 @@ DN_API int dn_step_kernels(const dn_layer *l, int batch) {
     const bool tc = batch >= dn::kTcMinBatch;
     const int in_proj = tc ? 2 : 1;                                // (pack) + projection
     return in_proj + 1 + 1 + 1;  // state kernel, out projection, reduction
+}
+
+DN_API int dn_stack_step(dn_layer *const *layers, int n_layers, int batch, float *h, const float *g,
+                         const float *beta, float eps, void *stream) {
+    if (layers == nullptr || n_layers < 1 || h == nullptr || g == nullptr || beta == nullptr) return DN_EINVAL;
+    if (!(eps >= 0.f)) return DN_EINVAL;
+    dn_layer *first = layers[0];
+    if (first == nullptr) return DN_EINVAL;
+    const dn::Dims &d0 = first->d;
+    for (int l = 0; l < n_layers; ++l) {
+        const dn_layer *L = layers[l];
+        if (L == nullptr || L->device != first->device) return DN_EINVAL;
+        if (L->d.hidden != d0.hidden || L->d.n_v != d0.n_v) return DN_EINVAL;
+        if (batch < 1 || batch > L->d.max_batch) return DN_EINVAL;
+        if (L->failed) return DN_EFAILED;
+    }
+    int cur = 0;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != first->device) return DN_EINVAL;
+    cudaStream_t st = stream != nullptr ? (cudaStream_t)stream : first->stream;
+    // the first layer's staging buffers hold the normalised input and the
+    // layer output (dn_step with device pointers does not touch them)
+    float *xn = first->L.x_stage, *y = first->L.out_stage;
+    const size_t gstride = (size_t)batch * d0.n_v;
+    if (dn::launch_residual_prenorm(h, nullptr, xn, batch, d0.hidden, eps, st) != cudaSuccess)
+        return cuda_fail(first);
+    for (int l = 0; l < n_layers; ++l) {
+        const int rc = dn_step(layers[l], batch, xn, g + l * gstride, beta + l * gstride, y, DN_PTR_DEVICE, st);
+        if (rc != DN_OK) return rc;
+        // h += y and the next layer's input (after the last layer: only the add matters)
+        if (dn::launch_residual_prenorm(h, y, xn, batch, d0.hidden, eps, st) != cudaSuccess)
+            return cuda_fail(layers[l]);
+    }
+    return DN_OK;
 }
 
 DN_API int dn_set_state(dn_layer *l, int seq0, int n, const float *S, const float *ring,

@@ -436,7 +436,7 @@ cudaError_t launch_kc(const StreamParams &p, cudaStream_t st) {
 
 bool dn_core_stream_ok(const Dims &d, int B) {
     const long items = (long)B * d.n_v, per_cta = (items + num_sms() - 1) / num_sms();
-    return d.dk == D && d.dv == D && d.conv_k <= 4 && items >= 2L * num_sms() &&
+    return d.dk == D && d.dv == D && d.conv_k <= 4 && items >= 1 &&
            (d.in_rows + kTileM - 1) / kTileM <= kMaxMT && per_cta / d.n_v + 2 <= kMaxSeqCta;
 }
 

@@ -606,7 +606,7 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ part, const int *
     const int nseg = nseg_tab[tile];
     const float *pt = part + (size_t)tile * sv.max_seg * (NB_CHUNK * BM) + b * BM + r;
     float acc = 0.f;
-#pragma unroll 4
+#pragma unroll 8
     for (int k = 0; k < nseg; ++k) acc += __ldcg(pt + (size_t)k * (NB_CHUNK * BM));
     y[(size_t)(chunk * NB_CHUNK + b) * M + m] = s[m] * acc;
 }
@@ -627,7 +627,8 @@ GemmPlan plan_tc_gemm(int M, int K, int B) {
     g.TP = (B >= kTcMinBatch && g.nchunks * ((g.MT + 1) / 2) * g.UT >= 4 * num_sms()) ? 2 : 1;
     g.MP = (g.MT + g.TP - 1) / g.TP;
     g.U = g.nchunks * g.MP * g.UT;
-    g.G = std::min(num_sms(), g.U);
+    // one CTA per SM, two for the CUDA-core kernel at batch 1 (dn_gemv.cu)
+    g.G = std::min((B == 1 ? 2 : 1) * num_sms(), g.U);
     // segments per tile (pair): UT units meet at most ceil(UT / min_range) + 1 ranges
     const int min_range = g.U / g.G;
     g.max_seg = (g.UT + min_range - 1) / min_range + 1;

@@ -118,6 +118,10 @@ cudaError_t launch_ring_export(const Dims &d, const LayerDev &L, int seq0, int n
 
 int num_sms();
 
+// h += add (add may be NULL); xn = h / sqrt(mean(h^2) + eps), per sequence
+cudaError_t launch_residual_prenorm(float *h, const float *add, float *xn, int B, int hidden, float eps,
+                                    cudaStream_t st);
+
 // Programmatic dependent launch.  Every kernel of a step is launched with
 // the programmatic-serialization attribute (with_pdl), so it may start while
 // the kernel before it is still running.  A kernel may only read read-only

@@ -155,6 +155,27 @@ int dn_step(dn_layer *layer, int batch, const float *x, const float *g, const fl
 void dn_destroy(dn_layer *layer);
 
 /*
+ * dn_stack_step — one decode token through a stack of layers, the residual
+ * stream h carried between them (the pages' model runs 30 DeltaNet layers per
+ * token, page "qwen36: run the DeltaNet layer end to end on the card
+ * (Q36_DN_GPU=1)", section "Measured"):
+ *   for l = 0 .. n_layers-1:  h <- h + layer_l( h / sqrt(mean(h^2) + eps) )
+ * with an unweighted RMS pre-norm per sequence over `hidden`.
+ *   layers  n_layers layer handles with equal hidden and n_v_heads, on the
+ *           current device, each with max_batch >= batch
+ *   h       [batch][hidden] device, read and overwritten
+ *   g, beta [n_layers][batch][n_v_heads] device, each layer's gates
+ * Device pointers only; the call enqueues on `stream` (NULL: the first
+ * layer's stream) and uses the first layer's staging buffers for the
+ * normalised input and each layer's output.  Errors: DN_EINVAL (NULL, bad
+ * sizes, mismatched layers, eps < 0), DN_EFAILED (a failed layer), and the
+ * errors of dn_step; on an error the layers before the failing one have
+ * already advanced.
+ */
+int dn_stack_step(dn_layer *const *layers, int n_layers, int batch, float *h, const float *g,
+                  const float *beta, float eps, void *stream);
+
+/*
  * dn_debug_fail_next — failure injection for tests: the next dn_step on this
  * layer returns `code` (a negative DN_E* value) before any device work and
  * marks the layer failed, as the page's fake backend "can be told to fail;

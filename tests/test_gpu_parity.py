@@ -70,6 +70,17 @@ def test_tiny_ragged_batch_in_larger_layer():
     _assert_ok(run_parity(wl, max_batch=7))
 
 
+@pytest.mark.parametrize("batch", [1, 3, 8, 20])
+def test_35b_small_batch_in_a_layer_sized_for_64(batch):
+    """A layer sized for 64 sequences stepping fewer: the projections'
+    schedules (and so their segment counts) depend on the batch, and the
+    layer's scratch must hold the largest of them (batch 1 runs the most
+    segments per tile)."""
+    wl = custom_workload("b%d_in_64" % batch, SHAPE_35B, batch=batch, steps=6, seed=31 + batch,
+                         init_std=0.02)
+    _assert_ok(run_parity(wl, sample=np.array(sorted({0, batch - 1})), max_batch=64))
+
+
 @pytest.mark.parametrize("batch", [8, 9, 40, 64, 65, 130])
 def test_tiny_tensor_core_batches(batch):
     """Batches >= 8 take the tensor-core projections: padded batch columns
