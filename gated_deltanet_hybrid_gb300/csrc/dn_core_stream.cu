@@ -145,10 +145,9 @@ struct RowRef {
     int b, c;          // sequence, in_proj row
     bool conv, ring_w; // goes through the conv; this item writes its ring slot
 };
-__device__ __forceinline__ RowRef row_of(const StreamParams &p, int b, int h, int t) {
+__device__ __forceinline__ RowRef row_of(const StreamParams &p, int b, int h, int hq, int t) {
     RowRef r;
     r.b = b;
-    const int hq = h / p.group;
     const int region = t >> 7, o = t & (D - 1);
     r.c = region == 0 ? hq * D + o
         : region == 1 ? p.qk_dim + hq * D + o
@@ -156,7 +155,7 @@ __device__ __forceinline__ RowRef row_of(const StreamParams &p, int b, int h, in
                       : p.conv_ch + h * D + o;
     r.conv = region < 3;
     // q and k rows are shared by the value heads of a q/k head: the first writes
-    r.ring_w = region == 2 || (region < 2 && h % p.group == 0);
+    r.ring_w = region == 2 || (region < 2 && h == hq * p.group);
     return r;
 }
 
@@ -183,8 +182,8 @@ struct Ahead {
 
 template <int KC>
 __device__ __forceinline__ void load_ahead(const StreamParams &p, const StreamSmem &sm, int b0, int b, int h,
-                                           int t, Ahead<KC> &a) {
-    const RowRef r = row_of(p, b, h, t);
+                                           int hq, int t, Ahead<KC> &a) {
+    const RowRef r = row_of(p, b, h, hq, t);
     const int item = b * p.n_v + h;
     const int ptile = (r.b >> 6) * p.MT + (r.c >> 7);
     const float *pp = p.part_in + (size_t)ptile * p.max_seg * (64 * D) + (r.b & 63) * D + (r.c & (D - 1));
@@ -210,8 +209,8 @@ __device__ __forceinline__ void load_ahead(const StreamParams &p, const StreamSm
 // new input is written by the item that owns the row.
 template <int KC>
 __device__ __forceinline__ float build_input(const StreamParams &p, const StreamSmem &sm, int b0, int chunk0,
-                                             int b, int h, int t, const Ahead<KC> &a) {
-    const RowRef r = row_of(p, b, h, t);
+                                             int b, int h, int hq, int t, const Ahead<KC> &a) {
+    const RowRef r = row_of(p, b, h, hq, t);
     const int ns = sm.nseg[(r.b >> 6) - chunk0][r.c >> 7];
     float acc = 0.f;
 #pragma unroll
@@ -236,6 +235,28 @@ __device__ __forceinline__ float build_input(const StreamParams &p, const Stream
     return silu_f(cv);
 }
 
+// Gated RMSNorm of one item's readout (thread t < 128 holds o[t]; the warp
+// sums of o^2 are in ssq_o) and the store of the result: fp32 rows for the
+// CUDA-core out_proj, or bf16 hi/lo operand rows for the tensor-core one.
+__device__ __forceinline__ void store_norm(const StreamParams &p, const StreamSmem &sm, float o, int b, int h,
+                                           const float *rz, int t) {
+    const float total = (sm.ssq_o[0] + sm.ssq_o[1]) + (sm.ssq_o[2] + sm.ssq_o[3]);
+    const float rinv = 1.0f / sqrtf(total / (float)D + p.norm_eps);
+    const float n = o * rinv * sm.wn[t] * rz[t];
+    const int k = h * D + t;
+    if (p.xb_out == nullptr) {
+        p.nrm[(size_t)b * p.v_dim + k] = n;
+    } else {
+        const __nv_bfloat16 hi = __float2bfloat16_rn(n);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(n - __bfloat162float(hi));
+        uint8_t *ot = p.xb_out + ((size_t)(b >> 6) * p.kt_out + (k >> 6)) * kOpTile;
+        const int kc = (k & 63) >> 3, e = k & 7;
+        const int rh = 2 * (b & 63), rl = rh + 1;
+        *reinterpret_cast<__nv_bfloat16 *>(ot + op_chunk_offset(rh, kc) + e * 2) = hi;
+        *reinterpret_cast<__nv_bfloat16 *>(ot + op_chunk_offset(rl, kc) + e * 2) = lo;
+    }
+}
+
 template <int KC>
 __global__ void __launch_bounds__(NT, 1) dn_core_stream_kernel(const StreamParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -256,42 +277,46 @@ __global__ void __launch_bounds__(NT, 1) dn_core_stream_kernel(const StreamParam
     int issued = 0;  // (thread 0) tile loads issued so far
     if (t == 0)
         for (int j = 0; j < 2 && j < n_items; ++j, ++issued) load_tile(sm, j, p, i0 + j);
-    // the state is not written by the in_proj kernel, its partials are
-    pdl_wait();
-    if (t == 0) pdl_trigger();
-    // the segment counts of the CTA's batch chunks and its sequences' ring positions
+    // the sequences' ring positions (advanced by the previous step) first; the
+    // state is not written by the in_proj kernel, its partials and segment
+    // counts are
     const int b0 = i0 / p.n_v, chunk0 = b0 >> 6;
     const int nseq = n_items > 0 ? (i1 - 1) / p.n_v - b0 + 1 : 0;
     const int nchunk = n_items > 0 ? (((i1 - 1) / p.n_v) >> 6) - chunk0 + 1 : 0;
+    for (int i = t; i < nseq; i += NT) sm.dpos[i] = p.rpos[2 * (b0 + i)];
+    pdl_wait();
+    if (t == 0) pdl_trigger();
     for (int i = t; i < nchunk * p.MT; i += NT) {
         const int ci = i / p.MT, mt = i - ci * p.MT;
         sm.nseg[ci][mt] = p.nseg_in[(chunk0 + ci) * p.MT + mt];
     }
-    for (int i = t; i < nseq; i += NT) sm.dpos[i] = p.rpos[2 * (b0 + i)];
     __syncthreads();
 
+    // the item (b, h) and its q/k head hq, stepped without divisions
+    int b = b0, h = i0 - b0 * p.n_v, hq = h / p.group;
     Ahead<KC> ac;  // item j
-    if (n_items > 0) load_ahead(p, sm, b0, i0 / p.n_v, i0 % p.n_v, t, ac);
+    if (n_items > 0) load_ahead(p, sm, b0, b, h, hq, t, ac);
 
     const int c4 = t % LPR, r0 = t / LPR;
     bool failed = false;
+    float o_prev = 0.f;      // (t < D) the previous item's readout, normalised after the next barrier
+    int b_prev = 0, h_prev = 0;
     for (int j = 0; j < n_items; ++j) {
         const int item = i0 + j;
-        const int b = item / p.n_v, h = item - b * p.n_v;
         const int st = j % STAGES, rbuf = j & 1;
+        const int hn = h + 1 == p.n_v ? 0 : h + 1, bn = hn == 0 ? b + 1 : b;
+        const int hqn = hn == 0 ? 0 : (hn == (hq + 1) * p.group ? hq + 1 : hq);
 
-        // ---- the item's q^, k^, v, silu(z), gates; loads for the next items ----
-        const float u = build_input(p, sm, b0, chunk0, b, h, t, ac);
+        // ---- the item's q^, k^, v, silu(z), gates; loads for the next item ----
+        const float u = build_input(p, sm, b0, chunk0, b, h, hq, t, ac);
         const float gv = ac.gv, bv = ac.bv;
-        if (j + 1 < n_items) {
-            const bool wrap = h + 1 == p.n_v;
-            load_ahead(p, sm, b0, wrap ? b + 1 : b, wrap ? 0 : h + 1, t, ac);
-        }
+        if (j + 1 < n_items) load_ahead(p, sm, b0, bn, hn, hqn, t, ac);
         if (warp < 8) {  // q (warps 0-3) and k (warps 4-7): sums of squares
             const float sq = warp_sum(u * u);
             if (lane == 0) sm.ssq_qk[rbuf][warp] = sq;
         }
         __syncthreads();
+        if (j > 0 && t < D) store_norm(p, sm, o_prev, b_prev, h_prev, sm.rec[rbuf ^ 1] + 3 * D, t);
         float val = u;
         if (t < 2 * D) {
             const float *ssq = sm.ssq_qk[rbuf] + (t >> 7) * 4;
@@ -310,7 +335,7 @@ __global__ void __launch_bounds__(NT, 1) dn_core_stream_kernel(const StreamParam
             failed = true;
             break;
         }
-        const float *rq = sm.rec[rbuf], *rk = rq + D, *rv = rq + 2 * D, *rz = rq + 3 * D;
+        const float *rq = sm.rec[rbuf], *rk = rq + D, *rv = rq + 2 * D;
         const float eg = sm.gate[rbuf][0], bt = sm.gate[rbuf][1];
 
         float *tile = sm.tile[st];
@@ -371,35 +396,26 @@ __global__ void __launch_bounds__(NT, 1) dn_core_stream_kernel(const StreamParam
                 issued = j + 3;
             }
         }
-        // readout o = S^T q and gated RMSNorm over the head
-        float o = 0.f;
+        // readout o = S^T q; its gated RMSNorm over the head is finished after
+        // the next barrier (the next item's first, or the one after the loop)
         if (t < D) {
+            float o = 0.f;
 #pragma unroll
             for (int r = 0; r < RPP; ++r) o += sm.red[r][t];
             const float sq = warp_sum(o * o);
             if (lane == 0) sm.ssq_o[warp] = sq;
+            o_prev = o;
         }
-        __syncthreads();
-        if (t < D) {
-            const float total = (sm.ssq_o[0] + sm.ssq_o[1]) + (sm.ssq_o[2] + sm.ssq_o[3]);
-            const float rinv = 1.0f / sqrtf(total / (float)D + p.norm_eps);
-            const float n = o * rinv * sm.wn[t] * rz[t];
-            const int k = h * D + t;
-            if (p.xb_out == nullptr) {
-                p.nrm[(size_t)b * p.v_dim + k] = n;
-            } else {
-                const __nv_bfloat16 hi = __float2bfloat16_rn(n);
-                const __nv_bfloat16 lo = __float2bfloat16_rn(n - __bfloat162float(hi));
-                uint8_t *ot = p.xb_out + ((size_t)(b >> 6) * p.kt_out + (k >> 6)) * kOpTile;
-                const int kc = (k & 63) >> 3, e = k & 7;
-                const int rh = 2 * (b & 63), rl = rh + 1;
-                *reinterpret_cast<__nv_bfloat16 *>(ot + op_chunk_offset(rh, kc) + e * 2) = hi;
-                *reinterpret_cast<__nv_bfloat16 *>(ot + op_chunk_offset(rl, kc) + e * 2) = lo;
-            }
-        }
+        b_prev = b;
+        h_prev = h;
+        b = bn;
+        h = hn;
+        hq = hqn;
         // (red, delta, ssq_* and the other record buffer are next written after
         // a barrier of the next item)
     }
+    __syncthreads();
+    if (!failed && n_items > 0 && t < D) store_norm(p, sm, o_prev, b_prev, h_prev, sm.rec[(n_items - 1) & 1] + 3 * D, t);
     if (t == 0) {
         if (failed) atomicOr(p.err, 1);
         asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
