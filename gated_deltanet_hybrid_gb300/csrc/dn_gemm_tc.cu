@@ -39,15 +39,17 @@
 // converters free a weight stage as soon as they hold its bytes in
 // registers, so up to six weight copies are in flight per SM however long
 // the MMAs of a unit take; activation stages are freed by the MMAs.
-// Roles: warp 0 copies weights, warp 22 copies activations, warp 1 (one
-// thread) issues the MMAs, warps 2-17 convert the int8 unit to bf16 into one
-// of four tensor-memory A buffers (warp w owns lane quarter w % 4 and 32 k of
-// the unit: one row per lane), warps 18-21 read the accumulators
-// (tcgen05.ld) and write results.  Tensor memory (all 512 columns):
-// accumulators in columns 0-255, A buffers in 256-511, so conversion runs up
-// to three units ahead of the MMAs.  The weight producer does not wait for
-// the previous kernel of the step (programmatic dependent launch): weights
-// are read-only, the activations and the partial buffers are not.
+// Roles (28 warps): warp 0 copies weights, warp 26 copies activations,
+// warps 1 and 27 (one thread each) issue the MMAs of the first and second
+// row tile of a unit (two issuers: in this kernel a single thread issuing
+// both tiles' MMAs paces the whole pipeline), warps 2-17 convert the int8
+// unit to bf16 into one of two tensor-memory A buffers (warp w owns lane
+// quarter w % 4 and 64 k of one row tile: one row per lane), warps 18-25
+// read the accumulators (tcgen05.ld) and write results.  Tensor memory (all
+// 512 columns): the two row tiles' accumulators in columns 0-255, A buffers
+// in 256-511.  The weight producer does not wait for the previous kernel of
+// the step (programmatic dependent launch): weights are read-only, the
+// activations and the partial buffers are not.
 // Every wait is bounded (about one second of the global timer): on timeout
 // the kernel records an error in `err`, waits (bounded) for its own copies
 // and MMAs in flight, frees its tensor memory and returns.
@@ -71,7 +73,8 @@ constexpr int kConvWarps = 16;
 constexpr int kEpiWarps = 8;
 constexpr int kEpiWarp0 = 2 + kConvWarps;
 constexpr int kBProdWarp = kEpiWarp0 + kEpiWarps;
-constexpr int kThreads = 32 * (kBProdWarp + 1);      // 27 warps
+constexpr int kMma1Warp = kBProdWarp + 1;            // the second row tile's MMA issuer
+constexpr int kThreads = 32 * (kMma1Warp + 1);       // 28 warps
 constexpr int NABUF = 2;                             // tensor-memory A buffers (one pair unit each)
 constexpr uint32_t kATileBytes = BM * BK;            // 8 KB int8
 constexpr uint32_t kAUnitBytes = KU * kATileBytes;   // 16 KB: one row tile of a unit
@@ -96,9 +99,9 @@ struct __align__(1024) GemmSmem {
     uint64_t b_empty[BST];                   // MMAs done reading the stage
     uint64_t conv[NABUF];                    // A converted into tensor-memory buffer i (one arrival per converter warp)
     uint64_t a_free[NABUF];                  // MMAs done reading tensor-memory A buffer i
-    uint64_t acc_full;                       // accumulators ready for the epilogue
+    uint64_t acc_full;                       // accumulators ready for the epilogue (one commit per issuer)
     uint64_t acc_empty;                      // epilogue done reading the accumulators (one arrival per warp)
-    uint64_t drain;                          // all MMAs of this CTA completed
+    uint64_t drain[2];                       // all MMAs of an issuer completed
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -302,15 +305,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_i8_tc_kernel(const GemmParam
         }
         for (int s = 0; s < BST; ++s) {
             mbar_init(&sm.b_full[s], 1);
-            mbar_init(&sm.b_empty[s], 1);
+            mbar_init(&sm.b_empty[s], 2);  // both issuers' commits
         }
         for (int a = 0; a < NABUF; ++a) {
             mbar_init(&sm.conv[a], kConvWarps);
-            mbar_init(&sm.a_free[a], 1);
+            mbar_init(&sm.a_free[a], 2);
         }
-        mbar_init(&sm.acc_full, 1);
+        mbar_init(&sm.acc_full, 2);
         mbar_init(&sm.acc_empty, kEpiWarps);
-        mbar_init(&sm.drain, 1);
+        mbar_init(&sm.drain[0], 1);
+        mbar_init(&sm.drain[1], 1);
         sm.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -381,9 +385,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_i8_tc_kernel(const GemmParam
                     mbar_wait(&sm.b_full[it % BST], (it / BST) & 1, abort_flag, true);
             }
         }
-    } else if (warp == 1) {
-        // ---- MMA issuer -----------------------------------------------------------
+    } else if (warp == 1 || warp == kMma1Warp) {
+        // ---- MMA issuers: row tile tp of the pair, its own accumulator (columns
+        //      128 tp); both follow every unit's barriers, so with a single row
+        //      tile the second one only commits -------------------------------------
         if (lane == 0) {
+            const int tp = warp == 1 ? 0 : 1;
             int it = 0, seg = 0;
             bool ok = true;
             for (int u = u0; u < u1 && ok; ++seg) {
@@ -398,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_i8_tc_kernel(const GemmParam
                     break;
                 }
                 tc_fence_after();
-                const int useg = u;  // first unit of this segment: overwrite the accumulators
+                const int useg = u;  // first unit of this segment: overwrite the accumulator
                 for (; u < ue; ++u, ++it) {
                     const int sb = it % BST, ab = it % NABUF;
                     if (!mbar_wait(&sm.conv[ab], (it / NABUF) & 1, abort_flag) ||
@@ -410,16 +417,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_i8_tc_kernel(const GemmParam
                     // K steps of 16: 8 tensor-memory columns of A and 32 bytes of
                     // B's rows (+2 in the descriptor's address field) each; the
                     // second 64-k tile's B starts 16 KB (+1024) further.  Row tile
-                    // tp of the pair: accumulator columns 128 tp, A columns 64 tp.
-                    const uint32_t ta = tmem + kTmemA + (uint32_t)ab * kACols;
-                    const uint64_t bd = smem_desc_sw128(smem_u32(sm.b16[sb]));
-                    const bool two_k = (u % p.UT) * KU + 1 < p.KT;
-                    const uint32_t acc0 = u == useg ? 0u : 1u;
-                    mma_bf16_ts_x4(tmem, ta, bd, idesc, acc0);
-                    if (two_k) mma_bf16_ts_x4(tmem, ta + 32u, bd + 1024u, idesc, 1u);
-                    if (ntl == 2) {
-                        mma_bf16_ts_x4(tmem + 128u, ta + 64u, bd, idesc, acc0);
-                        if (two_k) mma_bf16_ts_x4(tmem + 128u, ta + 96u, bd + 1024u, idesc, 1u);
+                    // tp: accumulator columns 128 tp, A columns 64 tp of the buffer.
+                    if (tp < ntl) {
+                        const uint32_t ta = tmem + kTmemA + (uint32_t)ab * kACols + (uint32_t)tp * 64u;
+                        const uint32_t dt = tmem + (uint32_t)tp * 128u;
+                        const uint64_t bd = smem_desc_sw128(smem_u32(sm.b16[sb]));
+                        mma_bf16_ts_x4(dt, ta, bd, idesc, u == useg ? 0u : 1u);
+                        if ((u % p.UT) * KU + 1 < p.KT) mma_bf16_ts_x4(dt, ta + 32u, bd + 1024u, idesc, 1u);
                     }
                     mma_commit(&sm.b_empty[sb]);
                     mma_commit(&sm.a_free[ab]);
@@ -428,8 +432,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_i8_tc_kernel(const GemmParam
                 mma_commit(&sm.acc_full);
             }
             if (!ok) *abort_flag = 1;
-            mma_commit(&sm.drain);  // arrives once every MMA issued above has completed
-            mbar_wait(&sm.drain, 0, abort_flag, true);
+            mma_commit(&sm.drain[tp]);  // arrives once every MMA issued above has completed
+            mbar_wait(&sm.drain[tp], 0, abort_flag, true);
         }
     } else if (warp < kEpiWarp0) {
         // ---- int8 -> bf16 converters: lane = row; warp group g = (w - 2) / 4
