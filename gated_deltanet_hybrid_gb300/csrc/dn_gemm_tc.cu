@@ -24,10 +24,12 @@
 // converters' int8 reads and the MMA's B reads.
 //
 // Work split (stream-K).  A unit is one (batch chunk, m tile, k tile).  The
-// grid has one CTA per SM; CTA c takes the contiguous unit range
-// [c*U/G, (c+1)*U/G), so all SMs get the same number of units whatever the
-// tile count.  A range covers the tail of one m tile and the head of the next
-// (a "segment" each); two TMEM accumulators alternate between segments.
+// grid has at most one CTA per SM, G = the fewest that keep each CTA at
+// ceil(U / SMs) units; CTA c takes the contiguous unit range
+// [c*U/G, (c+1)*U/G), so all CTAs get (nearly) the same number of units
+// whatever the tile count.  A range covers the tail of one m tile and the
+// head of the next (a "segment" each); two TMEM accumulators alternate
+// between segments.
 // Every segment's partial sums go to a slot of a partial buffer (schedule in
 // dn_sched.cuh); the consumer sums a tile's slots in slot order (the state
 // kernel for the in_proj, splitk_reduce_kernel for the out_proj), so
@@ -633,6 +635,12 @@ GemmPlan plan_tc_gemm(int M, int K, int B) {
     g.U = g.nchunks * g.MP * g.UT;
     // one CTA per SM, two for the CUDA-core kernel at batch 1 (dn_gemv.cu)
     g.G = std::min((B == 1 ? 2 : 1) * num_sms(), g.U);
+    // then the fewest CTAs that still take no more than ceil(U / G) units
+    // each: every CTA gets the same count (the step waits on the slowest one),
+    // segments are longer, and the SMs left over take the next kernel's CTAs
+    // early
+    const int per = (g.U + g.G - 1) / g.G;
+    g.G = (g.U + per - 1) / per;
     // segments per tile (pair): UT units meet at most ceil(UT / min_range) + 1 ranges
     const int min_range = g.U / g.G;
     g.max_seg = (g.UT + min_range - 1) / min_range + 1;

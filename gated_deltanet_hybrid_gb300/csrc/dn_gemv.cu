@@ -9,9 +9,10 @@
 //
 // W is stored as contiguous 8 KB tiles of 128 rows x 64 int8 in four 16-k
 // parts (dn_internal.cuh; shared with the tensor-core kernel) and the work is
-// split exactly like the tensor-core projection (stream-K, dn_sched.cuh): one
-// CTA per SM takes a contiguous range of units, each 4 consecutive k tiles of
-// one row tile (32 KB).  The weights stream straight into registers: lane l
+// split exactly like the tensor-core projection (stream-K, dn_sched.cuh): up
+// to one CTA per SM (two at batch 1), as few as keep every CTA at the same
+// unit count, each takes a contiguous range of units, each unit 4
+// consecutive k tiles of one row tile (32 KB).  The weights stream straight into registers: lane l
 // of warp w loads 16 bytes (16 weights of row 8w + l%8, k part l/8) of each
 // tile with a 16-byte load, so a warp reads 4 x 128 contiguous bytes, and the
 // loads of the next D units are always in flight (a software pipeline over
