@@ -20,14 +20,15 @@
 //    (dn_sched.cuh) times the row scale; q, k, v go through the conv over the
 //    ring (K-1 history slots read, the newest written) and SiLU, z through
 //    SiLU; q and k are L2-normalised with fp32 warp sums combined in a fixed
-//    order.  The CTA's segment counts and ring positions are read once into
-//    shared memory, so an item's loads (partials, ring history, row scale and
+//    order.  The CTA's ring positions are read once into shared memory, so
+//    an item's loads (segment count, partials, ring history, row scale and
 //    conv weights) depend on nothing else and are issued one item ahead (as
 //    volatile loads, so that the compiler keeps them there): their latency
 //    hides behind the previous item's tile;
-//  * the first two state tiles are fetched before the kernel waits for the
-//    in_proj kernel (programmatic dependent launch): the state is not written
-//    by it, the partials are.
+//  * the first two state tiles, and the first item's loads that do not come
+//    from the in_proj kernel, are issued before the kernel waits for it
+//    (programmatic dependent launch): the state, ring, gates and weights are
+//    not written by it, the partials and segment counts are.
 //
 // Every wait is bounded (about one second); on timeout the kernel records an
 // error in `err`, waits (bounded) for its own bulk copies and returns.
@@ -49,7 +50,6 @@ constexpr int LPR = D / 4;           // 32 lanes across a row (float4 each)
 constexpr int RPP = NT / LPR;        // 16 rows per pass
 constexpr int NP = D / RPP;          // 8 float4 per thread
 constexpr int PV = 6;                // partial slots fetched ahead (more are read on the spot)
-constexpr int kMaxMT = 256;          // in_proj row tiles (in_rows <= 32768)
 constexpr int kMaxSeqCta = 64;       // sequences one CTA's item range may touch
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
@@ -80,7 +80,6 @@ struct __align__(128) StreamSmem {
     float ssq_o[4];
     float ssq_qk[2][8];         // warp sums of squares (warps 0-3 q, 4-7 k), double-buffered
     float wn[D];                // gated-RMSNorm weight
-    int nseg[2][kMaxMT];        // in_proj segment counts of the CTA's (up to 2) batch chunks
     int dpos[kMaxSeqCta];       // ring positions of the CTA's sequences
     uint64_t full[STAGES];
 };
@@ -178,18 +177,23 @@ __device__ __forceinline__ float ld_nc(const float *ptr) {
 template <int KC>
 struct Ahead {
     float pv[PV], hist[KC - 1], sc, wc[KC], gv, bv;
+    int ns;  // segment count of the row's tile
 };
 
+__device__ __forceinline__ int ld_cg_s32(const int *ptr) {
+    int v;
+    asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(ptr));
+    return v;
+}
+
+// The loads that the in_proj kernel does not feed: ring history, row scale,
+// conv weights, gates (for the first item they go out before the kernel
+// waits for the in_proj kernel).
 template <int KC>
-__device__ __forceinline__ void load_ahead(const StreamParams &p, const StreamSmem &sm, int b0, int b, int h,
-                                           int hq, int t, Ahead<KC> &a) {
+__device__ __forceinline__ void load_ahead_fixed(const StreamParams &p, const StreamSmem &sm, int b0, int b,
+                                                 int h, int hq, int t, Ahead<KC> &a) {
     const RowRef r = row_of(p, b, h, hq, t);
     const int item = b * p.n_v + h;
-    const int ptile = (r.b >> 6) * p.MT + (r.c >> 7);
-    const float *pp = p.part_in + (size_t)ptile * p.max_seg * (64 * D) + (r.b & 63) * D + (r.c & (D - 1));
-#pragma unroll
-    for (int k = 0; k < PV; ++k)  // slots past max_seg fall back to slot 0
-        a.pv[k] = ld_cg(pp + (size_t)(k < p.max_seg ? k : 0) * (64 * D));
     const int cr = r.conv ? r.c : 0;  // z rows read channel 0's ring and weights
     const float *rb = p.ring + (size_t)r.b * KC * p.conv_ch + cr;
     int slot = sm.dpos[r.b - b0];
@@ -204,14 +208,32 @@ __device__ __forceinline__ void load_ahead(const StreamParams &p, const StreamSm
     a.gv = ld_cg(p.g + item);  // [B][n_v] = item order
     a.bv = ld_cg(p.beta + item);
 }
+// The in_proj kernel's output for the row: segment count and partials.
+template <int KC>
+__device__ __forceinline__ void load_ahead_part(const StreamParams &p, int b, int h, int hq, int t,
+                                                Ahead<KC> &a) {
+    const RowRef r = row_of(p, b, h, hq, t);
+    const int ptile = (r.b >> 6) * p.MT + (r.c >> 7);
+    a.ns = ld_cg_s32(p.nseg_in + ptile);
+    const float *pp = p.part_in + (size_t)ptile * p.max_seg * (64 * D) + (r.b & 63) * D + (r.c & (D - 1));
+#pragma unroll
+    for (int k = 0; k < PV; ++k)  // slots past max_seg fall back to slot 0
+        a.pv[k] = ld_cg(pp + (size_t)(k < p.max_seg ? k : 0) * (64 * D));
+}
+template <int KC>
+__device__ __forceinline__ void load_ahead(const StreamParams &p, const StreamSmem &sm, int b0, int b, int h,
+                                           int hq, int t, Ahead<KC> &a) {
+    load_ahead_part(p, b, h, hq, t, a);
+    load_ahead_fixed(p, sm, b0, b, h, hq, t, a);
+}
 
 // The row's in_proj output, conv + SiLU (z: SiLU only); the ring slot of the
 // new input is written by the item that owns the row.
 template <int KC>
-__device__ __forceinline__ float build_input(const StreamParams &p, const StreamSmem &sm, int b0, int chunk0,
-                                             int b, int h, int hq, int t, const Ahead<KC> &a) {
+__device__ __forceinline__ float build_input(const StreamParams &p, const StreamSmem &sm, int b0, int b, int h,
+                                             int hq, int t, const Ahead<KC> &a) {
     const RowRef r = row_of(p, b, h, hq, t);
-    const int ns = sm.nseg[(r.b >> 6) - chunk0][r.c >> 7];
+    const int ns = a.ns;
     float acc = 0.f;
 #pragma unroll
     for (int k = 0; k < PV; ++k)
@@ -280,22 +302,17 @@ __global__ void __launch_bounds__(NT, 1) dn_core_stream_kernel(const StreamParam
     // the sequences' ring positions (advanced by the previous step) first; the
     // state is not written by the in_proj kernel, its partials and segment
     // counts are
-    const int b0 = i0 / p.n_v, chunk0 = b0 >> 6;
+    const int b0 = i0 / p.n_v;
     const int nseq = n_items > 0 ? (i1 - 1) / p.n_v - b0 + 1 : 0;
-    const int nchunk = n_items > 0 ? (((i1 - 1) / p.n_v) >> 6) - chunk0 + 1 : 0;
     for (int i = t; i < nseq; i += NT) sm.dpos[i] = p.rpos[2 * (b0 + i)];
-    pdl_wait();
-    if (t == 0) pdl_trigger();
-    for (int i = t; i < nchunk * p.MT; i += NT) {
-        const int ci = i / p.MT, mt = i - ci * p.MT;
-        sm.nseg[ci][mt] = p.nseg_in[(chunk0 + ci) * p.MT + mt];
-    }
     __syncthreads();
-
     // the item (b, h) and its q/k head hq, stepped without divisions
     int b = b0, h = i0 - b0 * p.n_v, hq = h / p.group;
     Ahead<KC> ac;  // item j
-    if (n_items > 0) load_ahead(p, sm, b0, b, h, hq, t, ac);
+    if (n_items > 0) load_ahead_fixed(p, sm, b0, b, h, hq, t, ac);
+    pdl_wait();
+    if (t == 0) pdl_trigger();
+    if (n_items > 0) load_ahead_part(p, b, h, hq, t, ac);
 
     const int c4 = t % LPR, r0 = t / LPR;
     bool failed = false;
@@ -308,7 +325,7 @@ __global__ void __launch_bounds__(NT, 1) dn_core_stream_kernel(const StreamParam
         const int hqn = hn == 0 ? 0 : (hn == (hq + 1) * p.group ? hq + 1 : hq);
 
         // ---- the item's q^, k^, v, silu(z), gates; loads for the next item ----
-        const float u = build_input(p, sm, b0, chunk0, b, h, hq, t, ac);
+        const float u = build_input(p, sm, b0, b, h, hq, t, ac);
         const float gv = ac.gv, bv = ac.bv;
         if (j + 1 < n_items) load_ahead(p, sm, b0, bn, hn, hqn, t, ac);
         if (warp < 8) {  // q (warps 0-3) and k (warps 4-7): sums of squares
@@ -452,8 +469,7 @@ cudaError_t launch_kc(const StreamParams &p, cudaStream_t st) {
 
 bool dn_core_stream_ok(const Dims &d, int B) {
     const long items = (long)B * d.n_v, per_cta = (items + num_sms() - 1) / num_sms();
-    return d.dk == D && d.dv == D && d.conv_k <= 4 && items >= 1 &&
-           (d.in_rows + kTileM - 1) / kTileM <= kMaxMT && per_cta / d.n_v + 2 <= kMaxSeqCta;
+    return d.dk == D && d.dv == D && d.conv_k <= 4 && items >= 1 && per_cta / d.n_v + 2 <= kMaxSeqCta;
 }
 
 cudaError_t launch_dn_core_stream(const Dims &d, const LayerDev &L, int B, const float *g,
