@@ -552,8 +552,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_i8_tc_kernel(const GemmParam
 // 2b (hi) and 2b+1 (lo) of sequence b; k >= K and b in [Bc, Bpad) are zero.
 __global__ void pack_b_kernel(const float *__restrict__ x, uint8_t *__restrict__ xb, int B, int K,
                               int KT) {
+    pdl_trigger();  // the projection after this kernel may start streaming its weights
     pdl_wait();
-    pdl_trigger();
     const int kt = blockIdx.x, chunk = blockIdx.y;
     const int Bc = min(NB_CHUNK, B - chunk * NB_CHUNK);
     const int Bpad = (Bc + 7) & ~7;
@@ -592,8 +592,8 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ part, const int *
                                      const float *__restrict__ s, float *__restrict__ y,
                                      SchedView sv, int M, int B, int32_t *__restrict__ rpos,
                                      int conv_k) {
+    pdl_trigger();  // the next step's first kernels may be launched already
     pdl_wait();
-    pdl_trigger();
     if (rpos != nullptr && blockIdx.x == 0 && blockIdx.y == 0) {
         for (int b = threadIdx.x; b < B; b += blockDim.x) {
             int2 q = reinterpret_cast<int2 *>(rpos)[b];

@@ -127,8 +127,13 @@ cudaError_t launch_residual_prenorm(float *h, const float *add, float *xn, int B
 // the kernel before it is still running.  A kernel may only read read-only
 // data (weights, the recurrent state when the previous kernel does not touch
 // it) before pdl_wait(), which returns once the previous kernel has
-// completed and its writes are visible; it signals pdl_trigger() only after
-// its own pdl_wait(), so at most two kernels of the chain overlap.
+// completed and its writes are visible.  Every kernel calls pdl_wait() before
+// it completes, so "completed" is transitive down the chain: once a kernel's
+// wait returns, every earlier kernel of the stream has completed too.  That
+// lets the small kernels ahead of a projection (packing the activations, the
+// out_proj reduction) signal pdl_trigger() first thing, so that the
+// projection's CTAs are launched, and stream their weights, while those
+// kernels still wait or run; the others signal it after their own wait.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

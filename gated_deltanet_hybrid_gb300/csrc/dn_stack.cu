@@ -24,8 +24,8 @@ __global__ void __launch_bounds__(kNormThreads) residual_prenorm_kernel(float *_
                                                                         float *__restrict__ xn, int hidden,
                                                                         float eps) {
     __shared__ float wsum[kNormThreads / 32];
-    pdl_wait();  // h and add come from the previous kernels
-    pdl_trigger();
+    pdl_trigger();  // the next layer's first kernels may be launched already
+    pdl_wait();     // h and add come from the previous kernels
     float *hb = h + (size_t)blockIdx.x * hidden;
     const float *ab = add == nullptr ? nullptr : add + (size_t)blockIdx.x * hidden;
     float ss = 0.f;
