@@ -289,19 +289,17 @@ __global__ void __launch_bounds__(NT, 1) dn_core_stream_kernel(const StreamParam
     const int i1 = (int)(((unsigned)(blockIdx.x + 1) * (unsigned)p.items) / gridDim.x);
     const int n_items = i1 - i0;
 
+    int issued = 0;  // (thread 0) tile loads issued so far
     if (t == 0) {
         for (int s = 0; s < STAGES; ++s)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&sm.full[s])));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    if (t < D) sm.wn[t] = p.w_norm[t];
-    __syncthreads();
-    int issued = 0;  // (thread 0) tile loads issued so far
-    if (t == 0)
         for (int j = 0; j < 2 && j < n_items; ++j, ++issued) load_tile(sm, j, p, i0 + j);
-    // the sequences' ring positions (advanced by the previous step) first; the
-    // state is not written by the in_proj kernel, its partials and segment
-    // counts are
+    }
+    // the norm weights and the sequences' ring positions (advanced by the
+    // previous step) in one round trip; the state is not written by the
+    // in_proj kernel, its partials and segment counts are
+    if (t < D) sm.wn[t] = p.w_norm[t];
     const int b0 = i0 / p.n_v;
     const int nseq = n_items > 0 ? (i1 - 1) / p.n_v - b0 + 1 : 0;
     for (int i = t; i < nseq; i += NT) sm.dpos[i] = p.rpos[2 * (b0 + i)];
