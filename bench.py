@@ -12,7 +12,11 @@ the same run and reported under "batch1".
 Timed regions rotate over --layers independent layer objects (distinct
 weights and states), so the working set of consecutive steps (about 300 MB
 per layer-step at batch 64) is larger than the 129 MB L2: nothing of a step
-is served from L2 by the previous step of the same layer.
+is served from L2 by the previous step of the same layer.  The timed region
+replays a CUDA graph of one dn_step per layer object (the same kernels and
+work as eager calls, without the per-launch CPU cost); --no-graph times
+eager dn_step calls.  The end-to-end figure ("e2e") always goes through
+dn_step with pinned host buffers.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -517,8 +521,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=tuple(WORKLOAD_SPECS), default="35b_b64")
     ap.add_argument("--layers", type=int, default=8, help="layer objects rotated in the timed region")
-    ap.add_argument("--graph", action=argparse.BooleanOptionalAction, default=False,
-                    help="replay a CUDA graph of one step per layer in the timed region")
+    ap.add_argument("--graph", action=argparse.BooleanOptionalAction, default=True,
+                    help="replay a CUDA graph of one step per layer in the timed region "
+                         "(--no-graph: eager dn_step calls)")
     ap.add_argument("--secondary", action=argparse.BooleanOptionalAction, default=True,
                     help="also measure the batch-1 workload")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
