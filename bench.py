@@ -25,6 +25,10 @@ workload (the sequences of a batch are independent; nothing is exchanged);
 `value` counts the layer-steps of all ranks divided by the slowest rank's
 time.  --impl reference times the CPU oracle (float64 numpy) on a bounded
 sample of the same workload, on rank 0 only.
+
+Other workloads (--workload): 35b_b1 and 35b_b8 (the same layer at batch 1
+and 8), stack30_b1 and stack30_b16 (30 distinct layers per token through
+dn_stack_step; the line adds tokens_per_s and ms_per_token).
 """
 from __future__ import annotations
 
@@ -409,7 +413,102 @@ class DistCtx:
 WORKLOAD_SPECS = {
     "35b_b64": (SHAPE_35B, 64, 0.02),
     "35b_b1": (SHAPE_35B, 1, 0.0),
+    "35b_b8": (SHAPE_35B, 8, 0.0),  # the batch of the 2048-token long-prompt parity case
 }
+# stacks of distinct layers driven through dn_stack_step (zero initial state)
+STACK_SPECS = {
+    "stack30_b1": (SHAPE_35B, 1, 30),
+    "stack30_b16": (SHAPE_35B, 16, 30),
+}
+
+
+def bench_stack(cfg, B, n_layers, steps, warmup, seed, use_graph, dist_ctx, torch, abi):
+    """Tokens through a stack of n_layers layer objects: each timed token
+    starts the residual stream from a fresh input row set (as a new token's
+    embedding would) and runs dn_stack_step over every layer."""
+    dev = torch.device("cuda")
+    layers = setup_layers(cfg, B, n_layers, 0.0, seed, torch, abi)
+    rng = np.random.Generator(np.random.PCG64(seed + 7))
+    h0 = torch.from_numpy(rng.standard_normal((B, cfg.hidden)).astype(np.float32)).to(dev)
+    gb = [gates_from_ab(rng.standard_normal((B, cfg.n_v_heads)), rng.standard_normal((B, cfg.n_v_heads)))
+          for _ in range(n_layers)]
+    g = torch.from_numpy(np.stack([x[0] for x in gb]).astype(np.float32)).to(dev)
+    beta = torch.from_numpy(np.stack([x[1] for x in gb]).astype(np.float32)).to(dev)
+    h = torch.empty_like(h0)
+    stream = torch.cuda.current_stream()
+
+    def token():
+        h.copy_(h0)
+        abi.dn_stack_step(layers, B, h, g, beta)
+
+    for _ in range(warmup):
+        token()
+    torch.cuda.synchronize()
+    graph = None
+    if use_graph:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream()
+            cap.wait_stream(stream)
+            with torch.cuda.stream(cap):
+                with torch.cuda.graph(graph, stream=cap):
+                    token()
+            torch.cuda.synchronize()
+        except Exception as e:  # capture not possible: time eager launches
+            print(f"[bench] graph capture failed ({e}); timing eager launches", file=sys.stderr)
+            graph = None
+    dist_ctx.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(steps):
+        if graph is not None:
+            graph.replay()
+        else:
+            token()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    dist_ctx.barrier()
+    t1 = time.time()
+    ms = dist_ctx.max(ev0.elapsed_time(ev1))
+    launches = steps * (n_layers * abi.dn_step_kernels(layers[0], B) + n_layers + 1)
+    del graph
+    for l in layers:
+        abi.dn_destroy(l)
+    return {"ms": ms, "t_wall": (t0, t1), "graph": use_graph, "launches": launches}
+
+
+def run_stack(args, torch, dist_ctx):
+    from gated_deltanet_hybrid_gb300 import abi
+    abi.load_library()
+    hbm_peak, peak_kind = load_peaks()
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+    except Exception:
+        pass
+    cfg, B, n_layers = STACK_SPECS[args.workload]
+    with ClockSampler(uuid) as clk:
+        r = bench_stack(cfg, B, n_layers, args.steps, args.warmup, 3, args.graph, dist_ctx, torch, abi)
+    n = dist_ctx.world
+    s = r["ms"] / 1e3
+    ms_layer = r["ms"] / (args.steps * n_layers)
+    sb = step_bytes(cfg, B)
+    return {
+        "metric": METRIC, "value": n * args.steps * n_layers / s, "unit": UNIT, "n_gpus": n,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_layer, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32 (int8 weights)",
+        "data": "synthetic (seeded random weights and inputs of the 35B-shape layer, zero initial state)",
+        "config": {"workload": args.workload, "layers": n_layers, "batch": B, "hidden": cfg.hidden,
+                   "l2": f"inputs larger than L2: {n_layers} distinct layers per token",
+                   "launch": "cuda graph of one token" if r["graph"] else "eager",
+                   "parallelism": f"replicas x{n}" if n > 1 else "single GPU"},
+        "tokens_per_s": n * args.steps * B / s, "ms_per_token": r["ms"] / args.steps,
+        "hbm_gbs_step": sb / (ms_layer / 1e3) / 1e9,
+        "step_roofline_frac": sb / (ms_layer / 1e3) / 1e9 / hbm_peak, "peak_kind": peak_kind,
+        "clocks": clk.summary(*r["t_wall"]), "gpu_launches": r["launches"] * n,
+    }
 
 
 def run_ours(args, torch, dist_ctx):
@@ -489,7 +588,11 @@ def run_reference(args, dist_ctx):
         return None
     from oracle import OracleLayer
     from gated_deltanet_hybrid_gb300.inputs import random_state, zero_state
-    cfg, B, init_std = WORKLOAD_SPECS[args.workload]
+    if args.workload in STACK_SPECS:
+        cfg, B, _ = STACK_SPECS[args.workload]
+        init_std = 0.0
+    else:
+        cfg, B, init_std = WORKLOAD_SPECS[args.workload]
     rng = np.random.Generator(np.random.PCG64(99))
     w = make_weights(cfg, rng)
     st = random_state(cfg, 1, rng, init_std) if init_std > 0 else zero_state(cfg, 1)
@@ -519,7 +622,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=tuple(WORKLOAD_SPECS), default="35b_b64")
+    ap.add_argument("--workload", choices=tuple(WORKLOAD_SPECS) + tuple(STACK_SPECS), default="35b_b64")
     ap.add_argument("--layers", type=int, default=8, help="layer objects rotated in the timed region")
     ap.add_argument("--graph", action=argparse.BooleanOptionalAction, default=True,
                     help="replay a CUDA graph of one step per layer in the timed region "
@@ -541,7 +644,7 @@ def main(argv=None):
             if not torch.cuda.is_available():
                 raise SystemExit("bench.py --impl ours needs a CUDA device")
             torch.cuda.set_device(dist_ctx.local_rank)
-            line = run_ours(args, torch, dist_ctx)
+            line = (run_stack if args.workload in STACK_SPECS else run_ours)(args, torch, dist_ctx)
         if line is not None and dist_ctx.rank == 0:
             print(json.dumps(line), flush=True)
     finally:
