@@ -33,10 +33,10 @@ def _json_lines(text):
     return [json.loads(l) for l in text.splitlines() if l.startswith("{")]
 
 
-def test_max_over_ranks_and_barriers_with_two_gloo_ranks():
-    r = _torchrun([os.path.join(ROOT, "tests", "dist_rank_probe.py")], timeout=240)
+def test_max_over_ranks_and_barriers_with_two_gloo_ranks(tmp_path):
+    r = _torchrun([os.path.join(ROOT, "tests", "dist_rank_probe.py"), str(tmp_path)], timeout=240)
     assert r.returncode == 0, r.stderr[-2000:]
-    lines = sorted(_json_lines(r.stdout), key=lambda d: d["rank"])
+    lines = [json.loads((tmp_path / f"rank{k}.json").read_text()) for k in range(2)]
     assert [d["rank"] for d in lines] == [0, 1]
     for d in lines:
         assert d["world"] == 2 and d["backend"] == "gloo"
