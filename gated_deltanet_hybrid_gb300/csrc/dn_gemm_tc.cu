@@ -35,8 +35,9 @@
 // kernel for the in_proj, splitk_reduce_kernel for the out_proj), so
 // results do not depend on scheduling and no CTA waits on another.
 //
-// A unit is 128 rows x 128 k (16 KB of int8 weights, one bulk copy: copies
-// this size keep the per-copy hand-off cost small against the HBM time).
+// A unit is one or two row tiles (TP) x 128 k: per row tile 16 KB of int8
+// weights, one bulk copy (copies this size keep the per-copy hand-off cost
+// small against the HBM time).
 // Weights and activations stream through separate shared-memory rings: the
 // converters free a weight stage as soon as they hold its bytes in
 // registers, so up to six weight copies are in flight per SM however long
