@@ -26,7 +26,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdn.so")
 
 #: every call the header declares, in declaration order
 ABI_SYMBOLS = ("dn_create", "dn_set_state", "dn_get_state", "dn_step", "dn_stack_step", "dn_destroy",
-               "dn_debug_fail_next", "dn_profile_next_step", "dn_proj_i8_noalloc",
+               "dn_debug_fail_next", "dn_debug_expire_wait", "dn_profile_next_step", "dn_proj_i8_noalloc",
                "dn_device_bytes", "dn_step_kernels", "dn_strerror")
 
 
@@ -77,6 +77,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dn_destroy.restype = None
     lib.dn_debug_fail_next.argtypes = [vp, i32]
     lib.dn_debug_fail_next.restype = i32
+    lib.dn_debug_expire_wait.argtypes = [vp, i32]
+    lib.dn_debug_expire_wait.restype = i32
     lib.dn_profile_next_step.argtypes = [vp, ctypes.POINTER(ctypes.c_void_p)]
     lib.dn_profile_next_step.restype = i32
     lib.dn_proj_i8_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp]
@@ -215,6 +217,12 @@ def dn_destroy(layer) -> None:
 
 def dn_debug_fail_next(layer, code: int, check: bool = True) -> int:
     return _check("dn_debug_fail_next", load_library().dn_debug_fail_next(layer, int(code)), check)
+
+
+def dn_debug_expire_wait(layer, limit_us: int, check: bool = True) -> int:
+    """The next dn_step first runs a bounded device wait that runs out after
+    limit_us; the give-up surfaces at the next dn_get_state (DN_ECUDA)."""
+    return _check("dn_debug_expire_wait", load_library().dn_debug_expire_wait(layer, int(limit_us)), check)
 
 
 def dn_profile_next_step(layer, events, check: bool = True) -> int:

@@ -21,6 +21,7 @@ struct dn_layer {
     int device;
     int failed;
     int fail_next;
+    int expire_us_next;  // dn_debug_expire_wait: bounded device wait before the next step
     cudaEvent_t prof[5];  // one-shot per-stage events for the next step
     int prof_armed;
     size_t bytes;
@@ -257,6 +258,12 @@ DN_API int dn_debug_fail_next(dn_layer *l, int code) {
     return DN_OK;
 }
 
+DN_API int dn_debug_expire_wait(dn_layer *l, int limit_us) {
+    if (l == nullptr || limit_us < 0 || limit_us > 1000000) return DN_EINVAL;
+    l->expire_us_next = limit_us;
+    return DN_OK;
+}
+
 DN_API int dn_profile_next_step(dn_layer *l, void *const *events) {
     if (l == nullptr) return DN_EINVAL;
     if (events == nullptr) {
@@ -396,6 +403,11 @@ DN_API int dn_step(dn_layer *l, int batch, const float *x, const float *g, const
         gd = L.g_stage;
         bd = L.beta_stage;
         od = L.out_stage;
+    }
+    if (l->expire_us_next > 0) {
+        const int us = l->expire_us_next;
+        l->expire_us_next = 0;
+        DN_TRY(l, dn::launch_expire_wait(L.err, us, st));
     }
     const bool prof = l->prof_armed != 0;
     l->prof_armed = 0;

@@ -118,6 +118,10 @@ cudaError_t launch_ring_export(const Dims &d, const LayerDev &L, int seq0, int n
 
 int num_sms();
 
+// dn_debug_expire_wait: one bounded wait that runs out after limit_us and
+// sets the device error word (dn_debug.cu)
+cudaError_t launch_expire_wait(int *err, int limit_us, cudaStream_t st);
+
 // h += add (add may be NULL); xn = h / sqrt(mean(h^2) + eps), per sequence
 cudaError_t launch_residual_prenorm(float *h, const float *add, float *xn, int B, int hidden, float eps,
                                     cudaStream_t st);

@@ -185,6 +185,20 @@ int dn_stack_step(dn_layer *const *layers, int n_layers, int batch, float *h, co
 int dn_debug_fail_next(dn_layer *layer, int code);
 
 /*
+ * dn_debug_expire_wait — device-side failure detection for tests: the next
+ * dn_step on this layer first launches one thread that waits for a flag
+ * nothing sets, gives up after `limit_us` microseconds (global timer) and
+ * records the give-up in the layer's device error word, as every bounded wait
+ * of the step's kernels does when it runs out (about one second).  The step
+ * itself then runs normally; the next dn_get_state finds the error word set,
+ * still copies the state out, returns DN_ECUDA and marks the layer failed,
+ * so later steps return DN_EFAILED.  No trap, fault or unbounded wait is
+ * involved.  limit_us in 1 .. 1000000; 0 cancels a pending request.
+ * Errors: DN_EINVAL.
+ */
+int dn_debug_expire_wait(dn_layer *layer, int limit_us);
+
+/*
  * dn_profile_next_step — instrumentation for benchmarks: the next dn_step on
  * this layer records, on its stream, events[0] before its first kernel,
  * events[1] after the in_proj (activation packing + projection),

@@ -66,6 +66,7 @@ def test_host_side_argument_checks_need_no_gpu(lib_path):
     assert lib.dn_step(None, 1, None, None, None, None, 1, None) == abi.DN_EINVAL
     assert lib.dn_get_state(None, 0, 1, None, None, None, 0) == abi.DN_EINVAL
     assert lib.dn_debug_fail_next(None, -5) == abi.DN_EINVAL
+    assert lib.dn_debug_expire_wait(None, 1000) == abi.DN_EINVAL
     assert lib.dn_profile_next_step(None, None) == abi.DN_EINVAL
     assert lib.dn_step_kernels(None, 1) == 0
     assert lib.dn_stack_step(None, 1, 1, None, None, None, 1e-6, None) == abi.DN_EINVAL

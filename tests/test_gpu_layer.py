@@ -131,6 +131,41 @@ def test_injected_failure_turns_layer_off_and_state_stays_readable():
         layer.destroy()
 
 
+def test_bounded_device_wait_that_runs_out_is_reported():
+    """Every wait of the step's kernels is bounded and records a give-up in
+    the layer's device error word.  Here one thread waits 2 ms for a flag
+    that nothing sets, ahead of a step: the step itself completes as usual
+    (its state equals a second layer's that ran the same steps), the next
+    get_state still copies the state out but returns DN_ECUDA, and the layer
+    is off from then on.  A cancelled request changes nothing."""
+    rng = np.random.default_rng(5)
+    w = make_weights(TINY, rng)
+    layer = GpuLayer.create(TINY, w, 2)
+    twin = GpuLayer.create(TINY, w, 2)
+    try:
+        s1 = WorkloadStream(custom_workload("t", TINY, 2, 8, seed=6))
+        s2 = WorkloadStream(custom_workload("t", TINY, 2, 8, seed=6))
+        abi.dn_debug_expire_wait(layer.handle, 2000)
+        abi.dn_debug_expire_wait(layer.handle, 0)  # cancelled
+        _run(layer, s1, 2, 2)
+        _run(twin, s2, 3, 2)
+        abi.dn_debug_expire_wait(layer.handle, 2000)
+        x, gates = s1.next_step()
+        xd, gd, bd, od = _dev_inputs(x, *gates[0])
+        assert abi.dn_step(layer.handle, 2, xd, gd, bd, od, check=False) == abi.DN_OK
+        S = np.empty((2, TINY.n_v_heads, TINY.dk, TINY.dv), np.float32)
+        ring = np.empty((2, TINY.conv_k - 1, TINY.conv_ch), np.float32)
+        rp = np.empty(2, np.int32)
+        assert abi.dn_get_state(layer.handle, 0, 2, S, ring, rp, check=False) == abi.DN_ECUDA
+        ref = twin.get_state()
+        assert np.array_equal(S, ref.S) and np.array_equal(ring, ref.ring)
+        assert np.array_equal(rp, ref.ring_pos)
+        assert abi.dn_step(layer.handle, 2, xd, gd, bd, od, check=False) == abi.DN_EFAILED
+    finally:
+        layer.destroy()
+        twin.destroy()
+
+
 def test_device_memory_accounting_returns_to_zero():
     base = abi.dn_device_bytes()
     w = make_weights(TINY, np.random.default_rng(4))
