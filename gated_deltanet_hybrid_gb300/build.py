@@ -33,8 +33,8 @@ def sources() -> list[str]:
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def _compile(src: str, extra: list[str]) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+def _compile(src: str, extra: list[str], build_dir: str) -> str:
+    obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
     cmd = [nvcc(), *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -42,22 +42,28 @@ def _compile(src: str, extra: list[str]) -> str:
     return obj
 
 
-def build(verbose: bool = False, extra: list[str] | None = None) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, extra: list[str] | None = None, lib: str | None = None,
+          build_dir: str | None = None) -> str:
+    """Compile every source and link the library.  `extra` flags go to every
+    compile and to the link (e.g. host sanitizers); `lib` / `build_dir`
+    place a variant build elsewhere (default: the package's libdn.so)."""
+    lib = lib or LIB
+    build_dir = build_dir or BUILD
+    os.makedirs(build_dir, exist_ok=True)
     extra = list(extra or [])
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), srcs))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, extra, build_dir), srcs))
+    tmp = lib + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-Xlinker", f"--version-script={os.path.join(CSRC, 'dn.map')}",
-           *objs, "-o", tmp]
+           *extra, *objs, "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     if verbose:
-        print(f"built {LIB}")
-    return LIB
+        print(f"built {lib}")
+    return lib
 
 
 if __name__ == "__main__":
