@@ -90,6 +90,19 @@ def test_tiny_tensor_core_batches(batch):
     _assert_ok(run_parity(wl, sample=sample))
 
 
+def test_35b_largest_accepted_batch():
+    """max_batch = 1024, the largest a layer accepts: 16 batch chunks in the
+    tensor-core projections, 216 items per CTA in the state kernel; three
+    sequences (first, middle, last) recomputed by the oracle."""
+    wl = custom_workload("35b_b1024", SHAPE_35B, batch=1024, steps=3, seed=1024, init_std=0.0)
+    _assert_ok(run_parity(wl, sample=np.array([0, 517, 1023])))
+
+
+def test_tiny_largest_accepted_batch():
+    wl = custom_workload("tiny_b1024", TINY, batch=1024, steps=6, seed=77, init_std=0.1)
+    _assert_ok(run_parity(wl, sample=np.array([0, 1, 500, 1022, 1023])))
+
+
 def test_35b_batch65_two_chunks():
     wl = custom_workload("35b_b65", SHAPE_35B, batch=65, steps=6, seed=65, init_std=0.02)
     _assert_ok(run_parity(wl, sample=np.array([0, 63, 64])))
