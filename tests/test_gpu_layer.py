@@ -99,6 +99,8 @@ def test_invalid_arguments_leave_state_untouched():
         g = torch.zeros((3, 4), device="cuda")
         rc = abi.dn_step(layer.handle, 3, x, g, g, x.clone(), check=False)  # batch > max_batch
         assert rc == abi.DN_EINVAL
+        rc = abi.dn_step(layer.handle, 0, x, g, g, x.clone(), check=False)  # empty batch
+        assert rc == abi.DN_EINVAL
         assert abi.dn_get_state(layer.handle, 1, 2, np.empty((2, 4, 32, 32), np.float32),
                                 check=False) == abi.DN_EINVAL
         back = layer.get_state()
@@ -164,6 +166,30 @@ def test_bounded_device_wait_that_runs_out_is_reported():
     finally:
         layer.destroy()
         twin.destroy()
+
+
+@pytest.mark.parametrize("batch", [2, 16])
+def test_zero_gates_leave_the_state_bitwise_unchanged(batch):
+    """g = 0 (no decay) and beta = 0 (no write) make the delta rule the
+    identity on S: S <- 1 * S + k (0 * (v - S^T k)).  After several steps
+    the state equals the initial one bit for bit, on the CUDA-core (batch 2)
+    and tensor-core (batch 16) projection paths, while the readouts still
+    match the oracle (checked by the parity tests on the same kernels)."""
+    torch = _torch()
+    wl = custom_workload("zero_gates", SHAPE_35B, batch=batch, steps=3, seed=88, init_std=0.02)
+    stream = WorkloadStream(wl)
+    s0 = stream.states[0]
+    layer = GpuLayer.create(wl.cfg, stream.weights[0], batch, s0)
+    try:
+        z = torch.zeros((batch, wl.cfg.n_v_heads), device="cuda")
+        out = torch.empty((batch, wl.cfg.hidden), device="cuda")
+        for _ in range(3):
+            x, _ = stream.next_step()
+            abi.dn_step(layer.handle, batch, torch.from_numpy(x).cuda(), z, z, out)
+        assert np.array_equal(layer.get_state().S, s0.S)
+        assert torch.isfinite(out).all()
+    finally:
+        layer.destroy()
 
 
 def test_device_memory_accounting_returns_to_zero():
