@@ -98,16 +98,21 @@ int cuda_fail(dn_layer *l) {
 
 namespace dn {
 int num_sms() {
-    static int cached_dev = -1, cached = 0;
+    // per device (ordinals below 64 cached), safe from several host threads
+    static std::atomic<int> cached[64];
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev != cached_dev) {
-        int n = 0;
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        cached = n > 0 ? n : 1;
-        cached_dev = dev;
+    if (dev >= 0 && dev < 64) {
+        const int c = cached[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
     }
-    return cached;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();  // no device: the caller's next CUDA call reports it; nothing is cached
+        return 1;
+    }
+    if (dev >= 0 && dev < 64) cached[dev].store(n, std::memory_order_relaxed);
+    return n;
 }
 }  // namespace dn
 

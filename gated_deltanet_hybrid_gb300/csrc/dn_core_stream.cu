@@ -443,16 +443,13 @@ __global__ void __launch_bounds__(NT, 1) dn_core_stream_kernel(const StreamParam
 
 template <int KC>
 cudaError_t launch_kc(const StreamParams &p, cudaStream_t st) {
-    static int attr_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
+    static std::atomic<uint64_t> attr_done{0};
     const size_t smem = sizeof(StreamSmem) + 128;
-    if (attr_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(dn_core_stream_kernel<KC>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        attr_dev = dev;
-    }
+    const cudaError_t e = once_per_device(attr_done, [&](int) {
+        return cudaFuncSetAttribute(dn_core_stream_kernel<KC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)smem);
+    });
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)std::min(num_sms(), p.items));
     cfg.blockDim = dim3(NT);

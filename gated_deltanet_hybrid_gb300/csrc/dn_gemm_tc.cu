@@ -664,16 +664,12 @@ cudaError_t launch_pack_b(const float *x, uint8_t *xb, int B, int K, cudaStream_
 
 cudaError_t launch_gemm_i8_tc(const uint8_t *Wt, const uint8_t *xb, float *part, int *nseg, int *err,
                               int M, int K, int B, cudaStream_t st) {
-    static int attr_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
+    static std::atomic<uint64_t> attr_done{0};
     const size_t smem = tc_gemm_smem_bytes();
-    if (attr_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_i8_tc_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        attr_dev = dev;
-    }
+    const cudaError_t e = once_per_device(attr_done, [&](int) {
+        return cudaFuncSetAttribute(gemm_i8_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    });
+    if (e != cudaSuccess) return e;
     const GemmPlan g = plan_tc_gemm(M, K, B);
     GemmParams p;
     p.Wt = Wt;

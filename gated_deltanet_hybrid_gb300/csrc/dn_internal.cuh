@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/dn.h"
 
 namespace dn {
@@ -142,6 +144,22 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+// Runs `set(device)` the first time a function is launched on each device
+// (ordinals below 64; beyond that, every time): for per-function attributes
+// such as a large dynamic shared-memory size.  Safe when several host
+// threads launch on several devices.
+template <typename Set>
+cudaError_t once_per_device(std::atomic<uint64_t> &done, Set set) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? (uint64_t{1} << dev) : 0;
+    if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+    e = set(dev);
+    if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
+
 struct PdlAttr {
     cudaLaunchAttribute a[1];
     void apply(cudaLaunchConfig_t &cfg) {
