@@ -24,6 +24,9 @@
  *     call on the same layer.
  *   - Arrays are dense, row-major (last index fastest), fp32 unless stated.
  *   - The library keeps no pointer to caller memory after a call returns.
+ *   - Threads: calls on one layer must not overlap (a layer holds one step's
+ *     scratch); different layers may be driven from different host threads
+ *     and devices at the same time.
  */
 #ifndef DN_H
 #define DN_H
