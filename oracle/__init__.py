@@ -12,6 +12,7 @@ from .dn_oracle import (  # noqa: F401
     gated_rmsnorm,
     int8_rowscaled_gemv,
     l2_normalize,
+    normalize_qk,
     rms_prenorm,
     silu,
     stack_step,

@@ -86,6 +86,12 @@ def l2_normalize(x: np.ndarray, eps: float) -> np.ndarray:
     return x / np.sqrt(np.sum(x * x) + eps)
 
 
+def normalize_qk(q: np.ndarray, k: np.ndarray, l2_eps: float, q_scale: float) -> tuple[np.ndarray, np.ndarray]:
+    """The per-head L2 norms of q and k (eps inside the root, double), then
+    the query scale on the normalised q only: returns (q_scale * q / |q|, k / |k|)."""
+    return l2_normalize(q, l2_eps) * F64(q_scale), l2_normalize(k, l2_eps)
+
+
 def gated_delta_rule_step(S: np.ndarray, q: np.ndarray, k: np.ndarray, v: np.ndarray,
                           g: float, beta: float) -> tuple[np.ndarray, np.ndarray]:
     """One token of the gated delta rule for one value head, in the page's order.
@@ -152,8 +158,7 @@ class OracleLayer:
             v_all = u[2 * qk:].reshape(c.n_v_heads, c.dv)
             for h in range(c.n_v_heads):
                 hq = h // group
-                qh = l2_normalize(q_all[hq], c.l2_eps) * c.qscale
-                kh = l2_normalize(k_all[hq], c.l2_eps)
+                qh, kh = normalize_qk(q_all[hq], k_all[hq], c.l2_eps, c.qscale)
                 self.S[b, h], o = gated_delta_rule_step(self.S[b, h], qh, kh, v_all[h],
                                                         g[b, h], beta[b, h])
                 o_all[b, h] = o

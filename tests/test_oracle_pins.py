@@ -10,7 +10,8 @@ import numpy as np
 import pytest
 from scipy.special import expit
 
-from gated_deltanet_hybrid_gb300.inputs import DNConfig, DNState, make_weights, zero_state
+import oracle.dn_oracle as dn_oracle
+from gated_deltanet_hybrid_gb300.inputs import DNConfig, DNState, DNWeights, make_weights, zero_state
 from oracle import (
     OracleLayer,
     causal_conv_silu_step,
@@ -232,6 +233,106 @@ def test_gated_rmsnorm_invariants():
     # constant head: every entry normalises to sign(o) (times w * silu(z))
     c = gated_rmsnorm(np.full(4, -2.0), np.full(4, 60.0), np.ones(4), 0.0)
     assert np.allclose(c, -60.0, rtol=1e-14)
+
+
+def _golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *nums = line.split()
+            vals[key] = np.array([float(v) for v in nums])
+    return vals
+
+
+def _rmsnorm_golden_ok() -> bool:
+    """The hand-worked head of tests/golden/handworked_gated_rmsnorm.txt:
+    non-uniform weight, z where silu(z) differs from z and from sigmoid(z),
+    and an eps whose place (inside or outside the root) changes the result."""
+    gv = _golden("handworked_gated_rmsnorm.txt")
+    y = dn_oracle.gated_rmsnorm(gv["o"], gv["z"], gv["w"], float(gv["eps"][0]))
+    return bool(np.allclose(y, gv["y"], rtol=1e-14, atol=1e-15))
+
+
+def test_gated_rmsnorm_handworked():
+    assert _rmsnorm_golden_ok()
+
+
+def _hand_layer():
+    """The one-head layer of tests/golden/handworked_layer_step.txt, one step."""
+    gv = _golden("handworked_layer_step.txt")
+    cfg = DNConfig(hidden=8, n_qk_heads=1, n_v_heads=1, dk=2, dv=2, conv_k=2,
+                   l2_eps=float(gv["l2_eps"][0]), norm_eps=float(gv["norm_eps"][0]),
+                   q_scale=float(gv["q_scale"][0]))
+    w_out = np.zeros((8, 2), np.int8)
+    w_out[0, 0] = w_out[1, 1] = 1
+    w = DNWeights(w_in=np.eye(8, dtype=np.int8), s_in=np.ones(8, np.float32),
+                  w_conv=np.tile(np.array([0.0, 1.0], np.float32), (cfg.conv_ch, 1)),
+                  w_norm=gv["w_norm"].astype(np.float32), w_out=w_out, s_out=np.ones(8, np.float32))
+    st = DNState(S=gv["S0"].reshape(1, 1, 2, 2), ring=np.zeros((1, 1, cfg.conv_ch)),
+                 ring_pos=np.zeros(1, np.int32))
+    layer = OracleLayer(cfg, w, st)
+    tr = {}
+    out = layer.step(gv["x"].reshape(1, 8), np.array([[math.log(gv["decay"][0])]]),
+                     np.array([[gv["beta"][0]]]), trace=tr)
+    return out, layer, tr, gv
+
+
+def _layer_golden_ok() -> bool:
+    out, layer, tr, gv = _hand_layer()
+    return bool(np.allclose(layer.S[0, 0].reshape(-1), gv["S"], rtol=0, atol=1e-14)
+                and np.allclose(tr["o"][0, 0], gv["o"], rtol=0, atol=1e-14)
+                and np.allclose(out[0], gv["out"], rtol=0, atol=1e-14))
+
+
+def test_layer_step_handworked():
+    """A whole step of a one-head layer worked by hand: the readout uses
+    q_scale times the normalised q, the gated RMSNorm (norm_eps = 1, large
+    enough that the scale of o shows) and the out_proj."""
+    assert _layer_golden_ok()
+    _, layer, _, gv = _hand_layer()
+    assert layer.ring_pos[0] == 0  # one slot: the position stays 0
+    assert np.array_equal(layer.ring[0, 0], gv["x"][:6])
+
+
+# Planted mistakes: each is a plausible error in the oracle; the pins above
+# must catch every one of them (the mutation is undone after each case).
+def _silu(z):
+    return z / (1.0 + np.exp(-z))
+
+
+RMSNORM_MUTANTS = {
+    "weight dropped": lambda o, z, w, eps: o / np.sqrt(np.mean(o * o) + eps) * _silu(z),
+    "gated by z": lambda o, z, w, eps: o / np.sqrt(np.mean(o * o) + eps) * w * z,
+    "gated by sigmoid(z)": lambda o, z, w, eps: o / np.sqrt(np.mean(o * o) + eps) * w / (1 + np.exp(-z)),
+    "eps outside the root": lambda o, z, w, eps: o / (np.sqrt(np.mean(o * o)) + eps) * w * _silu(z),
+    "sum for mean": lambda o, z, w, eps: o / np.sqrt(np.sum(o * o) + eps) * w * _silu(z),
+}
+
+
+@pytest.mark.parametrize("name", sorted(RMSNORM_MUTANTS))
+def test_pins_catch_rmsnorm_mutant(name, monkeypatch):
+    monkeypatch.setattr(dn_oracle, "gated_rmsnorm",
+                        lambda o, z, w, eps: RMSNORM_MUTANTS[name](np.asarray(o, np.float64),
+                                                                   np.asarray(z, np.float64),
+                                                                   np.asarray(w, np.float64), eps))
+    assert not (_rmsnorm_golden_ok() and _layer_golden_ok())
+
+
+QSCALE_MUTANTS = {
+    "q_scale on k": lambda q, k, e, s: (dn_oracle.l2_normalize(q, e), dn_oracle.l2_normalize(k, e) * s),
+    "q_scale before the norm": lambda q, k, e, s: (dn_oracle.l2_normalize(q * s, e), dn_oracle.l2_normalize(k, e)),
+    "q_scale dropped": lambda q, k, e, s: (dn_oracle.l2_normalize(q, e), dn_oracle.l2_normalize(k, e)),
+    "q and k swapped": lambda q, k, e, s: (dn_oracle.l2_normalize(k, e) * s, dn_oracle.l2_normalize(q, e)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(QSCALE_MUTANTS))
+def test_pins_catch_qscale_mutant(name, monkeypatch):
+    monkeypatch.setattr(dn_oracle, "normalize_qk", QSCALE_MUTANTS[name])
+    assert not _layer_golden_ok()
 
 
 # ---------------------------------------------------------------- whole step
