@@ -227,7 +227,67 @@ def make_inputs(cfg: DNConfig, B: int, n: int, seed: int):
     return sets
 
 
-def bench_gpu(cfg, B, init_std, steps, warmup, n_layers, seed, use_graph, dist_ctx, torch, abi):
+def capture_steps(n_layers, step, torch):
+    """One CUDA graph per layer object, each holding one dn_step (so a timed
+    region of any length is made of whole graph replays); None if capture
+    is not possible."""
+    stream = torch.cuda.current_stream()
+    graphs = []
+    try:
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            for i in range(n_layers):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=cap):
+                    step(i)
+                graphs.append(g)
+        torch.cuda.synchronize()
+    except Exception as e:  # capture not possible: time eager launches
+        print(f"[bench] graph capture failed ({e}); timing eager launches", file=sys.stderr)
+        return None
+    return graphs
+
+
+def timed_regions(run_region, steps, dist_ctx, torch, min_repeats=5, min_total_s=0.5, max_repeats=2000):
+    """Times the region (exactly `steps` steps) with CUDA events on the
+    launching stream, a barrier and a synchronize on both sides, the max over
+    ranks; repeats it until it has run at least min_repeats times and for at
+    least min_total_s in total.  Returns (per-repeat ms list, wall start, wall
+    end).  Every rank takes the same decision (it uses the max over ranks)."""
+    stream = torch.cuda.current_stream()
+    ms_list = []
+    t_first = None
+    total = 0.0
+    while True:
+        dist_ctx.barrier()
+        torch.cuda.synchronize()
+        t0 = time.time()
+        if t_first is None:
+            t_first = t0
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        run_region()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        dist_ctx.barrier()
+        ms = dist_ctx.max(ev0.elapsed_time(ev1))
+        ms_list.append(ms)
+        total += ms / 1e3
+        if (len(ms_list) >= min_repeats and total >= min_total_s) or len(ms_list) >= max_repeats:
+            break
+    return ms_list, t_first, time.time()
+
+
+def region_stats(ms_list, steps):
+    med = statistics.median(ms_list)
+    return {"repeats": len(ms_list), "steps_per_repeat": steps,
+            "ms_per_step_median": med / steps, "ms_per_step_min": min(ms_list) / steps,
+            "ms_per_step_max": max(ms_list) / steps}
+
+
+def bench_gpu(cfg, B, init_std, steps, warmup, n_layers, seed, use_graph, dist_ctx, torch, abi,
+              profile=True, e2e=True):
     dev = torch.device("cuda")
     layers = setup_layers(cfg, B, n_layers, init_std, seed, torch, abi)
     host_inputs = make_inputs(cfg, B, n_layers, seed + 7)
@@ -244,133 +304,162 @@ def bench_gpu(cfg, B, init_std, steps, warmup, n_layers, seed, use_graph, dist_c
     for i in range(warmup):
         step(i)
     torch.cuda.synchronize()
-
-    graph = None
-    if use_graph:
-        try:
-            graph = torch.cuda.CUDAGraph()
-            cap = torch.cuda.Stream()
-            cap.wait_stream(stream)
-            with torch.cuda.stream(cap):
-                with torch.cuda.graph(graph, stream=cap):
-                    for i in range(n_layers):
-                        step(i)
-            torch.cuda.synchronize()
-        except Exception as e:  # capture not possible: time eager launches
-            print(f"[bench] graph capture failed ({e}); timing eager launches", file=sys.stderr)
-            graph = None
+    graphs = capture_steps(n_layers, step, torch) if use_graph else None
     launches_per_step = abi.dn_step_kernels(layers[0], B)
 
-    # ---- timed region ----
+    # ---- timed region: exactly `steps` steps, rotating over the layers ----
     def run_region():
-        if graph is not None:
-            reps, rem = divmod(steps, n_layers)
-            for _ in range(reps):
-                graph.replay()
-            for i in range(rem):
-                step(i)
+        if graphs is not None:
+            for i in range(steps):
+                graphs[i % n_layers].replay()
         else:
             for i in range(steps):
                 step(i)
 
-    dist_ctx.barrier()
-    torch.cuda.synchronize()
-    t0 = time.time()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    run_region()
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    dist_ctx.barrier()
-    t1 = time.time()
-    ms = ev0.elapsed_time(ev1)
-    ms = dist_ctx.max(ms)
+    ms_list, t0, t1 = timed_regions(run_region, steps, dist_ctx, torch)
+    out = {"ms": statistics.median(ms_list), "region": region_stats(ms_list, steps), "t_wall": (t0, t1),
+           "graph": graphs is not None, "launches": steps * launches_per_step * len(ms_list),
+           "launches_per_region": steps * launches_per_step}
 
     # ---- per-kernel device times (CUDA events between the kernels) ----
-    n_prof = min(steps, 2048)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_prof)]
-    for es in evs:  # torch creates the CUDA event on first record
-        for e in es:
-            e.record(stream)
-    torch.cuda.synchronize()
-    if hasattr(torch.cuda, "_sleep"):
-        torch.cuda._sleep(200_000_000)  # ~0.1 s: the CPU queues the steps meanwhile
-    for i in range(n_prof):
-        l = i % n_layers
-        abi.dn_profile_next_step(layers[l], evs[i])
-        x, g, b = d_in[l]
-        abi.dn_step(layers[l], B, x, g, b, d_out[l])
-    torch.cuda.synchronize()
-    per_kernel = {k: 0.0 for k in KERNELS}
-    for e in evs:
-        for k in KERNELS:
-            a, z = STAGE_EVENTS[k]
-            per_kernel[k] += e[a].elapsed_time(e[z])
-    per_kernel = {k: v / n_prof for k, v in per_kernel.items()}
+    if profile:
+        n_prof = min(steps, 2048)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_prof)]
+        for es in evs:  # torch creates the CUDA event on first record
+            for e in es:
+                e.record(stream)
+        torch.cuda.synchronize()
+        if hasattr(torch.cuda, "_sleep"):
+            torch.cuda._sleep(200_000_000)  # ~0.1 s: the CPU queues the steps meanwhile
+        for i in range(n_prof):
+            l = i % n_layers
+            abi.dn_profile_next_step(layers[l], evs[i])
+            x, g, b = d_in[l]
+            abi.dn_step(layers[l], B, x, g, b, d_out[l])
+        torch.cuda.synchronize()
+        per_kernel = {k: 0.0 for k in KERNELS}
+        for e in evs:
+            for k in KERNELS:
+                a, z = STAGE_EVENTS[k]
+                per_kernel[k] += e[a].elapsed_time(e[z])
+        out["per_kernel_ms"] = {k: v / n_prof for k, v in per_kernel.items()}
 
     # ---- end to end through the ABI with host buffers ----
-    n_e2e = min(steps, 2000)
-    hx = [torch.from_numpy(x).pin_memory() for x, _, _ in host_inputs]
-    hg = [torch.from_numpy(g).pin_memory() for _, g, _ in host_inputs]
-    hb = [torch.from_numpy(b).pin_memory() for _, _, b in host_inputs]
-    ho = [torch.empty((B, cfg.hidden), dtype=torch.float32).pin_memory() for _ in range(n_layers)]
-    for i in range(min(warmup, 8)):
-        l = i % n_layers
-        abi.dn_step(layers[l], B, hx[l], hg[l], hb[l], ho[l], stream=stream.cuda_stream)
-    dist_ctx.barrier()
-    torch.cuda.synchronize()
-    te0 = time.perf_counter()
-    for i in range(n_e2e):
-        l = i % n_layers
-        abi.dn_step(layers[l], B, hx[l], hg[l], hb[l], ho[l], stream=stream.cuda_stream)
-    torch.cuda.synchronize()
-    e2e_s = dist_ctx.max(time.perf_counter() - te0)
-    dist_ctx.barrier()
+    if e2e:
+        n_e2e = min(steps, 2000)
+        hx = [torch.from_numpy(x).pin_memory() for x, _, _ in host_inputs]
+        hg = [torch.from_numpy(g).pin_memory() for _, g, _ in host_inputs]
+        hb = [torch.from_numpy(b).pin_memory() for _, _, b in host_inputs]
+        ho = [torch.empty((B, cfg.hidden), dtype=torch.float32).pin_memory() for _ in range(n_layers)]
+        for i in range(min(warmup, 8)):
+            l = i % n_layers
+            abi.dn_step(layers[l], B, hx[l], hg[l], hb[l], ho[l], stream=stream.cuda_stream)
+        dist_ctx.barrier()
+        torch.cuda.synchronize()
+        te0 = time.perf_counter()
+        for i in range(n_e2e):
+            l = i % n_layers
+            abi.dn_step(layers[l], B, hx[l], hg[l], hb[l], ho[l], stream=stream.cuda_stream)
+        torch.cuda.synchronize()
+        out["e2e_s"] = dist_ctx.max(time.perf_counter() - te0)
+        out["n_e2e"] = n_e2e
+        out["h2d_bytes"] = B * (cfg.hidden + 2 * cfg.n_v_heads) * 4
+        out["d2h_bytes"] = B * cfg.hidden * 4
+        dist_ctx.barrier()
 
+    del graphs
     for h in layers:
         abi.dn_destroy(h)
-    return {"ms": ms, "t_wall": (t0, t1), "per_kernel_ms": per_kernel, "graph": graph is not None,
-            "launches": steps * launches_per_step, "e2e_s": e2e_s, "n_e2e": n_e2e,
-            "h2d_bytes": B * (cfg.hidden + 2 * cfg.n_v_heads) * 4, "d2h_bytes": B * cfg.hidden * 4}
+    return out
 
 
 # --------------------------------------------------------------------- CPU oracle
-def oracle_rate(cfg: DNConfig, B: int, init_std: float, budget_s: float, n_seq: int = 1):
-    """The oracle as it stands on a bounded sample: n_seq sequences of the
-    workload stepped until budget_s has passed.  Returns (sequence-steps/s,
-    steps done, threads)."""
-    from oracle import OracleLayer
-    from gated_deltanet_hybrid_gb300.inputs import random_state, zero_state
-
-    rng = np.random.Generator(np.random.PCG64(99))
-    w = make_weights(cfg, rng)
-    st = random_state(cfg, n_seq, rng, init_std) if init_std > 0 else zero_state(cfg, n_seq)
-    layer = OracleLayer(cfg, w, st)
-    inputs = make_inputs(cfg, n_seq, 4, 123)
-    layer.step(*inputs[0])  # warm
-    t0 = time.perf_counter()
-    n = 0
-    while True:
-        layer.step(*inputs[n % 4])
-        n += 1
-        if time.perf_counter() - t0 >= budget_s:
-            break
-    dt = time.perf_counter() - t0
-    return n * n_seq / dt, n, blas_threads()
+BLAS_ENV = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS")
 
 
-def blas_threads() -> int:
+def host_cores() -> int:
     try:
-        from threadpoolctl import threadpool_info
-        info = [i for i in threadpool_info() if i.get("user_api") == "blas"]
-        if info:
-            return int(max(i.get("num_threads", 1) for i in info))
-    except Exception:
-        pass
-    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
-        if os.environ.get(var, "").isdigit():
-            return int(os.environ[var])
-    return os.cpu_count() or 1
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def _oracle_worker(q, barrier, cfg, n_seq, init_std, seconds, steps, warmup):
+    """One spawned process of the CPU oracle: n_seq independent sequences of
+    the workload's layer (float64 oracle, one BLAS thread), stepped either
+    exactly `steps` times or until `seconds` have passed, timed from a barrier
+    that every worker passes together.  Puts (sequence-steps, seconds)."""
+    try:
+        from oracle import OracleLayer
+        from gated_deltanet_hybrid_gb300.inputs import random_state, zero_state
+        rng = np.random.Generator(np.random.PCG64(99))
+        w = make_weights(cfg, rng)
+        st = random_state(cfg, n_seq, rng, init_std) if init_std > 0 else zero_state(cfg, n_seq)
+        layer = OracleLayer(cfg, w, st)
+        inputs = make_inputs(cfg, n_seq, 4, 123)
+        for i in range(warmup):
+            layer.step(*inputs[i % 4])
+        barrier.wait()
+        t0 = time.perf_counter()
+        n = 0
+        while (n < steps) if steps else (time.perf_counter() - t0 < seconds):
+            layer.step(*inputs[n % 4])
+            n += 1
+        q.put((n * n_seq, time.perf_counter() - t0))
+    except Exception as e:  # reported by the parent
+        barrier.abort()
+        q.put(("error", repr(e)))
+
+
+def run_oracle_pool(cfg, B, init_std, workers, seconds=None, steps=None, warmup=1):
+    """The float64 oracle on the host cores: the B sequences of one
+    layer-step split over `workers` spawned processes (one BLAS thread each),
+    all started together.  Returns (sequence-steps, seconds of the slowest
+    worker, workers used)."""
+    import multiprocessing as mp
+    workers = max(1, min(workers, B))
+    shares = [B // workers + (1 if i < B % workers else 0) for i in range(workers)]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    barrier = ctx.Barrier(workers)
+    saved = {v: os.environ.get(v) for v in BLAS_ENV}
+    procs = []
+    try:
+        for v in BLAS_ENV:
+            os.environ[v] = "1"
+        for n_seq in shares:
+            pr = ctx.Process(target=_oracle_worker,
+                             args=(q, barrier, cfg, n_seq, init_std, seconds, steps, warmup))
+            pr.start()
+            procs.append(pr)
+    finally:
+        for v, old in saved.items():
+            if old is None:
+                os.environ.pop(v, None)
+            else:
+                os.environ[v] = old
+    res = [q.get() for _ in procs]
+    for pr in procs:
+        pr.join()
+    errs = [r[1] for r in res if r[0] == "error"]
+    if errs:
+        raise RuntimeError(f"oracle worker failed: {errs[0]}")
+    return sum(r[0] for r in res), max(r[1] for r in res), workers
+
+
+def cpu_baseline(cfg, B, init_std, seconds, workload):
+    """The oracle as it stands on a bounded sample of the workload: every
+    host core steps its share of the batch's sequences (two thirds of the
+    budget), then one core steps min(B, 4) sequences (one third)."""
+    cores = host_cores()
+    n_all, t_all, used = run_oracle_pool(cfg, B, init_std, cores, seconds=2 * seconds / 3)
+    n1, t1, _ = run_oracle_pool(cfg, min(B, 4), init_std, 1, seconds=seconds / 3)
+    return {"value": n_all / t_all / B, "unit": UNIT, "cores": used, "kind": "oracle",
+            "value_1core": n1 / t1 / B,
+            "sample": f"{n_all} sequence-steps of the {workload} layer's {B} sequences spread over "
+                      f"{used} host processes (one BLAS thread each, {t_all:.1f} s), and {n1} "
+                      f"sequence-steps on one core ({t1:.1f} s); float64 numpy oracle, scaled to "
+                      f"layer-steps of batch {B}"}
 
 
 # --------------------------------------------------------------------- distributed
@@ -422,106 +511,113 @@ STACK_SPECS = {
 }
 
 
-def bench_stack(cfg, B, n_layers, steps, warmup, seed, use_graph, dist_ctx, torch, abi):
-    """Tokens through a stack of n_layers layer objects: each timed token
-    starts the residual stream from a fresh input row set (as a new token's
-    embedding would) and runs dn_stack_step over every layer."""
+def bench_stack(cfg, batches, n_layers, steps, warmup, seed, use_graph, dist_ctx, torch, abi):
+    """Tokens through a stack of n_layers layer objects (held once, for the
+    largest batch): for each batch size, `warmup` tokens (the prompt, token
+    by token), then timed regions of `steps` tokens, each token starting the
+    residual stream from the same fresh input rows (as a new token's
+    embedding would) and running dn_stack_step over every layer."""
     dev = torch.device("cuda")
-    layers = setup_layers(cfg, B, n_layers, 0.0, seed, torch, abi)
-    rng = np.random.Generator(np.random.PCG64(seed + 7))
-    h0 = torch.from_numpy(rng.standard_normal((B, cfg.hidden)).astype(np.float32)).to(dev)
-    gb = [gates_from_ab(rng.standard_normal((B, cfg.n_v_heads)), rng.standard_normal((B, cfg.n_v_heads)))
-          for _ in range(n_layers)]
-    g = torch.from_numpy(np.stack([x[0] for x in gb]).astype(np.float32)).to(dev)
-    beta = torch.from_numpy(np.stack([x[1] for x in gb]).astype(np.float32)).to(dev)
-    h = torch.empty_like(h0)
+    Bmax = max(batches)
+    layers = setup_layers(cfg, Bmax, n_layers, 0.0, seed, torch, abi)
     stream = torch.cuda.current_stream()
+    res = {}
+    for B in batches:
+        rng = np.random.Generator(np.random.PCG64(seed + 7 + B))
+        h0 = torch.from_numpy(rng.standard_normal((B, cfg.hidden)).astype(np.float32)).to(dev)
+        gb = [gates_from_ab(rng.standard_normal((B, cfg.n_v_heads)), rng.standard_normal((B, cfg.n_v_heads)))
+              for _ in range(n_layers)]
+        g = torch.from_numpy(np.stack([x[0] for x in gb]).astype(np.float32)).to(dev)
+        beta = torch.from_numpy(np.stack([x[1] for x in gb]).astype(np.float32)).to(dev)
+        h = torch.empty_like(h0)
 
-    def token():
-        h.copy_(h0)
-        abi.dn_stack_step(layers, B, h, g, beta)
+        def token():
+            h.copy_(h0)
+            abi.dn_stack_step(layers, B, h, g, beta)
 
-    for _ in range(warmup):
-        token()
-    torch.cuda.synchronize()
-    graph = None
-    if use_graph:
-        try:
-            graph = torch.cuda.CUDAGraph()
-            cap = torch.cuda.Stream()
-            cap.wait_stream(stream)
-            with torch.cuda.stream(cap):
-                with torch.cuda.graph(graph, stream=cap):
-                    token()
-            torch.cuda.synchronize()
-        except Exception as e:  # capture not possible: time eager launches
-            print(f"[bench] graph capture failed ({e}); timing eager launches", file=sys.stderr)
-            graph = None
-    dist_ctx.barrier()
-    torch.cuda.synchronize()
-    t0 = time.time()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(steps):
-        if graph is not None:
-            graph.replay()
-        else:
+        for _ in range(warmup):
             token()
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    dist_ctx.barrier()
-    t1 = time.time()
-    ms = dist_ctx.max(ev0.elapsed_time(ev1))
-    launches = steps * (n_layers * abi.dn_step_kernels(layers[0], B) + n_layers + 1)
-    del graph
+        torch.cuda.synchronize()
+        graph = None
+        if use_graph:
+            try:
+                graph = torch.cuda.CUDAGraph()
+                cap = torch.cuda.Stream()
+                cap.wait_stream(stream)
+                with torch.cuda.stream(cap):
+                    with torch.cuda.graph(graph, stream=cap):
+                        token()
+                torch.cuda.synchronize()
+            except Exception as e:  # capture not possible: time eager launches
+                print(f"[bench] graph capture failed ({e}); timing eager launches", file=sys.stderr)
+                graph = None
+
+        def run_region():
+            for _ in range(steps):
+                if graph is not None:
+                    graph.replay()
+                else:
+                    token()
+
+        ms_list, t0, t1 = timed_regions(run_region, steps, dist_ctx, torch, min_repeats=3, min_total_s=0.2)
+        per_token = steps * (n_layers * abi.dn_step_kernels(layers[0], B) + n_layers + 1)
+        res[B] = {"ms": statistics.median(ms_list), "region": region_stats(ms_list, steps),
+                  "t_wall": (t0, t1), "graph": graph is not None, "launches": per_token * len(ms_list)}
+        del graph
     for l in layers:
         abi.dn_destroy(l)
-    return {"ms": ms, "t_wall": (t0, t1), "graph": use_graph, "launches": launches}
+    return res
+
+
+def stack_summary(cfg, B, n_layers, steps, r, n, hbm_peak):
+    s = r["ms"] / 1e3
+    ms_layer = r["ms"] / (steps * n_layers)
+    sb = step_bytes(cfg, B)
+    return {"value": n * steps * n_layers / s, "unit": UNIT, "tokens_per_s": n * steps * B / s,
+            "ms_per_token": r["ms"] / steps, "ms_per_step": ms_layer, "batch": B, "layers": n_layers,
+            "hbm_gbs_step": sb / (ms_layer / 1e3) / 1e9,
+            "step_roofline_frac": sb / (ms_layer / 1e3) / 1e9 / hbm_peak,
+            "region": r["region"], "launch": "cuda graph of one token" if r["graph"] else "eager"}
 
 
 def run_stack(args, torch, dist_ctx):
     from gated_deltanet_hybrid_gb300 import abi
     abi.load_library()
     hbm_peak, peak_kind = load_peaks()
-    uuid = None
-    try:
-        uuid = "GPU-" + str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
-    except Exception:
-        pass
     cfg, B, n_layers = STACK_SPECS[args.workload]
-    with ClockSampler(uuid) as clk:
-        r = bench_stack(cfg, B, n_layers, args.steps, args.warmup, 3, args.graph, dist_ctx, torch, abi)
+    with ClockSampler(gpu_uuid(torch)) as clk:
+        r = bench_stack(cfg, [B], n_layers, args.steps, args.warmup, 3, args.graph, dist_ctx, torch, abi)[B]
     n = dist_ctx.world
-    s = r["ms"] / 1e3
-    ms_layer = r["ms"] / (args.steps * n_layers)
-    sb = step_bytes(cfg, B)
-    return {
-        "metric": METRIC, "value": n * args.steps * n_layers / s, "unit": UNIT, "n_gpus": n,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_layer, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32 (int8 weights)",
+    summ = stack_summary(cfg, B, n_layers, args.steps, r, n, hbm_peak)
+    line = {
+        "metric": METRIC, "value": summ["value"], "unit": UNIT, "n_gpus": n,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": summ["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32 (int8 weights)",
         "data": "synthetic (seeded random weights and inputs of the 35B-shape layer, zero initial state)",
         "config": {"workload": args.workload, "layers": n_layers, "batch": B, "hidden": cfg.hidden,
                    "l2": f"inputs larger than L2: {n_layers} distinct layers per token",
-                   "launch": "cuda graph of one token" if r["graph"] else "eager",
+                   "launch": summ["launch"],
                    "parallelism": f"replicas x{n}" if n > 1 else "single GPU"},
-        "tokens_per_s": n * args.steps * B / s, "ms_per_token": r["ms"] / args.steps,
-        "hbm_gbs_step": sb / (ms_layer / 1e3) / 1e9,
-        "step_roofline_frac": sb / (ms_layer / 1e3) / 1e9 / hbm_peak, "peak_kind": peak_kind,
-        "clocks": clk.summary(*r["t_wall"]), "gpu_launches": r["launches"] * n,
+        "clocks": clk.summary(*r["t_wall"]), "gpu_launches": r["launches"] * n, "peak_kind": peak_kind,
     }
+    line.update({k: summ[k] for k in ("tokens_per_s", "ms_per_token", "hbm_gbs_step", "step_roofline_frac",
+                                      "region")})
+    return line
+
+
+def gpu_uuid(torch):
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+    except Exception:
+        return None
 
 
 def run_ours(args, torch, dist_ctx):
     from gated_deltanet_hybrid_gb300 import abi
     abi.load_library()
     hbm_peak, peak_kind = load_peaks()
-    uuid = None
-    try:
-        uuid = "GPU-" + str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
-    except Exception:
-        pass
     cfg, B, init_std = WORKLOAD_SPECS[args.workload]
-    with ClockSampler(uuid) as clk:
+    with ClockSampler(gpu_uuid(torch)) as clk:
         r = bench_gpu(cfg, B, init_std, args.steps, args.warmup, args.layers, 2, args.graph,
                       dist_ctx, torch, abi)
     clocks = clk.summary(*r["t_wall"])
@@ -545,6 +641,7 @@ def run_ours(args, torch, dist_ctx):
                          f"{sb / 1e6:.1f} MB per layer-step",
                    "launch": "cuda graph of one step per layer" if r["graph"] else "eager",
                    "parallelism": f"replicas x{n}" if n > 1 else "single GPU"},
+        "region": r["region"],
         "hbm_gbs_step": sb / (ms_per_step / 1e3) / 1e9,
         "step_roofline_frac": sb / (ms_per_step / 1e3) / 1e9 / hbm_peak,
         "per_kernel_us": {k: v * 1e3 for k, v in r["per_kernel_ms"].items()},
@@ -559,60 +656,59 @@ def run_ours(args, torch, dist_ctx):
                 "h2d_bytes_per_step": r["h2d_bytes"], "d2h_bytes_per_step": r["d2h_bytes"],
                 "steps": r["n_e2e"], "api": "dn_step with pinned host pointers (copies + sync inside)"},
     }
-    if args.secondary and args.workload != "35b_b1":
-        cfg1, B1, std1 = WORKLOAD_SPECS["35b_b1"]
-        r1 = bench_gpu(cfg1, B1, std1, max(args.steps, 2000), args.warmup, args.layers, 1, True,
-                       dist_ctx, torch, abi)
-        ms1 = r1["ms"] / max(args.steps, 2000)
-        sb1 = step_bytes(cfg1, B1)
-        line["batch1"] = {"value": n / (ms1 / 1e3), "unit": UNIT, "ms_per_step": ms1,
-                          "hbm_gbs_step": sb1 / (ms1 / 1e3) / 1e9,
-                          "step_roofline_frac": sb1 / (ms1 / 1e3) / 1e9 / hbm_peak,
-                          "per_kernel_us": {k: v * 1e3 for k, v in r1["per_kernel_ms"].items()},
-                          "launch": "cuda graph" if r1["graph"] else "eager",
-                          "e2e_value": n * r1["n_e2e"] / r1["e2e_s"]}
-        line["gpu_launches"] += r1["launches"] * n
+    if args.secondary and args.workload == "35b_b64":
+        for key, wl in (("batch1", "35b_b1"), ("batch8", "35b_b8")):
+            c2, B2, std2 = WORKLOAD_SPECS[wl]
+            st2 = max(args.steps, 2000)
+            r2 = bench_gpu(c2, B2, std2, st2, args.warmup, args.layers, 1, True, dist_ctx, torch, abi,
+                           profile=key == "batch1", e2e=key == "batch1")
+            ms2 = r2["ms"] / st2
+            sb2 = step_bytes(c2, B2)
+            sec = {"value": n / (ms2 / 1e3), "unit": UNIT, "ms_per_step": ms2, "batch": B2,
+                   "hbm_gbs_step": sb2 / (ms2 / 1e3) / 1e9,
+                   "step_roofline_frac": sb2 / (ms2 / 1e3) / 1e9 / hbm_peak, "region": r2["region"],
+                   "launch": "cuda graph" if r2["graph"] else "eager"}
+            if "per_kernel_ms" in r2:
+                sec["per_kernel_us"] = {k: v * 1e3 for k, v in r2["per_kernel_ms"].items()}
+            if "e2e_s" in r2:
+                sec["e2e_value"] = n * r2["n_e2e"] / r2["e2e_s"]
+            line[key] = sec
+            line["gpu_launches"] += r2["launches"] * n
+        # the 30-layer stack: 49 prompt tokens token by token, then 200 timed tokens
+        cs, _, nl = STACK_SPECS["stack30_b1"]
+        rs = bench_stack(cs, [1, 16], nl, 200, 49, 3, True, dist_ctx, torch, abi)
+        for Bs, rr in rs.items():
+            line[f"stack30_b{Bs}"] = stack_summary(cs, Bs, nl, 200, rr, n, hbm_peak)
+            line["gpu_launches"] += rr["launches"] * n
     if dist_ctx.rank == 0 and not args.no_cpu_baseline:
-        rate, nst, thr = oracle_rate(cfg, B, init_std, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": rate / B, "unit": UNIT, "cores": thr, "kind": "oracle",
-                                "sample": f"{nst} sequence-steps of one sequence of the {args.workload} "
-                                          f"layer (float64 numpy oracle, {args.cpu_seconds:.0f} s), "
-                                          f"scaled to layer-steps of batch {B}"}
+        line["cpu_baseline"] = cpu_baseline(cfg, B, init_std, args.cpu_seconds, args.workload)
     return line
 
 
 def run_reference(args, dist_ctx):
-    """The oracle as the reference arm: each step is one sequence-step of the
-    workload's layer (a bounded sample of the batch), scaled to layer-steps."""
+    """The oracle as the reference arm: each timed step is one whole
+    layer-step (all B sequences of the workload advance one token), the
+    sequences spread over the host cores; rank 0 only."""
     if dist_ctx.rank != 0:
         return None
-    from oracle import OracleLayer
-    from gated_deltanet_hybrid_gb300.inputs import random_state, zero_state
     if args.workload in STACK_SPECS:
         cfg, B, _ = STACK_SPECS[args.workload]
         init_std = 0.0
     else:
         cfg, B, init_std = WORKLOAD_SPECS[args.workload]
-    rng = np.random.Generator(np.random.PCG64(99))
-    w = make_weights(cfg, rng)
-    st = random_state(cfg, 1, rng, init_std) if init_std > 0 else zero_state(cfg, 1)
-    layer = OracleLayer(cfg, w, st)
-    inputs = make_inputs(cfg, 1, 4, 123)
-    for i in range(args.warmup):
-        layer.step(*inputs[i % 4])
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        layer.step(*inputs[i % 4])
-    dt = time.perf_counter() - t0
-    value = args.steps / dt / B
-    thr = blas_threads()
+    seq_steps, dt, used = run_oracle_pool(cfg, B, init_std, host_cores(), steps=args.steps,
+                                          warmup=args.warmup)
+    value = args.steps / dt
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist_ctx.world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * B * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": args.workload, "batch": B},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle",
-                             "sample": f"each step is one sequence-step of one sequence of the "
-                                       f"batch-{B} layer, scaled to layer-steps"},
+            "data": "synthetic (seeded random weights and inputs of the workload's shape)",
+            "config": {"workload": args.workload, "batch": B, "hidden": cfg.hidden,
+                       "v_heads": cfg.n_v_heads, "dk": cfg.dk, "dv": cfg.dv},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
+                             "sample": f"{args.steps} whole layer-steps ({seq_steps} sequence-steps) "
+                                       f"of the batch-{B} layer, sequences spread over {used} host "
+                                       f"processes (one BLAS thread each), float64 numpy oracle"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

@@ -24,6 +24,10 @@ struct dn_layer {
     int expire_us_next;  // dn_debug_expire_wait: bounded device wait before the next step
     cudaEvent_t prof[5];  // one-shot per-stage events for the next step
     int prof_armed;
+    // completion of the last step enqueued on a stream other than `stream`
+    // (state copies wait for it); not recorded while that stream captures
+    cudaEvent_t step_done;
+    int step_done_pending;
     size_t bytes;
     std::vector<void *> allocs;
 };
@@ -48,6 +52,8 @@ int layer_alloc(dn_layer *l, void **p, size_t n) {
 }
 
 void layer_free_all(dn_layer *l) {
+    if (l->step_done != nullptr) cudaEventDestroy(l->step_done);
+    l->step_done = nullptr;
     for (void *p : l->allocs) cudaFree(p);
     g_device_bytes -= (int64_t)l->bytes;
     l->allocs.clear();
@@ -86,6 +92,21 @@ std::vector<uint8_t> tile_weights(const int8_t *W, int M, int K) {
 int cuda_fail(dn_layer *l) {
     l->failed = 1;
     return DN_ECUDA;
+}
+
+// The layer's device must be current for every call that enqueues work.
+bool on_layer_device(const dn_layer *l) {
+    int cur = -1;
+    return cudaGetDevice(&cur) == cudaSuccess && cur == l->device;
+}
+
+// State copies run on the layer's stream; order them after the last step
+// that ran on another stream.
+cudaError_t order_after_steps(dn_layer *l) {
+    if (!l->step_done_pending) return cudaSuccess;
+    const cudaError_t e = cudaStreamWaitEvent(l->stream, l->step_done, 0);
+    if (e == cudaSuccess) l->step_done_pending = 0;
+    return e;
 }
 
 #define DN_TRY(layer, expr)                            \
@@ -210,6 +231,11 @@ DN_API int dn_create(const dn_config *cfg, const dn_weights *w, void *stream, dn
     ALLOC(L.xb_out, xb_bytes_out);
     ALLOC(L.err, 4);
 #undef ALLOC
+    if (rc == DN_OK && cudaEventCreateWithFlags(&l->step_done, cudaEventDisableTiming) != cudaSuccess) {
+        (void)cudaGetLastError();
+        l->step_done = nullptr;
+        rc = DN_ECUDA;
+    }
     if (rc != DN_OK) {
         layer_free_all(l);
         delete l;
@@ -251,6 +277,7 @@ DN_API void dn_destroy(dn_layer *l) {
     int cur = 0;
     cudaGetDevice(&cur);
     if (cur != l->device) cudaSetDevice(l->device);
+    if (l->step_done_pending) cudaEventSynchronize(l->step_done);
     cudaStreamSynchronize(l->stream);
     layer_free_all(l);
     if (cur != l->device) cudaSetDevice(cur);
@@ -330,8 +357,10 @@ DN_API int dn_set_state(dn_layer *l, int seq0, int n, const float *S, const floa
     if (ptr_kind != DN_PTR_HOST && ptr_kind != DN_PTR_DEVICE) return DN_EINVAL;
     if (seq0 < 0 || n < 1 || seq0 + n > d.max_batch) return DN_EINVAL;
     if (S == nullptr || ring == nullptr || ring_pos == nullptr) return DN_EINVAL;
+    if (!on_layer_device(l)) return DN_EINVAL;
     if (l->failed) return DN_EFAILED;
     cudaStream_t st = l->stream;
+    DN_TRY(l, order_after_steps(l));
 
     // ring positions are validated on the host before anything is written
     std::vector<int32_t> rp((size_t)n);
@@ -361,11 +390,12 @@ DN_API int dn_get_state(dn_layer *l, int seq0, int n, float *S, float *ring, int
     const dn::Dims &d = l->d;
     if (ptr_kind != DN_PTR_HOST && ptr_kind != DN_PTR_DEVICE) return DN_EINVAL;
     if (seq0 < 0 || n < 1 || seq0 + n > d.max_batch) return DN_EINVAL;
+    if (!on_layer_device(l)) return DN_EINVAL;
     cudaStream_t st = l->stream;
     const size_t tile = (size_t)d.n_v * d.dk * d.dv;
     const size_t ring_n = (size_t)n * (d.conv_k - 1) * d.conv_ch;
     const cudaMemcpyKind kind = ptr_kind == DN_PTR_HOST ? cudaMemcpyDeviceToHost : cudaMemcpyDeviceToDevice;
-    cudaError_t e = cudaSuccess;
+    cudaError_t e = order_after_steps(l);
     if (S != nullptr)
         e = cudaMemcpyAsync(S, l->L.S + (size_t)seq0 * tile, (size_t)n * tile * 4, kind, st);
     if (e == cudaSuccess && (ring != nullptr || ring_pos != nullptr))
@@ -389,6 +419,7 @@ DN_API int dn_step(dn_layer *l, int batch, const float *x, const float *g, const
     if (ptr_kind != DN_PTR_HOST && ptr_kind != DN_PTR_DEVICE) return DN_EINVAL;
     if (batch < 1 || batch > d.max_batch) return DN_EINVAL;
     if (x == nullptr || g == nullptr || beta == nullptr || out == nullptr) return DN_EINVAL;
+    if (!on_layer_device(l)) return DN_EINVAL;
     if (l->failed) return DN_EFAILED;
     if (l->fail_next != 0) {
         const int code = l->fail_next;
@@ -442,6 +473,16 @@ DN_API int dn_step(dn_layer *l, int batch, const float *x, const float *g, const
     DN_TRY(l, dn::launch_splitk_reduce(L.part_out, L.nseg_out, L.s_out, od, d.hidden, d.v_dim, batch,
                                        L.rpos, d.conv_k, st));
     if (prof) DN_TRY(l, cudaEventRecord(l->prof[4], st));
+    if (st != l->stream) {
+        // let later state copies on the layer's stream wait for this step
+        // (a step captured into a graph is ordered by whoever launches it)
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        DN_TRY(l, cudaStreamIsCapturing(st, &cs));
+        if (cs == cudaStreamCaptureStatusNone) {
+            DN_TRY(l, cudaEventRecord(l->step_done, st));
+            l->step_done_pending = 1;
+        }
+    }
     if (ptr_kind == DN_PTR_HOST) {
         DN_TRY(l, cudaMemcpyAsync(out, L.out_stage, (size_t)batch * d.hidden * 4, cudaMemcpyDeviceToHost, st));
         DN_TRY(l, cudaStreamSynchronize(st));

@@ -1,7 +1,7 @@
 // int8 row-scaled projection on the 5th-generation tensor cores (tcgen05),
 // for batches large enough that the GEMV becomes a dense contraction:
 //   y[b][m] = s[m] * sum_k W[m][k] * x[b][k]
-// (the fused in_proj "qkv ++ z" and the out_proj of the gated-DeltaNet step;
+// (the fused in_proj of q, k, v and z rows and the out_proj of the step;
 // int8 rows with one fp32 scale each, page "feat(qwen36): the dense trunk
 // places itself", section "What this adds", item 1).
 //

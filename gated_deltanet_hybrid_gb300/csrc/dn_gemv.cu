@@ -3,8 +3,8 @@
 //
 // The projections of the gated-DeltaNet step are int8 matrices with one fp32
 // scale per output row (page "feat(qwen36): the dense trunk places itself",
-// section "What this adds", item 1; the fused in_proj is "qkv ++ z, one GEMV
-// instead of two").  At small batch the step is a weight stream: the kernel
+// section "What this adds", item 1; the in_proj holds the q, k, v rows and
+// the z rows in one matrix, so one GEMV serves both).  At small batch the step is a weight stream: the kernel
 // is built so that every SM keeps about 128 KB of weights in flight.
 //
 // W is stored as contiguous 8 KB tiles of 128 rows x 64 int8 in four 16-k

@@ -16,8 +16,8 @@ Draw order, with ``numpy.random.Generator(PCG64(seed))``:
   2. initial state (only when the workload asks for a random one): S, ring
   3. per decode step, in step order: x, then the two gate draws.
 
-The gates travel as inputs (the page keeps them on the host: "the gates
-(a/b, 32 outputs) stay on the CPU and travel as kernel parameters").  The
+The gates travel as inputs (the page computes the two small a/b gate
+projections on the host and hands their values to the kernels).  The
 workload turns its two normal draws a, b into the per-head log-decay g and
 write strength beta with g = -0.5 * softplus(a) and beta = sigmoid(b), in
 float64, then rounds both to float32 once; every consumer reads those

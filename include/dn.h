@@ -18,7 +18,7 @@
  *   - A CUDA error seen by a call marks the layer failed (sticky): afterwards
  *     dn_step and dn_set_state return DN_EFAILED, while dn_get_state still
  *     copies out what the device holds and dn_destroy still frees it (the
- *     page: "get_state works after a failed step").
+ *     page lets the state be read back after a step has failed).
  *   - Device work is enqueued on a CUDA stream and is asynchronous unless a
  *     call says otherwise; errors of asynchronous work surface at a later
  *     call on the same layer.
@@ -52,8 +52,9 @@ extern "C" {
 typedef struct dn_layer dn_layer; /* opaque; owns all of its device memory */
 
 /*
- * Layer dimensions.  The page's backend object "takes those dimensions as
- * parameters (vh <= 64, kdim/vdim <= 256)" (section "Where this goes next").
+ * Layer dimensions.  The page's backend object is parameterised by them, up
+ * to 64 value heads and key/value head sizes up to 256 (section "Where this
+ * goes next").
  * This build accepts:
  *   hidden      multiple of 16, 16 .. 16384
  *   n_qk_heads  >= 1, divides n_v_heads; n_v_heads <= 64
@@ -73,8 +74,9 @@ typedef struct dn_config {
 
 /*
  * Layer weights, host pointers, copied by dn_create (the caller may free
- * them afterwards).  The fused in_proj is "qkv ++ z, one GEMV instead of
- * two" with int8 rows and one fp32 scale per row (page "feat(qwen36): the
+ * them afterwards).  The in_proj fuses the q, k, v rows and the z rows into
+ * one matrix (one GEMV where there were two), int8 rows with one fp32 scale
+ * per row (page "feat(qwen36): the
  * dense trunk places itself", section "What this adds", item 1):
  *   w_in   int8 [in_rows][hidden]; rows are q | k | v | z, head h of a block
  *          is the contiguous slice h*d .. (h+1)*d; y[o] = s_in[o]*sum_i w_in[o][i]*x[i]
@@ -111,10 +113,14 @@ int dn_create(const dn_config *cfg, const dn_weights *w, void *stream, dn_layer 
  *   ring     [n][conv_k-1][conv_ch]   the last conv_k-1 conv inputs
  *   ring_pos [n] int32 in [0, conv_k-2], the ring slot of the oldest input
  * ptr_kind (DN_PTR_HOST or DN_PTR_DEVICE) says where all three live.  This
- * is the push of the page's host-canonical state ("The host copy of the
- * state stays the engine's, moved with set/get_state").  Returns after the
- * copy has completed (synchronises the layer's stream).  Errors: DN_EINVAL
- * (range, pointer or ring_pos out of range), DN_EFAILED, DN_ECUDA.
+ * is the push half of the page's state hand-over: the engine keeps the
+ * canonical copy of the state and moves it in and out of the layer with
+ * set/get.  The copy is ordered after every dn_step already enqueued on this
+ * layer, on whatever stream (the layer waits for the last step's completion
+ * event), and the call returns after the copy has completed (it synchronises
+ * the layer's stream).  Errors: DN_EINVAL (range, pointer or ring_pos out of
+ * range, or a device other than the layer's is current), DN_EFAILED,
+ * DN_ECUDA.
  */
 int dn_set_state(dn_layer *layer, int seq0, int n, const float *S, const float *ring,
                  const int32_t *ring_pos, int ptr_kind);
@@ -122,16 +128,19 @@ int dn_set_state(dn_layer *layer, int seq0, int n, const float *S, const float *
 /*
  * dn_get_state — copy out the state of sequences [seq0, seq0+n) in the same
  * layout as dn_set_state.  Any of S, ring, ring_pos may be NULL to skip it.
- * Works on a failed layer (returns what the device holds).  Synchronises the
- * layer's stream (so all prior dn_step work is included).  Errors:
- * DN_EINVAL, DN_ECUDA.
+ * Works on a failed layer (returns what the device holds).  The copy is
+ * ordered after every dn_step already enqueued on this layer, whichever
+ * stream it was enqueued on (the layer's stream waits for the last step's
+ * completion event), and the call synchronises the layer's stream before it
+ * returns.  Errors: DN_EINVAL (including a device other than the layer's
+ * being current), DN_ECUDA.
  */
 int dn_get_state(dn_layer *layer, int seq0, int n, float *S, float *ring, int32_t *ring_pos,
                  int ptr_kind);
 
 /*
- * dn_step — advance sequences [0, batch) by one decode token ("a decode
- * token end to end": in_proj GEMV, causal conv + SiLU with the ring
+ * dn_step — advance sequences [0, batch) by one decode token, the whole
+ * step on the device: in_proj GEMV, causal conv + SiLU with the ring
  * advancing, per value head the L2 norms of q and k, the decay, the delta
  * against the decayed state, the write-back, out = q^T S over the updated
  * state, the gated RMSNorm with silu(z), out_proj GEMV):
@@ -145,10 +154,14 @@ int dn_get_state(dn_layer *layer, int seq0, int n, float *S, float *ring, int32_
  *   CUDA graph.  x/g/beta must stay valid until the work has run.
  * ptr_kind DN_PTR_HOST: all four are host pointers; the call uploads x, g
  *   and beta, runs the step, downloads out and synchronises `stream` before
- *   returning (the page's "x up ... out down").  Pinned host memory makes
- *   the copies asynchronous DMA.
+ *   returning (the page's one upload of x and one download of out per
+ *   token).  Pinned host memory makes the copies asynchronous DMA.
+ * Steps of one layer on different streams must be ordered by the caller
+ * (events); dn_get_state and dn_set_state order themselves after the last
+ * step, whatever its stream.  The layer's device must be current.
  * Sequences >= batch are untouched.  Errors: DN_EINVAL (batch < 1 or >
- * max_batch, NULL pointer, bad ptr_kind), DN_EFAILED, DN_EINJECTED, DN_ECUDA.
+ * max_batch, NULL pointer, bad ptr_kind, another device current),
+ * DN_EFAILED, DN_EINJECTED, DN_ECUDA.
  */
 int dn_step(dn_layer *layer, int batch, const float *x, const float *g, const float *beta,
             float *out, int ptr_kind, void *stream);
@@ -181,9 +194,9 @@ int dn_stack_step(dn_layer *const *layers, int n_layers, int batch, float *h, co
 /*
  * dn_debug_fail_next — failure injection for tests: the next dn_step on this
  * layer returns `code` (a negative DN_E* value) before any device work and
- * marks the layer failed, as the page's fake backend "can be told to fail;
- * a failing step turns the layer off".  code = 0 cancels a pending
- * injection.  Errors: DN_EINVAL.
+ * marks the layer failed, like the page's fake backend, whose steps can be
+ * made to fail and whose failure switches the layer off.  code = 0 cancels a
+ * pending injection.  Errors: DN_EINVAL.
  */
 int dn_debug_fail_next(dn_layer *layer, int code);
 
@@ -244,7 +257,9 @@ int dn_step_kernels(const dn_layer *layer, int batch);
  * Work is enqueued on `stream` (NULL: the legacy default stream) and the
  * call returns without synchronising.  The first call on a device looks up
  * the array's device address (cudaGetSymbolAddress) with that device
- * current; make that first call before any stream capture.  Every call on a
+ * current; make that first call before any stream capture.  The address is
+ * kept for the life of the process, so a device reset (cudaDeviceReset) while
+ * the library stays loaded is not supported by this call.  Every call on a
  * device shares the one array: nothing in it needs to start at zero (a call
  * writes every scratch value it reads before reading it), but calls whose
  * work overlaps on the GPU (other streams, other threads) race on it.

@@ -1,6 +1,6 @@
 """The C-ABI library builds, loads without a GPU and exports exactly the
-calls that include/dn.h declares (the page's loader "ABI tripwire counts the
-five optional symbols"; here the tripwire covers the whole header)."""
+calls that include/dn.h declares (the page's loader checks that the optional
+entry points are all present; here the check covers the whole header)."""
 import os
 import re
 import shutil

@@ -1,7 +1,7 @@
 """The layer object's contract on the GPU: state ownership (set/get round
-trip, slices, ring-position convention), failure handling (the page's fake
-backend "can be told to fail; a failing step turns the layer off and the CPU
-continues from the card's state"), device-memory accounting, bitwise
+trip, slices, ring-position convention), failure handling (as with the page's fake
+backend: a step can be made to fail, the failure switches the layer off and
+the host carries on from the state read back from the card), device-memory accounting, bitwise
 reproducibility and checkpoint/resume."""
 import numpy as np
 import pytest
@@ -332,3 +332,44 @@ def test_profiled_step_records_five_stage_events_and_changes_nothing():
     finally:
         a.destroy()
         b.destroy()
+
+
+def test_state_copies_wait_for_steps_on_another_stream():
+    """Steps enqueued on a non-blocking stream other than the layer's: an
+    immediate dn_get_state (no synchronisation by the caller) already sees
+    every one of them, and a dn_set_state issued right after the steps lands
+    after them (the next get returns exactly what was set)."""
+    torch = _torch()
+    wl = custom_workload("xstream_35b_b64", SHAPE_35B, batch=64, steps=24, seed=21, init_std=0.02)
+    st = WorkloadStream(wl)
+    layer = GpuLayer.create(wl.cfg, st.weights[0], wl.batch, st.states[0])
+    try:
+        side = torch.cuda.Stream()  # torch pool streams are non-blocking
+        steps = []
+        for _ in range(24):
+            x, gates = st.next_step()
+            steps.append(_dev_inputs(x, gates[0][0], gates[0][1]))
+        torch.cuda.synchronize()
+        with torch.cuda.stream(side):
+            for xd, gd, bd, od in steps:
+                abi.dn_step(layer.handle, wl.batch, xd, gd, bd, od, stream=side.cuda_stream)
+        early = layer.get_state()          # no synchronisation before it
+        torch.cuda.synchronize()
+        late = layer.get_state()
+        assert np.array_equal(early.S, late.S)
+        assert np.array_equal(early.ring, late.ring)
+        assert np.array_equal(early.ring_pos, late.ring_pos)
+        # set_state right after more steps on the side stream
+        with torch.cuda.stream(side):
+            for xd, gd, bd, od in steps[:8]:
+                abi.dn_step(layer.handle, wl.batch, xd, gd, bd, od, stream=side.cuda_stream)
+        rng = np.random.default_rng(5)
+        want = random_state(wl.cfg, wl.batch, rng, 0.01)
+        abi.dn_set_state(layer.handle, 0, want.S, want.ring, want.ring_pos)
+        torch.cuda.synchronize()
+        got = layer.get_state()
+        assert np.array_equal(got.S, want.S)
+        assert np.array_equal(got.ring, want.ring)
+        assert np.array_equal(got.ring_pos, want.ring_pos)
+    finally:
+        layer.destroy()

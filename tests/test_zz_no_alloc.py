@@ -55,6 +55,34 @@ def test_noalloc_projection_matches_dn_step_in_proj_twice():
         layer.destroy()
 
 
+@pytest.mark.parametrize("M,K,B", [(200, 80, 1), (1000, 1040, 8), (1, 16, 1), (16384, 16384, 8)])
+def test_noalloc_projection_ragged_and_largest_shapes(M, K, B):
+    """Row tails (M not a multiple of 128), k tails (K not a multiple of 64),
+    one and eight sequences, the smallest shape and the largest accepted one,
+    each against the exact float64 product; y starts as NaN so that a row
+    the call does not write shows."""
+    import torch
+
+    rng = np.random.default_rng(M * 7 + K * 3 + B)
+    W = rng.integers(-127, 128, size=(M, K), dtype=np.int8)
+    s = rng.uniform(0.001, 0.01, size=M).astype(np.float32)
+    x = rng.standard_normal((B, K)).astype(np.float32)
+    W_d, s_d, x_d = torch.from_numpy(W).cuda(), torch.from_numpy(s).cuda(), torch.from_numpy(x).cuda()
+    y = torch.full((B, M), float("nan"), device="cuda")
+    for _ in range(2):  # the second call reuses the scratch the first one left
+        abi.dn_proj_i8_noalloc(W_d, s_d, x_d, y)
+        torch.cuda.synchronize()
+        got = y.cpu().numpy()
+        assert np.isfinite(got).all()
+        exact = np.empty((B, M))
+        x64 = x.astype(np.float64)
+        for r0 in range(0, M, 2048):  # bounded host memory for the largest shape
+            exact[:, r0:r0 + 2048] = x64 @ W[r0:r0 + 2048].astype(np.float64).T
+        exact *= s.astype(np.float64)
+        assert rel_err(got, exact) <= REL_TOL
+        y.fill_(float("nan"))
+
+
 def test_noalloc_projection_rejects_sizes_beyond_its_limits():
     import torch
 
