@@ -13,8 +13,11 @@ Timed regions rotate over --layers independent layer objects (distinct
 weights and states), so the working set of consecutive steps (about 300 MB
 per layer-step at batch 64) is larger than the 129 MB L2: nothing of a step
 is served from L2 by the previous step of the same layer.  The timed region
-replays a CUDA graph of one dn_step per layer object (the same kernels and
-work as eager calls, without the per-launch CPU cost); --no-graph times
+replays CUDA graphs of up to 512 consecutive dn_step calls (the same kernels
+and work as eager calls, without the per-launch CPU cost; consecutive steps
+overlap through programmatic dependent launch as eager calls do), so that
+exactly --steps steps are timed; the region is repeated (at least five times
+and 0.5 s) and the median reported with its spread; --no-graph times
 eager dn_step calls.  The end-to-end figure ("e2e") always goes through
 dn_step with pinned host buffers.
 
@@ -227,26 +230,46 @@ def make_inputs(cfg: DNConfig, B: int, n: int, seed: int):
     return sets
 
 
-def capture_steps(n_layers, step, torch):
-    """One CUDA graph per layer object, each holding one dn_step (so a timed
-    region of any length is made of whole graph replays); None if capture
-    is not possible."""
+GRAPH_CHUNK = 512  # steps per captured graph
+
+
+def capture_steps(n_steps, step, torch):
+    """One CUDA graph holding steps 0 .. n_steps-1 (dn_step calls in stream
+    order, so programmatic dependent launch overlaps consecutive steps inside
+    it as it does for eager calls); None if capture is not possible."""
     stream = torch.cuda.current_stream()
-    graphs = []
     try:
+        g = torch.cuda.CUDAGraph()
         cap = torch.cuda.Stream()
         cap.wait_stream(stream)
         with torch.cuda.stream(cap):
-            for i in range(n_layers):
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=cap):
+            with torch.cuda.graph(g, stream=cap):
+                for i in range(n_steps):
                     step(i)
-                graphs.append(g)
         torch.cuda.synchronize()
     except Exception as e:  # capture not possible: time eager launches
         print(f"[bench] graph capture failed ({e}); timing eager launches", file=sys.stderr)
         return None
-    return graphs
+    return g
+
+
+def step_graphs(steps, n_layers, step, torch):
+    """Graphs for a region of exactly `steps` steps: a graph of
+    min(steps, GRAPH_CHUNK) steps (a multiple of n_layers when longer than
+    that) replayed whole, then one graph of the remainder.  Returns a list of
+    graphs to replay in order, or None."""
+    chunk = min(steps, max(n_layers, GRAPH_CHUNK // n_layers * n_layers))
+    reps, rem = divmod(steps, chunk)
+    main = capture_steps(chunk, step, torch)
+    if main is None:
+        return None
+    seq = [main] * reps
+    if rem:
+        tail = capture_steps(rem, step, torch)
+        if tail is None:
+            return None
+        seq.append(tail)
+    return seq
 
 
 def timed_regions(run_region, steps, dist_ctx, torch, min_repeats=5, min_total_s=0.5, max_repeats=2000):
@@ -304,14 +327,14 @@ def bench_gpu(cfg, B, init_std, steps, warmup, n_layers, seed, use_graph, dist_c
     for i in range(warmup):
         step(i)
     torch.cuda.synchronize()
-    graphs = capture_steps(n_layers, step, torch) if use_graph else None
+    graphs = step_graphs(steps, n_layers, step, torch) if use_graph else None
     launches_per_step = abi.dn_step_kernels(layers[0], B)
 
     # ---- timed region: exactly `steps` steps, rotating over the layers ----
     def run_region():
         if graphs is not None:
-            for i in range(steps):
-                graphs[i % n_layers].replay()
+            for g in graphs:
+                g.replay()
         else:
             for i in range(steps):
                 step(i)
@@ -639,7 +662,7 @@ def run_ours(args, torch, dist_ctx):
                    "batch": B, "layers_rotated": args.layers,
                    "l2": f"inputs larger than L2: {args.layers} layer objects rotated, "
                          f"{sb / 1e6:.1f} MB per layer-step",
-                   "launch": "cuda graph of one step per layer" if r["graph"] else "eager",
+                   "launch": f"cuda graphs of up to {GRAPH_CHUNK} consecutive steps" if r["graph"] else "eager",
                    "parallelism": f"replicas x{n}" if n > 1 else "single GPU"},
         "region": r["region"],
         "hbm_gbs_step": sb / (ms_per_step / 1e3) / 1e9,
