@@ -1,37 +1,45 @@
-// Persistent, bulk-copy-pipelined kernel for large batches of 128 x 128
-// heads: the whole part of the page's step ("qwen36: run the DeltaNet layer
-// end to end on the card (Q36_DN_GPU=1)", section "What the PR does")
-// between the in_proj and the out_proj - causal conv + SiLU with the ring
-// advancing, the L2 norms of q and k, the decay, the delta against the
-// decayed state, the write-back, out = q^T S over the updated state, and
-// the gated RMSNorm with silu(z) - for one (sequence, value head) item at a
-// time.  Organised for HBM streaming:
+// Persistent, bulk-copy-pipelined kernel for 128 x 128 heads: the whole part
+// of the page's step ("qwen36: run the DeltaNet layer end to end on the card
+// (Q36_DN_GPU=1)", section "What the PR does") between the in_proj and the
+// out_proj - causal conv + SiLU with the ring advancing, the L2 norms of q
+// and k, the decay, the delta against the decayed state, the write-back,
+// out = q^T S over the updated state, and the gated RMSNorm with silu(z) -
+// one (sequence, value head) item at a time.  Organised for HBM streaming:
 //
-//  * one CTA per SM walks a contiguous range of items (b-major);
+//  * one CTA per SM walks a contiguous range of items (b-major, so the two
+//    value heads of a q/k head follow each other);
 //  * each item's 64 KB state tile arrives by one cp.async.bulk copy on an
-//    mbarrier into a 3-deep shared-memory ring, is updated in place by 16
-//    warps (each thread keeps its 32 values in registers between the
-//    decay/delta pass and the write-back/readout pass) and leaves by one bulk
-//    store; the load of item j+2 is issued as soon as the store of item j-1
-//    has been read out of shared memory;
-//  * the item's inputs - its q and k rows (of its q/k head), its v and z rows,
-//    one per thread (512 = 4 x 128 rows) - are built on the fly: the in_proj
-//    output of a row is the sum of its segment partials in slot order
-//    (dn_sched.cuh) times the row scale; q, k, v go through the conv over the
-//    ring (K-1 history slots read, the newest written) and SiLU, z through
-//    SiLU; q and k are L2-normalised with fp32 warp sums combined in a fixed
-//    order.  The CTA's ring positions are read once into shared memory, so
-//    an item's loads (segment count, partials, ring history, row scale and
-//    conv weights) depend on nothing else and are issued one item ahead (as
-//    volatile loads, so that the compiler keeps them there): their latency
-//    hides behind the previous item's tile;
-//  * the first two state tiles, and the first item's loads that do not come
-//    from the in_proj kernel, are issued before the kernel waits for it
-//    (programmatic dependent launch): the state, ring, gates and weights are
-//    not written by it, the partials and segment counts are.
+//    mbarrier into a 3-deep shared-memory ring;
+//  * 16 consumer warps (512 threads) read the tile into registers (32 values
+//    per thread), decay it,
+//    reduce it against k^ (delta), write it back and reduce it against q^
+//    (readout) in registers, write it back into its stage and send it out
+//    with one bulk store (global stores from registers would hold up the
+//    load/store unit that the producers' loads need);
+//  * 4 producer warps build the next item's inputs meanwhile, in a
+//    double-buffered record, one warp per row kind (16-byte loads of four
+//    channels per lane): for each of the item's q, k, v and z rows the
+//    in_proj output (its segment partials summed in slot order, dn_sched.cuh,
+//    times the row scale), then the conv over the ring (K-1 history slots
+//    read, the newest written by the row's owner) and SiLU for q, k, v, SiLU
+//    for z, the q/k L2 norms (one warp's fp32 shuffle sum, fixed order), the
+//    query scale and the gates.  The second value head of a q/k head reuses
+//    the first one's q^ and k^.  Producers and consumers meet on two
+//    mbarriers per record buffer (full, empty).  The loads of item j+1 are
+//    issued as soon as item j's rows are computed;
+//  * a stage takes the item three ahead once the bulk store of its item has
+//    read it; the readout's gated RMSNorm is finished during the next item
+//    by warps 4-7, which are otherwise idle while warps 0-3 form the delta;
+//  * the first three state tiles, the ring positions and the norm weights
+//    are requested before the kernel waits for the in_proj kernel
+//    (programmatic dependent launch): the in_proj writes only the partials
+//    and segment counts.
 //
-// Every wait is bounded (about one second); on timeout the kernel records an
-// error in `err`, waits (bounded) for its own bulk copies and returns.
+// Every mbarrier wait is bounded (about one second of the global timer); on
+// timeout the kernel records an error in `err`, leaves its loop (the
+// consumers on a vote that all of them take, so no named barrier is left
+// waiting; a producer warp on its own: it meets the others on mbarriers only),
+// waits (bounded) for its own bulk copies and returns.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -43,15 +51,22 @@ namespace dn {
 namespace {
 
 constexpr int D = 128;               // dk = dv
-constexpr int NT = 512;              // threads: one input row of the item each
+constexpr int NC = 512;              // consumer threads (16 warps)
+constexpr int NPW = 4;               // producer warps (one row kind each: q, k, v, z)
+constexpr int NT = NC + 32 * NPW;    // 640
 constexpr int STAGES = 3;
 constexpr uint32_t kTileBytes = D * D * 4;
 constexpr int LPR = D / 4;           // 32 lanes across a row (float4 each)
-constexpr int RPP = NT / LPR;        // 16 rows per pass
-constexpr int NP = D / RPP;          // 8 float4 per thread
-constexpr int PV = 6;                // partial slots fetched ahead (more are read on the spot)
+constexpr int RPP = NC / LPR;        // 16 rows per pass
+constexpr int NP = D / RPP;          // 8 float4 per consumer thread
+constexpr int PV = 4;                // partial slots loaded unconditionally (more are read on the spot)
 constexpr int kMaxSeqCta = 64;       // sequences one CTA's item range may touch
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
+// named barriers (0 is __syncthreads)
+constexpr int kBarCons = 1;          // the 512 consumer threads
+// the consumer thread that issues the tile copies and stores (warp 15 has
+// nothing else to do after the readout's barrier)
+constexpr int kTma = NC - 32;
 
 struct StreamParams {
     const float *part_in;  // in_proj segment partials
@@ -75,13 +90,17 @@ struct __align__(128) StreamSmem {
     float tile[STAGES][D * D];  // 3 x 64 KB
     float rec[2][4 * D];        // the item's q^ | k^ | v | silu(z), double-buffered
     float gate[2][2];           // exp(g), beta
-    float red[RPP][D];          // 8 KB
+    float red[2][RPP][D];       // 2 x 8 KB: per-pass partial sums (kv, then readout)
     float delta[D];
-    float ssq_o[4];
-    float ssq_qk[2][8];         // warp sums of squares (warps 0-3 q, 4-7 k), double-buffered
+    float ssq_o[4];             // readout warp sums of squares
+    float o_prev[D];            // the last item's readout, normalised during the next item
+    float zw_prev[D];           // its w_norm * silu(z)
     float wn[D];                // gated-RMSNorm weight
     int dpos[kMaxSeqCta];       // ring positions of the CTA's sequences
-    uint64_t full[STAGES];
+    uint64_t full[STAGES];      // tile landed
+    uint64_t rec_full[2];       // record built (one arrival per producer warp)
+    uint64_t rec_empty[2];      // record read (one arrival per consumer warp)
+    int failed;                 // a role gave up on a wait
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -111,6 +130,26 @@ __device__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
         if ((it & 63u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
     }
 }
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// named barrier over `n` threads
+__device__ __forceinline__ void bar_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+// named barrier over `n` threads that also returns the AND of `ok`
+__device__ __forceinline__ bool bar_and(int id, int n, bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)ok), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
 // the item's state tile, on the stage's barrier
 __device__ __forceinline__ void load_tile(StreamSmem &sm, int st, const StreamParams &p, int item) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(&sm.full[st])),
@@ -122,12 +161,6 @@ __device__ __forceinline__ void load_tile(StreamSmem &sm, int st, const StreamPa
         "l"(p.S + (size_t)item * (D * D)), "r"(kTileBytes), "r"(smem_u32(&sm.full[st]))
         : "memory");
 }
-__device__ __forceinline__ void store_tile(float *dst, const float *src) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
-                 "r"(smem_u32(src)), "r"(kTileBytes)
-                 : "memory");
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -137,26 +170,6 @@ __device__ __forceinline__ float warp_sum(float v) {
 // (__expf, __fdividef: a few ulp, far inside the step's tolerance; for
 // a -> -inf the divisor overflows and the quotient is 0, silu's limit)
 __device__ __forceinline__ float silu_f(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
-
-// This thread's input row of item (b, h): region 0 q, 1 k, 2 v, 3 z (thread
-// t serves row t % 128 of region t / 128).
-struct RowRef {
-    int b, c;          // sequence, in_proj row
-    bool conv, ring_w; // goes through the conv; this item writes its ring slot
-};
-__device__ __forceinline__ RowRef row_of(const StreamParams &p, int b, int h, int hq, int t) {
-    RowRef r;
-    r.b = b;
-    const int region = t >> 7, o = t & (D - 1);
-    r.c = region == 0 ? hq * D + o
-        : region == 1 ? p.qk_dim + hq * D + o
-        : region == 2 ? 2 * p.qk_dim + h * D + o
-                      : p.conv_ch + h * D + o;
-    r.conv = region < 3;
-    // q and k rows are shared by the value heads of a q/k head: the first writes
-    r.ring_w = region == 2 || (region < 2 && h == hq * p.group);
-    return r;
-}
 
 __device__ __forceinline__ float ld_cg(const float *ptr) {
     float v;
@@ -168,104 +181,119 @@ __device__ __forceinline__ float ld_nc(const float *ptr) {
     asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(ptr));
     return v;
 }
-
-// One item ahead: the row's first PV segment partials, its ring history,
-// scale and conv weights, and the item's gates.  Every load is
-// unconditional, from an address that is valid whatever the row (slots past
-// the segment count and the conv inputs of z rows are masked where they are
-// used), because a select on a value still in flight would wait for it here.
-template <int KC>
-struct Ahead {
-    float pv[PV], hist[KC - 1], sc, wc[KC], gv, bv;
-    int ns;  // segment count of the row's tile
-};
-
 __device__ __forceinline__ int ld_cg_s32(const int *ptr) {
     int v;
     asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(ptr));
     return v;
 }
-
-// The loads that the in_proj kernel does not feed: ring history, row scale,
-// conv weights, gates (for the first item they go out before the kernel
-// waits for the in_proj kernel).
+// The loads of four channels c .. c+3 of one row kind (q, k, v or z) of an
+// item, 16 bytes each: the in_proj segment partials (the first PV slots
+// unconditionally, from clamped addresses, so no load waits for the segment
+// count), the segment count, the row scales and, for q, k and v, the conv
+// history and weights.
 template <int KC>
-__device__ __forceinline__ void load_ahead_fixed(const StreamParams &p, const StreamSmem &sm, int b0, int b,
-                                                 int h, int hq, int t, Ahead<KC> &a) {
-    const RowRef r = row_of(p, b, h, hq, t);
-    const int item = b * p.n_v + h;
-    const int cr = r.conv ? r.c : 0;  // z rows read channel 0's ring and weights
-    const float *rb = p.ring + (size_t)r.b * KC * p.conv_ch + cr;
-    int slot = sm.dpos[r.b - b0];
+struct RowLoads {
+    float4 pv[PV], sc, hist[KC - 1], wc[KC];
+    int ns;
+};
+
+__device__ __forceinline__ float4 ld_cg4(const float *ptr) {
+    float4 v;
+    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(ptr));
+    return v;
+}
+__device__ __forceinline__ float4 ld_nc4(const float *ptr) {
+    float4 v;
+    asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(ptr));
+    return v;
+}
+
+template <int KC>
+__device__ __forceinline__ void load_row_fixed(const StreamParams &p, const StreamSmem &sm, int b0, int b, int c,
+                                               bool conv, RowLoads<KC> &r) {
+    r.sc = ld_nc4(p.s_in + c);
+    if (!conv) return;  // z rows (uniform across the warp)
+    const float *rb = p.ring + (size_t)b * KC * p.conv_ch + c;
+    int slot = sm.dpos[b - b0];
 #pragma unroll
     for (int m = 0; m < KC - 1; ++m) {  // oldest input first
-        a.hist[m] = ld_cg(rb + (size_t)slot * p.conv_ch);
+        r.hist[m] = ld_cg4(rb + (size_t)slot * p.conv_ch);
         if (++slot == KC) slot = 0;
     }
-    a.sc = ld_nc(p.s_in + r.c);
 #pragma unroll
-    for (int m = 0; m < KC; ++m) a.wc[m] = ld_nc(p.wconv_t + (size_t)m * p.conv_ch + cr);
-    a.gv = ld_cg(p.g + item);  // [B][n_v] = item order
-    a.bv = ld_cg(p.beta + item);
+    for (int m = 0; m < KC; ++m) r.wc[m] = ld_nc4(p.wconv_t + (size_t)m * p.conv_ch + c);
 }
-// The in_proj kernel's output for the row: segment count and partials.
+
+__device__ __forceinline__ const float *row_partials(const StreamParams &p, int b, int c) {
+    const int ptile = (b >> 6) * p.MT + (c >> 7);
+    return p.part_in + (size_t)ptile * p.max_seg * (64 * D) + (b & 63) * D + (c & (D - 1));
+}
+
 template <int KC>
-__device__ __forceinline__ void load_ahead_part(const StreamParams &p, int b, int h, int hq, int t,
-                                                Ahead<KC> &a) {
-    const RowRef r = row_of(p, b, h, hq, t);
-    const int ptile = (r.b >> 6) * p.MT + (r.c >> 7);
-    a.ns = ld_cg_s32(p.nseg_in + ptile);
-    const float *pp = p.part_in + (size_t)ptile * p.max_seg * (64 * D) + (r.b & 63) * D + (r.c & (D - 1));
+__device__ __forceinline__ void load_row_part(const StreamParams &p, int b, int c, RowLoads<KC> &r) {
+    r.ns = ld_cg_s32(p.nseg_in + (b >> 6) * p.MT + (c >> 7));
+    const float *pp = row_partials(p, b, c);
 #pragma unroll
     for (int k = 0; k < PV; ++k)  // slots past max_seg fall back to slot 0
-        a.pv[k] = ld_cg(pp + (size_t)(k < p.max_seg ? k : 0) * (64 * D));
-}
-template <int KC>
-__device__ __forceinline__ void load_ahead(const StreamParams &p, const StreamSmem &sm, int b0, int b, int h,
-                                           int hq, int t, Ahead<KC> &a) {
-    load_ahead_part(p, b, h, hq, t, a);
-    load_ahead_fixed(p, sm, b0, b, h, hq, t, a);
+        r.pv[k] = ld_cg4(pp + (size_t)(k < p.max_seg ? k : 0) * (64 * D));
 }
 
-// The row's in_proj output, conv + SiLU (z: SiLU only); the ring slot of the
-// new input is written by the item that owns the row.
+__device__ __forceinline__ void add4(float4 &a, const float4 &b) {
+    a.x += b.x;
+    a.y += b.y;
+    a.z += b.z;
+    a.w += b.w;
+}
+
+// The four channels' in_proj output (partials in slot order, times the row scale)
 template <int KC>
-__device__ __forceinline__ float build_input(const StreamParams &p, const StreamSmem &sm, int b0, int b, int h,
-                                             int hq, int t, const Ahead<KC> &a) {
-    const RowRef r = row_of(p, b, h, hq, t);
-    const int ns = a.ns;
-    float acc = 0.f;
+__device__ __forceinline__ float4 row_value(const StreamParams &p, int b, int c, const RowLoads<KC> &r) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < PV; ++k)
-        if (k < ns) acc += a.pv[k];  // slot order
-    if (ns > PV) {
-        const int ptile = (r.b >> 6) * p.MT + (r.c >> 7);
-        const float *pp = p.part_in + (size_t)ptile * p.max_seg * (64 * D) + (r.b & 63) * D + (r.c & (D - 1));
-        for (int k = PV; k < ns; ++k) acc += __ldcg(pp + (size_t)k * (64 * D));
+        if (k < r.ns) add4(acc, r.pv[k]);
+    if (r.ns > PV) {
+        const float *pp = row_partials(p, b, c);
+        for (int k = PV; k < r.ns; ++k) add4(acc, ld_cg4(pp + (size_t)k * (64 * D)));
     }
-    const float xv = a.sc * acc;
-    if (!r.conv) return silu_f(xv);
-    float cv = 0.f;
-#pragma unroll
-    for (int m = 0; m < KC - 1; ++m) cv = fmaf(a.wc[m], a.hist[m], cv);
-    cv = fmaf(a.wc[KC - 1], xv, cv);
-    if (r.ring_w) {
-        int ws = sm.dpos[r.b - b0] + KC - 1;  // the oldest slot, not read by this step
-        if (ws >= KC) ws -= KC;
-        p.ring[((size_t)r.b * KC + ws) * p.conv_ch + r.c] = xv;
-    }
-    return silu_f(cv);
+    return make_float4(r.sc.x * acc.x, r.sc.y * acc.y, r.sc.z * acc.z, r.sc.w * acc.w);
 }
 
-// Gated RMSNorm of one item's readout (thread t < 128 holds o[t]; the warp
-// sums of o^2 are in ssq_o) and the store of the result: fp32 rows for the
-// CUDA-core out_proj, or bf16 hi/lo operand rows for the tensor-core one.
-__device__ __forceinline__ void store_norm(const StreamParams &p, const StreamSmem &sm, float o, int b, int h,
-                                           const float *rz, int t) {
+// conv over the history and the new input xv, then SiLU; the row's owner
+// writes xv into the ring slot that this step does not read
+template <int KC>
+__device__ __forceinline__ float4 conv_silu(const StreamParams &p, const StreamSmem &sm, int b0, int b, int c,
+                                            float4 xv, bool owner, const RowLoads<KC> &r) {
+    float4 cv = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int m = 0; m < KC - 1; ++m) {
+        cv.x = fmaf(r.wc[m].x, r.hist[m].x, cv.x);
+        cv.y = fmaf(r.wc[m].y, r.hist[m].y, cv.y);
+        cv.z = fmaf(r.wc[m].z, r.hist[m].z, cv.z);
+        cv.w = fmaf(r.wc[m].w, r.hist[m].w, cv.w);
+    }
+    cv.x = fmaf(r.wc[KC - 1].x, xv.x, cv.x);
+    cv.y = fmaf(r.wc[KC - 1].y, xv.y, cv.y);
+    cv.z = fmaf(r.wc[KC - 1].z, xv.z, cv.z);
+    cv.w = fmaf(r.wc[KC - 1].w, xv.w, cv.w);
+    if (owner) {
+        int ws = sm.dpos[b - b0] + KC - 1;  // the oldest slot, not read by this step
+        if (ws >= KC) ws -= KC;
+        *reinterpret_cast<float4 *>(p.ring + ((size_t)b * KC + ws) * p.conv_ch + c) = xv;
+    }
+    return make_float4(silu_f(cv.x), silu_f(cv.y), silu_f(cv.z), silu_f(cv.w));
+}
+
+// Gated RMSNorm of one item's readout o[i] (i = 0..127; the warp sums of
+// o^2 are in ssq_o, zw = w_norm[i] * silu(z[i])) and the store of the
+// result: fp32 rows for the CUDA-core out_proj, or bf16 hi/lo operand rows
+// for the tensor-core one.
+__device__ __forceinline__ void store_norm(const StreamParams &p, const StreamSmem &sm, float o, float zw, int b,
+                                           int h, int i) {
     const float total = (sm.ssq_o[0] + sm.ssq_o[1]) + (sm.ssq_o[2] + sm.ssq_o[3]);
     const float rinv = 1.0f / sqrtf(total / (float)D + p.norm_eps);
-    const float n = o * rinv * sm.wn[t] * rz[t];
-    const int k = h * D + t;
+    const float n = o * rinv * zw;
+    const int k = h * D + i;
     if (p.xb_out == nullptr) {
         p.nrm[(size_t)b * p.v_dim + k] = n;
     } else {
@@ -279,90 +307,116 @@ __device__ __forceinline__ void store_norm(const StreamParams &p, const StreamSm
     }
 }
 
+// Producer warps: build the record (q^, k^, v, silu(z), gates) of every item
+// of the CTA's range, one item ahead of the consumers.  Warp `kind` builds
+// one row kind (0 q, 1 k, 2 v, 3 z), lane l channels 4l .. 4l+3 of the head,
+// so a q or k norm is one warp's sum.  The loads of item j+1 are issued as
+// soon as item j's values are computed (the registers are free again), so
+// their latency hides behind the rest of item j.
 template <int KC>
-__global__ void __launch_bounds__(NT, 1) dn_core_stream_kernel(const StreamParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    StreamSmem &sm = *reinterpret_cast<StreamSmem *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    const int i0 = (int)(((unsigned)blockIdx.x * (unsigned)p.items) / gridDim.x);
-    const int i1 = (int)(((unsigned)(blockIdx.x + 1) * (unsigned)p.items) / gridDim.x);
-    const int n_items = i1 - i0;
-
-    int issued = 0;  // (thread 0) tile loads issued so far
-    if (t == 0) {
-        for (int s = 0; s < STAGES; ++s)
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&sm.full[s])));
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        for (int j = 0; j < 2 && j < n_items; ++j, ++issued) load_tile(sm, j, p, i0 + j);
-    }
-    // the norm weights and the sequences' ring positions (advanced by the
-    // previous step) in one round trip; the state is not written by the
-    // in_proj kernel, its partials and segment counts are
-    if (t < D) sm.wn[t] = p.w_norm[t];
-    const int b0 = i0 / p.n_v;
-    const int nseq = n_items > 0 ? (i1 - 1) / p.n_v - b0 + 1 : 0;
-    for (int i = t; i < nseq; i += NT) sm.dpos[i] = p.rpos[2 * (b0 + i)];
-    __syncthreads();
-    // the item (b, h) and its q/k head hq, stepped without divisions
+__device__ void produce(const StreamParams &p, StreamSmem &sm, int i0, int n_items, int b0, int kind, int lane) {
+    const int cl = 4 * lane;
+    const bool conv = kind < 3, qk = kind < 2;
+    const int base = kind == 0 ? 0 : kind == 1 ? p.qk_dim : kind == 2 ? 2 * p.qk_dim : p.conv_ch;
     int b = b0, h = i0 - b0 * p.n_v, hq = h / p.group;
-    Ahead<KC> ac;  // item j
-    if (n_items > 0) load_ahead_fixed(p, sm, b0, b, h, hq, t, ac);
+    RowLoads<KC> r;
+    float gv = 0.f, bv = 0.f;
+    // the first item's loads that the in_proj does not feed go out before the wait
+    int c = base + (qk ? hq : h) * D + cl;
+    load_row_fixed(p, sm, b0, b, c, conv, r);
+    if (kind == 0 && lane == 0) {
+        gv = ld_cg(p.g + i0);
+        bv = ld_cg(p.beta + i0);
+    }
     pdl_wait();
-    if (t == 0) pdl_trigger();
-    if (n_items > 0) load_ahead_part(p, b, h, hq, t, ac);
-
-    const int c4 = t % LPR, r0 = t / LPR;
-    bool failed = false;
-    float o_prev = 0.f;      // (t < D) the previous item's readout, normalised after the next barrier
-    int b_prev = 0, h_prev = 0;
+    load_row_part(p, b, c, r);
+    bool reuse = false;  // item j has the q/k head of item j-1
     for (int j = 0; j < n_items; ++j) {
-        const int item = i0 + j;
-        const int st = j % STAGES, rbuf = j & 1;
-        const int hn = h + 1 == p.n_v ? 0 : h + 1, bn = hn == 0 ? b + 1 : b;
-        const int hqn = hn == 0 ? 0 : (hn == (hq + 1) * p.group ? hq + 1 : hq);
-
-        // ---- the item's q^, k^, v, silu(z), gates; loads for the next item ----
-        const float u = build_input(p, sm, b0, b, h, hq, t, ac);
-        const float gv = ac.gv, bv = ac.bv;
-        if (j + 1 < n_items) load_ahead(p, sm, b0, bn, hn, hqn, t, ac);
-        if (warp < 8) {  // q (warps 0-3) and k (warps 4-7): sums of squares
-            const float sq = warp_sum(u * u);
-            if (lane == 0) sm.ssq_qk[rbuf][warp] = sq;
+        const int rb = j & 1;
+        c = base + (qk ? hq : h) * D + cl;
+        float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (!(qk && reuse)) {
+            const float4 xv = row_value(p, b, c, r);
+            if (conv) {
+                // v rows belong to one item; q/k rows are written by the q/k head's first value head
+                u = conv_silu(p, sm, b0, b, c, xv, kind == 2 || h == hq * p.group, r);
+            } else {
+                u = make_float4(silu_f(xv.x), silu_f(xv.y), silu_f(xv.z), silu_f(xv.w));
+            }
         }
-        __syncthreads();
-        if (j > 0 && t < D) store_norm(p, sm, o_prev, b_prev, h_prev, sm.rec[rbuf ^ 1] + 3 * D, t);
-        float val = u;
-        if (t < 2 * D) {
-            const float *ssq = sm.ssq_qk[rbuf] + (t >> 7) * 4;
-            val = u * (1.0f / sqrtf(((ssq[0] + ssq[1]) + (ssq[2] + ssq[3])) + p.l2_eps)) *
-                  (t < D ? p.q_scale : 1.0f);
+        const float gj = gv, bj = bv;
+        // item j+1 and its loads
+        const int bn = h + 1 == p.n_v ? b + 1 : b, hn = h + 1 == p.n_v ? 0 : h + 1, hqn = hn / p.group;
+        const bool reuse_n = bn == b && hqn == hq;
+        if (j + 1 < n_items) {
+            if (!(qk && reuse_n)) {
+                const int cn = base + (qk ? hqn : hn) * D + cl;
+                load_row_fixed(p, sm, b0, bn, cn, conv, r);
+                load_row_part(p, bn, cn, r);
+            }
+            if (kind == 0 && lane == 0) {
+                gv = ld_cg(p.g + i0 + j + 1);
+                bv = ld_cg(p.beta + i0 + j + 1);
+            }
         }
-        sm.rec[rbuf][t] = val;
-        if (t == 0) {
-            sm.gate[rbuf][0] = expf(gv);
-            sm.gate[rbuf][1] = bv;
+        float4 outv = u;
+        if (qk) {
+            if (!reuse) {
+                const float ss = warp_sum((u.x * u.x + u.y * u.y) + (u.z * u.z + u.w * u.w));
+                const float sc = (1.0f / sqrtf(ss + p.l2_eps)) * (kind == 0 ? p.q_scale : 1.0f);
+                outv = make_float4(u.x * sc, u.y * sc, u.z * sc, u.w * sc);
+            } else {
+                outv = *reinterpret_cast<const float4 *>(&sm.rec[rb ^ 1][kind * D + cl]);
+            }
         }
-
-        // ---- the state tile --------------------------------------------------
-        const bool landed = mbar_wait(&sm.full[st], (j / STAGES) & 1);
-        if (!__syncthreads_and(landed)) {
-            failed = true;
+        // record buffer rb is free once the consumers are done with item j-2
+        if (j >= 2 && !mbar_wait(&sm.rec_empty[rb], ((j >> 1) - 1) & 1)) {
+            sm.failed = 1;
             break;
         }
-        const float *rq = sm.rec[rbuf], *rk = rq + D, *rv = rq + 2 * D;
-        const float eg = sm.gate[rbuf][0], bt = sm.gate[rbuf][1];
+        *reinterpret_cast<float4 *>(&sm.rec[rb][kind * D + cl]) = outv;
+        if (kind == 0 && lane == 0) {
+            sm.gate[rb][0] = expf(gj);
+            sm.gate[rb][1] = bj;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.rec_full[rb]);  // release: the record's writes come first
+        b = bn;
+        h = hn;
+        hq = hqn;
+        reuse = reuse_n;
+    }
+}
 
+// Consumer warps (t = 0..511): the state update of every item.  Thread t
+// holds rows r0 + 16 i (i < 8), columns 4 c4 .. 4 c4 + 3 of the tile.  The
+// updated tile goes back into its stage and leaves by one bulk store; the
+// stage takes the item STAGES ahead once that store has read it (checked
+// during the next item).  The readout's gated RMSNorm is finished by warps
+// 4-7 during the next item.  Returns the number of tile copies issued.
+__device__ int consume(const StreamParams &p, StreamSmem &sm, int i0, int n_items, int b0, int t) {
+    const int warp = t >> 5, lane = t & 31;
+    const int c4 = t % LPR, r0 = t / LPR;
+    int issued = n_items < STAGES ? n_items : STAGES;
+    int b = b0, h = i0 - b0 * p.n_v, b_prev = 0, h_prev = 0;
+    int j = 0;
+    for (; j < n_items; ++j) {
+        const int item = i0 + j, st = j % STAGES, rb = j & 1;
+        bool ok = mbar_wait(&sm.full[st], (j / STAGES) & 1);
         float *tile = sm.tile[st];
+        float4 s[NP];
+#pragma unroll
+        for (int i = 0; i < NP; ++i) s[i] = *reinterpret_cast<const float4 *>(tile + (r0 + i * RPP) * D + c4 * 4);
+        ok = ok && mbar_wait(&sm.rec_full[rb], (j >> 1) & 1);
+        const float *rq = sm.rec[rb], *rk = rq + D, *rv = rq + 2 * D;
+        const float eg = sm.gate[rb][0], bt = sm.gate[rb][1];
+        float *red = &sm.red[rb][0][0];
 
         // decay, then what the decayed state predicts for k
-        float4 s[NP];
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < NP; ++i) {
-            const int r = r0 + i * RPP;
-            s[i] = *reinterpret_cast<const float4 *>(tile + r * D + c4 * 4);
-            const float kr = rk[r];
+            const float kr = rk[r0 + i * RPP];
             s[i].x *= eg;
             s[i].y *= eg;
             s[i].z *= eg;
@@ -372,17 +426,29 @@ __global__ void __launch_bounds__(NT, 1) dn_core_stream_kernel(const StreamParam
             acc.z = fmaf(s[i].z, kr, acc.z);
             acc.w = fmaf(s[i].w, kr, acc.w);
         }
-        *reinterpret_cast<float4 *>(&sm.red[r0][c4 * 4]) = acc;
-        __syncthreads();
-        // delta against the decayed state
+        *reinterpret_cast<float4 *>(red + r0 * D + c4 * 4) = acc;
+        if (!bar_and(kBarCons, NC, ok)) {  // no consumer gives up on a wait alone
+            sm.failed = 1;
+            break;
+        }
+        if (t == kTma && j >= 1 && j - 1 + STAGES < n_items) {
+            // the stage of item j-1 is free once its bulk store has read it
+            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            load_tile(sm, (j - 1) % STAGES, p, item - 1 + STAGES);
+            issued = j + STAGES;
+        }
         if (t < D) {
+            // delta against the decayed state
             float kv = 0.f;
 #pragma unroll
-            for (int r = 0; r < RPP; ++r) kv += sm.red[r][t];
+            for (int r = 0; r < RPP; ++r) kv += red[r * D + t];
             sm.delta[t] = bt * (rv[t] - kv);
+        } else if (t < 2 * D && j >= 1) {
+            store_norm(p, sm, sm.o_prev[t - D], sm.zw_prev[t - D], b_prev, h_prev, t - D);
         }
-        __syncthreads();
-        // write-back S += k delta^T, and the readout partials over the updated state
+        bar_sync(kBarCons, NC);
+        // write-back S += k delta^T into the stage, and the readout partials
+        // over the updated state
         const float4 d4 = *reinterpret_cast<const float4 *>(&sm.delta[c4 * 4]);
         acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -399,42 +465,86 @@ __global__ void __launch_bounds__(NT, 1) dn_core_stream_kernel(const StreamParam
             acc.z = fmaf(s[i].z, qr, acc.z);
             acc.w = fmaf(s[i].w, qr, acc.w);
         }
-        *reinterpret_cast<float4 *>(&sm.red[r0][c4 * 4]) = acc;
+        *reinterpret_cast<float4 *>(red + r0 * D + c4 * 4) = acc;
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // tile writes -> bulk store
-        __syncthreads();
-        if (t == 0) {
-            store_tile(p.S + (size_t)item * (D * D), tile);
-            // the stage of item j-1 is free once its store has read shared memory
-            asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-            if (j + 2 < n_items) {
-                load_tile(sm, (j + 2) % STAGES, p, item + 2);
-                issued = j + 3;
-            }
+        bar_sync(kBarCons, NC);
+        if (t == kTma) {
+            asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                             p.S + (size_t)item * (D * D)),
+                         "r"(smem_u32(tile)), "r"(kTileBytes)
+                         : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         }
-        // readout o = S^T q; its gated RMSNorm over the head is finished after
-        // the next barrier (the next item's first, or the one after the loop)
         if (t < D) {
+            // readout o = S^T q over the updated state; its norm waits for the next item
             float o = 0.f;
 #pragma unroll
-            for (int r = 0; r < RPP; ++r) o += sm.red[r][t];
+            for (int r = 0; r < RPP; ++r) o += red[r * D + t];
             const float sq = warp_sum(o * o);
             if (lane == 0) sm.ssq_o[warp] = sq;
-            o_prev = o;
+            sm.o_prev[t] = o;
+            sm.zw_prev[t] = sm.wn[t] * rq[3 * D + t];
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.rec_empty[rb]);
         b_prev = b;
         h_prev = h;
-        b = bn;
-        h = hn;
-        hq = hqn;
-        // (red, delta, ssq_* and the other record buffer are next written after
-        // a barrier of the next item)
+        if (++h == p.n_v) {
+            h = 0;
+            ++b;
+        }
+    }
+    if (j == n_items) {  // (uniform) the last item's norm
+        bar_sync(kBarCons, NC);
+        if (t >= D && t < 2 * D) store_norm(p, sm, sm.o_prev[t - D], sm.zw_prev[t - D], b_prev, h_prev, t - D);
+    }
+    return issued;
+}
+
+template <int KC>
+__global__ void __launch_bounds__(NT, 1) dn_core_stream_kernel(const StreamParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    StreamSmem &sm = *reinterpret_cast<StreamSmem *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int i0 = (int)(((unsigned)blockIdx.x * (unsigned)p.items) / gridDim.x);
+    const int i1 = (int)(((unsigned)(blockIdx.x + 1) * (unsigned)p.items) / gridDim.x);
+    const int n_items = i1 - i0;  // >= 1: the grid has at most one CTA per item
+    const int b0 = i0 / p.n_v;
+    const int nseq = (i1 - 1) / p.n_v - b0 + 1;
+
+    if (t == 0) {
+        for (int s = 0; s < STAGES; ++s)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&sm.full[s])));
+        for (int r = 0; r < 2; ++r) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&sm.rec_full[r])), "r"(NPW));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&sm.rec_empty[r])),
+                         "r"(NC / 32));
+        }
+        sm.failed = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        // the state is not written by the in_proj kernel
+        for (int j = 0; j < STAGES && j < n_items; ++j) load_tile(sm, j, p, i0 + j);
+    }
+    // the norm weights and the sequences' ring positions (advanced by the
+    // previous step's last kernel, which has completed)
+    if (t < D) sm.wn[t] = p.w_norm[t];
+    for (int i = t; i < nseq; i += NT) sm.dpos[i] = p.rpos[2 * (b0 + i)];
+    __syncthreads();
+
+    int issued = 0;
+    if (warp < NC / 32) {
+        pdl_wait();  // (consumers read nothing the in_proj writes; the wait keeps completion transitive)
+        if (t == 0) pdl_trigger();
+        issued = consume(p, sm, i0, n_items, b0, t);
+    } else {
+        produce<KC>(p, sm, i0, n_items, b0, warp - NC / 32, lane);
     }
     __syncthreads();
-    if (!failed && n_items > 0 && t < D) store_norm(p, sm, o_prev, b_prev, h_prev, sm.rec[(n_items - 1) & 1] + 3 * D, t);
-    if (t == 0) {
-        if (failed) atomicOr(p.err, 1);
+    if (t == kTma) {
         asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-        // let any load still in flight land before the CTA exits
+        if (sm.failed) atomicOr(p.err, 1);
+        // let any tile copy still in flight land before the CTA exits
         for (int j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j)
             (void)mbar_wait(&sm.full[j % STAGES], (j / STAGES) & 1);
     }
