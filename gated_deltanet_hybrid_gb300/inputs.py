@@ -45,6 +45,12 @@ class DNConfig:
     l2_eps: float = 1e-6
     norm_eps: float = 1e-6
     q_scale: float | None = None  # None: 1/sqrt(dk)
+    key_gate: bool = False        # per-key-channel decay: g is [n_v_heads][dk] per sequence
+
+    @property
+    def gate_width(self) -> int:
+        """Log-decay values per head and step: dk with the per-key gate, else 1."""
+        return self.dk if self.key_gate else 1
 
     @property
     def qscale(self) -> float:
@@ -177,17 +183,21 @@ class WorkloadStream:
             self.states = [zero_state(wl.cfg, wl.batch) for _ in range(wl.layers)]
 
     def next_step(self) -> tuple[np.ndarray, list[tuple[np.ndarray, np.ndarray]]]:
-        """x [B][hidden] f32 and, per layer, (g, beta) each [B][n_v_heads] f32."""
+        """x [B][hidden] f32 and, per layer, (g, beta): g [B][n_v_heads] f32
+        ([B][n_v_heads][dk] with the per-key gate), beta [B][n_v_heads] f32."""
         cfg, B = self.wl.cfg, self.wl.batch
         x = self.rng.standard_normal((B, cfg.hidden)).astype(np.float32)
         gates = []
+        gshape = (B, cfg.n_v_heads, cfg.dk) if cfg.key_gate else (B, cfg.n_v_heads)
         for _ in range(self.wl.layers):
             if self.wl.gate == "softplus":
-                a = self.rng.standard_normal((B, cfg.n_v_heads))
+                a = self.rng.standard_normal(gshape)
                 b = self.rng.standard_normal((B, cfg.n_v_heads))
-                gates.append(gates_from_ab(a, b))
+                g, _ = gates_from_ab(a, a)
+                _, beta = gates_from_ab(b, b)
+                gates.append((g, beta))
             elif self.wl.gate == "decay_band":
-                u = self.rng.uniform(0.9, 1.0, size=(B, cfg.n_v_heads))
+                u = self.rng.uniform(0.9, 1.0, size=gshape)
                 b = self.rng.standard_normal((B, cfg.n_v_heads))
                 g = np.log(u).astype(np.float32)
                 beta = (1.0 / (1.0 + np.exp(-b))).astype(np.float32)

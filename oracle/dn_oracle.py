@@ -30,6 +30,9 @@ notes):
   * L2 norm: x / sqrt(sum x^2 + l2_eps); q is then multiplied by q_scale.
   * gated RMSNorm over one head's dv values, one weight vector shared by all
     heads: o / sqrt(mean(o^2) + norm_eps) * w_norm * silu(z).
+  * the per-key-channel gate of the page's KDA engines (the page says only
+    that their gate differs): one log-decay per key index, scaling row i of
+    S (S <- diag(exp(g)) S), everything else unchanged.
 
 State S[h] is dk x dv (row i = key index, column j = value index), so the
 readout is o[j] = sum_i S[i, j] q[i].
@@ -93,16 +96,20 @@ def normalize_qk(q: np.ndarray, k: np.ndarray, l2_eps: float, q_scale: float) ->
 
 
 def gated_delta_rule_step(S: np.ndarray, q: np.ndarray, k: np.ndarray, v: np.ndarray,
-                          g: float, beta: float) -> tuple[np.ndarray, np.ndarray]:
+                          g, beta: float) -> tuple[np.ndarray, np.ndarray]:
     """One token of the gated delta rule for one value head, in the page's order.
 
-    1. decay:      S <- exp(g) * S
+    1. decay:      S <- exp(g) * S, g a scalar (one gate per head); or, with a
+                   per-key-channel gate g[dk] (the gate of the page's KDA
+                   engines, "Where this goes next"), row i of S (key index i)
+                   is scaled by exp(g[i]): S <- diag(exp(g)) S
     2. delta:      delta = beta * (v - S^T k)   (against the decayed state)
     3. write-back: S <- S + k delta^T
     4. readout:    o = S^T q                     (over the updated state)
     Returns (new S, o).
     """
-    S = np.exp(F64(g)) * S
+    g = np.asarray(g, F64)
+    S = (np.exp(g) * S) if g.ndim == 0 else (np.exp(g)[:, None] * S)
     kv = S.T @ k
     delta = F64(beta) * (v - kv)
     S = S + np.outer(k, delta)
@@ -136,7 +143,8 @@ class OracleLayer:
         self.ring_pos = np.array(state.ring_pos, dtype=np.int64, copy=True)
 
     def step(self, x: np.ndarray, g: np.ndarray, beta: np.ndarray, trace: dict | None = None) -> np.ndarray:
-        """x [B][hidden], g/beta [B][n_v_heads] -> out [B][hidden] (float64).
+        """x [B][hidden], g [B][n_v_heads] (or [B][n_v_heads][dk] with the
+        per-key gate), beta [B][n_v_heads] -> out [B][hidden] (float64).
 
         If ``trace`` is a dict it receives the intermediates: "y" (in_proj
         output), "u" (conv+SiLU output), "o" (readout per head) and "normed".

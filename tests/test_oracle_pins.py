@@ -217,6 +217,73 @@ def test_readout_uses_updated_state():
     assert np.allclose(o, v, atol=1e-14)
 
 
+def test_key_gate_handworked_head():
+    """Per-key-channel decay scales the rows of S (key index), worked by hand
+    in tests/golden/handworked_key_gate.txt."""
+    gv = _golden_file("handworked_key_gate.txt")
+    S, o = gated_delta_rule_step(gv["S0"].reshape(2, 2), l2_normalize(gv["q"], 0.0),
+                                 l2_normalize(gv["k"], 0.0), gv["v"], np.log(gv["decay"]), gv["beta"][0])
+    assert np.allclose(S.reshape(-1), gv["S"], rtol=0, atol=1e-15)
+    assert np.allclose(o, gv["o"], rtol=0, atol=1e-15)
+
+
+def test_key_gate_uniform_equals_scalar_gate():
+    """A per-key gate with every entry c is the per-head gate c, bitwise."""
+    rng = np.random.default_rng(12)
+    S = rng.standard_normal((16, 8))
+    q = l2_normalize(rng.standard_normal(16), 1e-6)
+    k = l2_normalize(rng.standard_normal(16), 1e-6)
+    v = rng.standard_normal(8)
+    a = gated_delta_rule_step(S, q, k, v, -0.37, 0.6)
+    b = gated_delta_rule_step(S, q, k, v, np.full(16, -0.37), 0.6)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_key_gate_recurrence_against_unrolled_products():
+    """Brute force with A_t = (I - beta_t k_t k_t^T) diag(exp(g_t)):
+    S_T = A_T ... A_1 S_0 + sum_s A_T ... A_{s+1} beta_s k_s v_s^T."""
+    rng = np.random.default_rng(13)
+    dk, dv, T = 24, 16, 48
+    S0 = rng.standard_normal((dk, dv)) * 0.1
+    ks = [l2_normalize(rng.standard_normal(dk), 1e-6) for _ in range(T)]
+    qs = [l2_normalize(rng.standard_normal(dk), 1e-6) for _ in range(T)]
+    vs = [rng.standard_normal(dv) for _ in range(T)]
+    gs = -0.5 * np.log1p(np.exp(rng.standard_normal((T, dk))))
+    bs = expit(rng.standard_normal(T))
+    A = [(np.eye(dk) - bs[t] * np.outer(ks[t], ks[t])) @ np.diag(np.exp(gs[t])) for t in range(T)]
+    S = S0.copy()
+    for t in range(T):
+        S, o = gated_delta_rule_step(S, qs[t], ks[t], vs[t], gs[t], bs[t])
+        P = np.eye(dk)
+        brute = np.zeros((dk, dv))
+        for s in range(t, -1, -1):
+            brute = brute + P @ (bs[s] * np.outer(ks[s], vs[s]))
+            P = P @ A[s]
+        brute = brute + P @ S0
+        assert np.allclose(S, brute, rtol=0, atol=1e-12 * max(1.0, np.abs(brute).max()))
+        assert np.allclose(o, brute.T @ qs[t], rtol=0, atol=1e-12)
+
+
+def test_key_gate_layer_uses_each_heads_vector():
+    """In a whole layer the per-key gate of (sequence b, head h) reaches that
+    head only: zeroing g for one head (decay 1) with beta = 0 leaves exactly
+    that head's state unchanged."""
+    cfg = DNConfig(hidden=24, n_qk_heads=2, n_v_heads=4, dk=4, dv=4, key_gate=True)
+    w = make_weights(cfg, np.random.default_rng(0))
+    rng = np.random.default_rng(3)
+    st = DNState(S=rng.standard_normal((2, 4, 4, 4)), ring=np.zeros((2, 3, cfg.conv_ch)),
+                 ring_pos=np.zeros(2, np.int32))
+    layer = OracleLayer(cfg, w, st)
+    g = -rng.uniform(0.1, 1.0, (2, 4, 4))
+    g[1, 2] = 0.0
+    layer.step(rng.standard_normal((2, cfg.hidden)), g, np.zeros((2, 4)))
+    for b in range(2):
+        for h in range(4):
+            want = st.S[b, h] * np.exp(g[b, h])[:, None]
+            assert np.allclose(layer.S[b, h], want, rtol=1e-15, atol=0)
+    assert np.array_equal(layer.S[1, 2], st.S[1, 2])
+
+
 # ---------------------------------------------------------------- gated RMSNorm
 def test_gated_rmsnorm_invariants():
     rng = np.random.default_rng(6)
@@ -233,6 +300,10 @@ def test_gated_rmsnorm_invariants():
     # constant head: every entry normalises to sign(o) (times w * silu(z))
     c = gated_rmsnorm(np.full(4, -2.0), np.full(4, 60.0), np.ones(4), 0.0)
     assert np.allclose(c, -60.0, rtol=1e-14)
+
+
+def _golden_file(name):
+    return _golden(name)
 
 
 def _golden(name):
