@@ -21,6 +21,7 @@ DN_EFAILED = -4
 DN_EINJECTED = -5
 DN_PTR_HOST = 0
 DN_PTR_DEVICE = 1
+DN_FLAG_KEY_GATE = 1
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdn.so")
 
@@ -41,7 +42,7 @@ class dn_config(ctypes.Structure):
                 ("n_v_heads", ctypes.c_int32), ("dk", ctypes.c_int32), ("dv", ctypes.c_int32),
                 ("conv_k", ctypes.c_int32), ("max_batch", ctypes.c_int32),
                 ("l2_eps", ctypes.c_float), ("norm_eps", ctypes.c_float),
-                ("q_scale", ctypes.c_float)]
+                ("q_scale", ctypes.c_float), ("flags", ctypes.c_int32)]
 
 
 class dn_weights(ctypes.Structure):
@@ -147,7 +148,8 @@ def dn_create(cfg, weights, max_batch: int, stream=None, check: bool = True):
     Returns the layer handle (ctypes.c_void_p)."""
     lib = load_library()
     c = dn_config(cfg.hidden, cfg.n_qk_heads, cfg.n_v_heads, cfg.dk, cfg.dv, cfg.conv_k,
-                  int(max_batch), cfg.l2_eps, cfg.norm_eps, cfg.qscale)
+                  int(max_batch), cfg.l2_eps, cfg.norm_eps, cfg.qscale,
+                  DN_FLAG_KEY_GATE if getattr(cfg, "key_gate", False) else 0)
     arrs = [np.ascontiguousarray(weights.w_in, np.int8), np.ascontiguousarray(weights.s_in, np.float32),
             np.ascontiguousarray(weights.w_conv, np.float32), np.ascontiguousarray(weights.w_norm, np.float32),
             np.ascontiguousarray(weights.w_out, np.int8), np.ascontiguousarray(weights.s_out, np.float32)]

@@ -64,8 +64,9 @@ bool valid_cfg(const dn_config *c) {
     if (c->hidden < 16 || c->hidden > 16384 || c->hidden % 16 != 0) return false;
     if (c->n_qk_heads < 1 || c->n_v_heads < 1 || c->n_v_heads > 64) return false;
     if (c->n_v_heads % c->n_qk_heads != 0) return false;
-    if (!(c->dk == 32 || c->dk == 64 || c->dk == 128)) return false;
-    if (!(c->dv == 32 || c->dv == 64 || c->dv == 128)) return false;
+    if (!(c->dk == 32 || c->dk == 64 || c->dk == 128 || c->dk == 256)) return false;
+    if (!(c->dv == 32 || c->dv == 64 || c->dv == 128 || c->dv == 256)) return false;
+    if (c->flags != 0 && c->flags != DN_FLAG_KEY_GATE) return false;
     if (c->conv_k < 2 || c->conv_k > 8) return false;
     if (c->max_batch < 1 || c->max_batch > 1024) return false;
     if (!(c->l2_eps > 0.f) || !(c->norm_eps > 0.f)) return false;
@@ -175,6 +176,7 @@ DN_API int dn_create(const dn_config *cfg, const dn_weights *w, void *stream, dn
     d.l2_eps = cfg->l2_eps;
     d.norm_eps = cfg->norm_eps;
     d.q_scale = cfg->q_scale;
+    d.gw = (cfg->flags & DN_FLAG_KEY_GATE) ? d.dk : 1;
     l->stream = (cudaStream_t)stream;
     cudaGetDevice(&l->device);
 
@@ -199,7 +201,7 @@ DN_API int dn_create(const dn_config *cfg, const dn_weights *w, void *stream, dn
     ALLOC(L.rpos, MB * 2 * 4);
     ALLOC(L.nrm, MB * d.v_dim * 4);
     ALLOC(L.x_stage, MB * d.hidden * 4);
-    ALLOC(L.g_stage, MB * d.n_v * 4);
+    ALLOC(L.g_stage, MB * d.n_v * d.gw * 4);
     ALLOC(L.beta_stage, MB * d.n_v * 4);
     ALLOC(L.out_stage, MB * d.hidden * 4);
     ALLOC(L.ring_stage, MB * (d.conv_k - 1) * d.conv_ch * 4);
@@ -327,7 +329,7 @@ DN_API int dn_stack_step(dn_layer *const *layers, int n_layers, int batch, float
     for (int l = 0; l < n_layers; ++l) {
         const dn_layer *L = layers[l];
         if (L == nullptr || L->device != first->device) return DN_EINVAL;
-        if (L->d.hidden != d0.hidden || L->d.n_v != d0.n_v) return DN_EINVAL;
+        if (L->d.hidden != d0.hidden || L->d.n_v != d0.n_v || L->d.gw != d0.gw) return DN_EINVAL;
         if (batch < 1 || batch > L->d.max_batch) return DN_EINVAL;
         if (L->failed) return DN_EFAILED;
     }
@@ -337,11 +339,11 @@ DN_API int dn_stack_step(dn_layer *const *layers, int n_layers, int batch, float
     // the first layer's staging buffers hold the normalised input and the
     // layer output (dn_step with device pointers does not touch them)
     float *xn = first->L.x_stage, *y = first->L.out_stage;
-    const size_t gstride = (size_t)batch * d0.n_v;
+    const size_t gstride = (size_t)batch * d0.n_v;  // beta; g has gw values per head
     if (dn::launch_residual_prenorm(h, nullptr, xn, batch, d0.hidden, eps, st) != cudaSuccess)
         return cuda_fail(first);
     for (int l = 0; l < n_layers; ++l) {
-        const int rc = dn_step(layers[l], batch, xn, g + l * gstride, beta + l * gstride, y, DN_PTR_DEVICE, st);
+        const int rc = dn_step(layers[l], batch, xn, g + l * gstride * d0.gw, beta + l * gstride, y, DN_PTR_DEVICE, st);
         if (rc != DN_OK) return rc;
         // h += y and the next layer's input (after the last layer: only the add matters)
         if (dn::launch_residual_prenorm(h, y, xn, batch, d0.hidden, eps, st) != cudaSuccess)
@@ -433,7 +435,7 @@ DN_API int dn_step(dn_layer *l, int batch, const float *x, const float *g, const
     float *od = out;
     if (ptr_kind == DN_PTR_HOST) {
         DN_TRY(l, cudaMemcpyAsync(L.x_stage, x, (size_t)batch * d.hidden * 4, cudaMemcpyHostToDevice, st));
-        DN_TRY(l, cudaMemcpyAsync(L.g_stage, g, (size_t)batch * d.n_v * 4, cudaMemcpyHostToDevice, st));
+        DN_TRY(l, cudaMemcpyAsync(L.g_stage, g, (size_t)batch * d.n_v * d.gw * 4, cudaMemcpyHostToDevice, st));
         DN_TRY(l, cudaMemcpyAsync(L.beta_stage, beta, (size_t)batch * d.n_v * 4, cudaMemcpyHostToDevice, st));
         xd = L.x_stage;
         gd = L.g_stage;

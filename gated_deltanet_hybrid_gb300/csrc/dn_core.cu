@@ -48,6 +48,7 @@ struct CoreParams {
     const float *g;        // [B][n_v]
     const float *beta;     // [B][n_v]
     int n_qk, n_v, dv, conv_k, conv_ch, qk_dim, in_rows, v_dim, kt_out;
+    int gw;                // log-decay values per head: 1, or dk (per-key-channel gate)
     float l2_eps, norm_eps, q_scale;
 };
 
@@ -77,6 +78,7 @@ __global__ void __launch_bounds__(kThreads, 2) dn_core_kernel(const CoreParams p
     __shared__ __align__(16) float v_s[DJ];
     __shared__ __align__(16) float delta_s[DJ];
     __shared__ __align__(16) float red[RPP][DJ];
+    __shared__ __align__(16) float eg_s[DK];  // exp(log-decay) of each key row
     __shared__ float inv_s[2];
     __shared__ float ssq_s;
 
@@ -152,15 +154,17 @@ __global__ void __launch_bounds__(kThreads, 2) dn_core_kernel(const CoreParams p
         else
             k_s[i - DK] = k_s[i - DK] * inv_s[1];
     }
+    // the decay of each key row: one gate per head, or one per key channel
+    for (int i = tid; i < DK; i += kThreads)
+        eg_s[i] = expf(p.gw == 1 ? p.g[b * p.n_v + h] : p.g[((size_t)b * p.n_v + h) * DK + i]);
     __syncthreads();
 
     // ---- 4. decay, then what the decayed state predicts for k ----------------
-    const float eg = expf(p.g[b * p.n_v + h]);
     const float bt = p.beta[b * p.n_v + h];
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
-        const float kr = k_s[r0 + i * RPP];
+        const float kr = k_s[r0 + i * RPP], eg = eg_s[r0 + i * RPP];
         s[i].x *= eg;
         s[i].y *= eg;
         s[i].z *= eg;
@@ -273,6 +277,10 @@ cudaError_t launch_core(const CoreParams &cp, int js, int n_v, int B, cudaStream
     return cudaLaunchKernelEx(&cfg, dn_core_kernel<DK, DJ, false>, cp);
 }
 
+// Widest slice a dk allows: a block's tile (dk x DJ floats over 256 threads)
+// stays at 64 registers per thread.
+constexpr int max_dj_of(int dk) { return dk >= 256 ? 64 : 128; }
+
 template <int DK>
 cudaError_t dispatch_dj(const CoreParams &cp, int dj, int js, int n_v, int B, cudaStream_t st) {
     switch (dj) {
@@ -283,7 +291,9 @@ cudaError_t dispatch_dj(const CoreParams &cp, int dj, int js, int n_v, int B, cu
             if constexpr (1024 / 32 <= DK) return launch_core<DK, 32>(cp, js, n_v, B, st);
             break;
         case 64: return launch_core<DK, 64>(cp, js, n_v, B, st);
-        case 128: return launch_core<DK, 128>(cp, js, n_v, B, st);
+        case 128:
+            if constexpr (max_dj_of(DK) >= 128) return launch_core<DK, 128>(cp, js, n_v, B, st);
+            break;
         default: break;
     }
     return cudaErrorInvalidValue;
@@ -300,10 +310,12 @@ int min_dj(int dk) {
 }  // namespace
 
 // Column slices per head: enough blocks to cover every SM at least once when
-// the batch is small, at most 8 (a portable cluster) and at least 16 columns.
+// the batch is small, at most 8 (a portable cluster), at least 16 columns and
+// at most max_dj_of(dk) columns each.
 int choose_js(const Dims &d, int B) {
     const int sms = num_sms();
     int js = 1;
+    while (d.dv / js > max_dj_of(d.dk)) js *= 2;
     const int max_js = d.dv / min_dj(d.dk);
     while (js < 8 && js * 2 <= max_js && (long)B * d.n_v * js < sms) js *= 2;
     return js;
@@ -340,12 +352,14 @@ cudaError_t launch_dn_core(const Dims &d, const LayerDev &L, int B, const float 
     cp.l2_eps = d.l2_eps;
     cp.norm_eps = d.norm_eps;
     cp.q_scale = d.q_scale;
+    cp.gw = d.gw;
     const int js = choose_js(d, B);
     const int dj = d.dv / js;
     switch (d.dk) {
         case 32: return dispatch_dj<32>(cp, dj, js, d.n_v, B, st);
         case 64: return dispatch_dj<64>(cp, dj, js, d.n_v, B, st);
         case 128: return dispatch_dj<128>(cp, dj, js, d.n_v, B, st);
+        case 256: return dispatch_dj<256>(cp, dj, js, d.n_v, B, st);
         default: return cudaErrorInvalidValue;
     }
 }

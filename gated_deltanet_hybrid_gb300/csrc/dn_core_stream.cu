@@ -23,7 +23,8 @@
 //    times the row scale), then the conv over the ring (K-1 history slots
 //    read, the newest written by the row's owner) and SiLU for q, k, v, SiLU
 //    for z, the q/k L2 norms (one warp's fp32 shuffle sum, fixed order), the
-//    query scale and the gates.  The second value head of a q/k head reuses
+//    query scale, the write strength and the decay of each key row (one
+//    gate per head, or one per key channel).  The second value head of a q/k head reuses
 //    the first one's q^ and k^.  Producers and consumers meet on two
 //    mbarriers per record buffer (full, empty).  The loads of item j+1 are
 //    issued as soon as item j's rows are computed;
@@ -83,15 +84,17 @@ struct StreamParams {
     int *err;
     int MT, max_seg;       // in_proj row tiles and segment slots per tile
     int n_v, group, conv_ch, qk_dim, v_dim, kt_out, items;
+    int gw;                // log-decay values per head: 1, or 128 (per-key-channel gate)
     float l2_eps, q_scale, norm_eps;
 };
 
 struct __align__(128) StreamSmem {
     float tile[STAGES][D * D];  // 3 x 64 KB
-    float rec[2][4 * D];        // the item's q^ | k^ | v | silu(z), double-buffered
-    float gate[2][2];           // exp(g), beta
-    float red[2][RPP][D];       // 2 x 8 KB: per-pass partial sums (kv, then readout)
-    float delta[D];
+    // (arrays read or written with 16-byte accesses are 16-byte aligned)
+    alignas(16) float rec[2][5 * D];   // the item's q^ | k^ | v | silu(z) | exp(g) per key row, double-buffered
+    alignas(16) float red[2][RPP][D];  // 2 x 8 KB: per-pass partial sums (kv, then readout)
+    alignas(16) float delta[D];
+    float beta[2];
     float ssq_o[4];             // readout warp sums of squares
     float o_prev[D];            // the last item's readout, normalised during the next item
     float zw_prev[D];           // its w_norm * silu(z)
@@ -307,6 +310,16 @@ __device__ __forceinline__ void store_norm(const StreamParams &p, const StreamSm
     }
 }
 
+// The log-decays of key rows cl .. cl+3 of `item`: one per head (repeated),
+// or one per key channel
+__device__ __forceinline__ float4 load_gate(const StreamParams &p, int item, int cl) {
+    if (p.gw == 1) {
+        const float g = ld_cg(p.g + item);
+        return make_float4(g, g, g, g);
+    }
+    return ld_cg4(p.g + (size_t)item * D + cl);
+}
+
 // Producer warps: build the record (q^, k^, v, silu(z), gates) of every item
 // of the CTA's range, one item ahead of the consumers.  Warp `kind` builds
 // one row kind (0 q, 1 k, 2 v, 3 z), lane l channels 4l .. 4l+3 of the head,
@@ -320,14 +333,13 @@ __device__ void produce(const StreamParams &p, StreamSmem &sm, int i0, int n_ite
     const int base = kind == 0 ? 0 : kind == 1 ? p.qk_dim : kind == 2 ? 2 * p.qk_dim : p.conv_ch;
     int b = b0, h = i0 - b0 * p.n_v, hq = h / p.group;
     RowLoads<KC> r;
-    float gv = 0.f, bv = 0.f;
+    float bv = 0.f;
+    float4 gv = make_float4(0.f, 0.f, 0.f, 0.f);  // (warp 3) the item's log-decays of key rows cl .. cl+3
     // the first item's loads that the in_proj does not feed go out before the wait
     int c = base + (qk ? hq : h) * D + cl;
     load_row_fixed(p, sm, b0, b, c, conv, r);
-    if (kind == 0 && lane == 0) {
-        gv = ld_cg(p.g + i0);
-        bv = ld_cg(p.beta + i0);
-    }
+    if (kind == 0 && lane == 0) bv = ld_cg(p.beta + i0);
+    if (kind == 3) gv = load_gate(p, i0, cl);
     pdl_wait();
     load_row_part(p, b, c, r);
     bool reuse = false;  // item j has the q/k head of item j-1
@@ -344,7 +356,8 @@ __device__ void produce(const StreamParams &p, StreamSmem &sm, int i0, int n_ite
                 u = make_float4(silu_f(xv.x), silu_f(xv.y), silu_f(xv.z), silu_f(xv.w));
             }
         }
-        const float gj = gv, bj = bv;
+        const float4 gj = gv;
+        const float bj = bv;
         // item j+1 and its loads
         const int bn = h + 1 == p.n_v ? b + 1 : b, hn = h + 1 == p.n_v ? 0 : h + 1, hqn = hn / p.group;
         const bool reuse_n = bn == b && hqn == hq;
@@ -354,10 +367,8 @@ __device__ void produce(const StreamParams &p, StreamSmem &sm, int i0, int n_ite
                 load_row_fixed(p, sm, b0, bn, cn, conv, r);
                 load_row_part(p, bn, cn, r);
             }
-            if (kind == 0 && lane == 0) {
-                gv = ld_cg(p.g + i0 + j + 1);
-                bv = ld_cg(p.beta + i0 + j + 1);
-            }
+            if (kind == 0 && lane == 0) bv = ld_cg(p.beta + i0 + j + 1);
+            if (kind == 3) gv = load_gate(p, i0 + j + 1, cl);
         }
         float4 outv = u;
         if (qk) {
@@ -375,10 +386,10 @@ __device__ void produce(const StreamParams &p, StreamSmem &sm, int i0, int n_ite
             break;
         }
         *reinterpret_cast<float4 *>(&sm.rec[rb][kind * D + cl]) = outv;
-        if (kind == 0 && lane == 0) {
-            sm.gate[rb][0] = expf(gj);
-            sm.gate[rb][1] = bj;
-        }
+        if (kind == 0 && lane == 0) sm.beta[rb] = bj;
+        if (kind == 3)
+            *reinterpret_cast<float4 *>(&sm.rec[rb][4 * D + cl]) =
+                make_float4(expf(gj.x), expf(gj.y), expf(gj.z), expf(gj.w));
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.rec_full[rb]);  // release: the record's writes come first
         b = bn;
@@ -409,14 +420,15 @@ __device__ int consume(const StreamParams &p, StreamSmem &sm, int i0, int n_item
         for (int i = 0; i < NP; ++i) s[i] = *reinterpret_cast<const float4 *>(tile + (r0 + i * RPP) * D + c4 * 4);
         ok = ok && mbar_wait(&sm.rec_full[rb], (j >> 1) & 1);
         const float *rq = sm.rec[rb], *rk = rq + D, *rv = rq + 2 * D;
-        const float eg = sm.gate[rb][0], bt = sm.gate[rb][1];
+        const float bt = sm.beta[rb];
+        const float *reg = rq + 4 * D;  // exp(g) of each key row
         float *red = &sm.red[rb][0][0];
 
         // decay, then what the decayed state predicts for k
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < NP; ++i) {
-            const float kr = rk[r0 + i * RPP];
+            const float kr = rk[r0 + i * RPP], eg = reg[r0 + i * RPP];
             s[i].x *= eg;
             s[i].y *= eg;
             s[i].z *= eg;
@@ -606,6 +618,7 @@ cudaError_t launch_dn_core_stream(const Dims &d, const LayerDev &L, int B, const
     p.l2_eps = d.l2_eps;
     p.q_scale = d.q_scale;
     p.norm_eps = d.norm_eps;
+    p.gw = d.gw;
     switch (d.conv_k) {
         case 2: return launch_kc<2>(p, st);
         case 3: return launch_kc<3>(p, st);

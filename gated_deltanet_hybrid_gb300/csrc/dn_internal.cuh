@@ -29,6 +29,7 @@ namespace dn {
 struct Dims {
     int hidden, n_qk, n_v, dk, dv, conv_k, max_batch;
     int qk_dim, v_dim, conv_ch, in_rows;
+    int gw;  // log-decay values per head and step: dk with the per-key gate, else 1
     float l2_eps, norm_eps, q_scale;
 };
 

@@ -45,6 +45,12 @@ extern "C" {
 #define DN_EFAILED   -4  /* the layer failed earlier; only get_state/destroy work */
 #define DN_EINJECTED -5  /* failure injected with dn_debug_fail_next */
 
+/* ---- dn_config.flags ----------------------------------------------------- */
+/* per-key-channel decay: g carries one log-decay per key index of each head
+ * (g[b][h][i] scales row i of that head's state), the gate of the page's
+ * KDA engines; without it one log-decay per head scales the whole state */
+#define DN_FLAG_KEY_GATE 1
+
 /* ---- where a pointer argument lives ------------------------------------ */
 #define DN_PTR_HOST   0
 #define DN_PTR_DEVICE 1
@@ -58,18 +64,20 @@ typedef struct dn_layer dn_layer; /* opaque; owns all of its device memory */
  * This build accepts:
  *   hidden      multiple of 16, 16 .. 16384
  *   n_qk_heads  >= 1, divides n_v_heads; n_v_heads <= 64
- *   dk, dv      each one of 32, 64, 128
+ *   dk, dv      each one of 32, 64, 128, 256
  *   conv_k      2 .. 8 (taps of the causal short conv; the ring keeps conv_k-1)
  *   max_batch   1 .. 1024 (sequences the layer holds state for)
  *   l2_eps      eps inside the square root of the q/k L2 norms (> 0)
  *   norm_eps    eps of the gated RMSNorm (> 0)
  *   q_scale     multiplies the normalised q (e.g. 1/sqrt(dk))
+ *   flags       0 or DN_FLAG_KEY_GATE
  * Derived: conv_ch = 2*n_qk_heads*dk + n_v_heads*dv,
  *          in_rows = conv_ch + n_v_heads*dv, v_dim = n_v_heads*dv.
  */
 typedef struct dn_config {
     int32_t hidden, n_qk_heads, n_v_heads, dk, dv, conv_k, max_batch;
     float l2_eps, norm_eps, q_scale;
+    int32_t flags;
 } dn_config;
 
 /*
@@ -145,7 +153,9 @@ int dn_get_state(dn_layer *layer, int seq0, int n, float *S, float *ring, int32_
  * against the decayed state, the write-back, out = q^T S over the updated
  * state, the gated RMSNorm with silu(z), out_proj GEMV):
  *   x    [batch][hidden]     layer input
- *   g    [batch][n_v_heads]  log-decay per head (the state is scaled by exp(g))
+ *   g    [batch][n_v_heads]  log-decay per head (the state is scaled by exp(g));
+ *        [batch][n_v_heads][dk] with DN_FLAG_KEY_GATE (row i of a head's
+ *        state is scaled by exp(g[b][h][i]))
  *   beta [batch][n_v_heads]  write strength per head
  *   out  [batch][hidden]     layer output (written)
  * ptr_kind DN_PTR_DEVICE: all four are device pointers; the call only
@@ -180,7 +190,8 @@ void dn_destroy(dn_layer *layer);
  *   layers  n_layers layer handles with equal hidden and n_v_heads, on the
  *           current device, each with max_batch >= batch
  *   h       [batch][hidden] device, read and overwritten
- *   g, beta [n_layers][batch][n_v_heads] device, each layer's gates
+ *   g, beta [n_layers][batch][n_v_heads] device, each layer's gates (g has a
+ *           trailing [dk] with DN_FLAG_KEY_GATE; all layers then share it)
  * Device pointers only; the call enqueues on `stream` (NULL: the first
  * layer's stream) and uses the first layer's staging buffers for the
  * normalised input and each layer's output.  Errors: DN_EINVAL (NULL, bad

@@ -91,8 +91,9 @@ def run_parity(wl: Workload, steps: int | None = None, sample=None, checkpoints=
     ora = OracleLayer(wl.cfg, w, DNState(s0.S[sample], s0.ring[sample], s0.ring_pos[sample]))
     dev = torch.device("cuda")
     x_d = torch.empty((B, wl.cfg.hidden), dtype=torch.float32, device=dev)
-    g_d = torch.empty((B, wl.cfg.n_v_heads), dtype=torch.float32, device=dev)
-    b_d = torch.empty_like(g_d)
+    gshape = (B, wl.cfg.n_v_heads, wl.cfg.dk) if getattr(wl.cfg, "key_gate", False) else (B, wl.cfg.n_v_heads)
+    g_d = torch.empty(gshape, dtype=torch.float32, device=dev)
+    b_d = torch.empty((B, wl.cfg.n_v_heads), dtype=torch.float32, device=dev)
     out_d = torch.empty_like(x_d)
     worst = {"out": 0.0, "S": 0.0, "ring": 0.0, "elementwise_out": 0.0, "ring_pos_equal": True}
     try:

@@ -137,3 +137,54 @@ def test_in_proj_exact_integer_case(batch):
         assert np.all(st.ring_pos == 1)
     finally:
         layer.destroy()
+
+
+# ---- other dimensions and gates of the same step (48 value heads, head sizes
+#      up to 256, the per-key-channel gate of the page's KDA engines) --------
+SHAPE_48V = DNConfig(hidden=2048, n_qk_heads=16, n_v_heads=48, dk=128, dv=128)
+
+
+@pytest.mark.parametrize("batch", [1, 8, 64])
+def test_48_value_heads(batch):
+    """Three value heads per q/k head (16 q/k heads, 48 value heads of 128):
+    the CUDA-core and the tensor-core projections (in_proj 2048 -> 16384,
+    out_proj 6144 -> 2048) and the streaming state kernel."""
+    wl = custom_workload(f"v48_b{batch}", SHAPE_48V, batch=batch, steps=16, seed=480 + batch, init_std=0.02)
+    _assert_ok(run_parity(wl, sample=np.array(sorted({0, batch // 2, batch - 1}))))
+
+
+@pytest.mark.parametrize("dims", [
+    dict(hidden=512, n_qk_heads=2, n_v_heads=4, dk=256, dv=256),
+    dict(hidden=256, n_qk_heads=1, n_v_heads=2, dk=256, dv=128, conv_k=3),
+    dict(hidden=256, n_qk_heads=2, n_v_heads=2, dk=128, dv=256, conv_k=2),
+    dict(hidden=128, n_qk_heads=1, n_v_heads=3, dk=32, dv=256),
+    dict(hidden=256, n_qk_heads=2, n_v_heads=4, dk=256, dv=32),
+])
+@pytest.mark.parametrize("batch", [1, 3, 16])
+def test_head_sizes_up_to_256(dims, batch):
+    cfg = DNConfig(**dims)
+    wl = custom_workload("d256", cfg, batch=batch, steps=16, seed=256 + batch, init_std=0.05)
+    _assert_ok(run_parity(wl, sample=np.array(sorted({0, batch - 1}))))
+
+
+@pytest.mark.parametrize("dims,batch", [
+    (dict(hidden=256, n_qk_heads=2, n_v_heads=4, dk=32, dv=32), 3),
+    (dict(hidden=512, n_qk_heads=2, n_v_heads=4, dk=256, dv=128), 9),
+    (dict(hidden=2048, n_qk_heads=16, n_v_heads=32, dk=128, dv=128), 1),
+    (dict(hidden=2048, n_qk_heads=16, n_v_heads=32, dk=128, dv=128), 64),
+])
+def test_key_gate(dims, batch):
+    """The per-key-channel gate on the generic state kernel (32 and 256-wide
+    keys) and on the streaming one (128 x 128 heads, batch 1 and 64)."""
+    cfg = DNConfig(key_gate=True, **dims)
+    wl = custom_workload("kgate", cfg, batch=batch, steps=24, seed=700 + batch, init_std=0.02)
+    _assert_ok(run_parity(wl, sample=np.array(sorted({0, batch - 1}))))
+
+
+def test_key_gate_35b_batch16_256_steps():
+    """A per-key-gate workload of the 35B-shape layer at batch 16 over 256
+    steps (exp(g) per key row in [0.9, 1], so the state keeps a long memory),
+    with the state and ring compared at steps 64 and 256."""
+    cfg = DNConfig(hidden=2048, n_qk_heads=16, n_v_heads=32, dk=128, dv=128, key_gate=True)
+    wl = custom_workload("kgate_35b_b16", cfg, batch=16, steps=256, seed=716, init_std=0.02, gate="decay_band")
+    _assert_ok(run_parity(wl, sample=np.array([0, 15]), checkpoints=(64, 256)))

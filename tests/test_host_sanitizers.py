@@ -50,10 +50,11 @@ for code in (0, -1, -2, -3, -4, -5, 7, -2**31, 2**31 - 1):
     assert len(lib.dn_strerror(code)) > 0
 
 # invalid configurations: one field at a time, extreme values included
-base = dict(hidden=256, qk=2, v=4, dk=32, dv=32, conv_k=4, max_batch=2, l2=1e-6, ne=1e-6, qs=1.0)
+base = dict(hidden=256, qk=2, v=4, dk=32, dv=32, conv_k=4, max_batch=2, l2=1e-6, ne=1e-6, qs=1.0, fl=0)
 bad = {"hidden": [0, 8, 250, 16400, -16, 2**31 - 1, -2**31],
        "qk": [0, -1, 3, 2**31 - 1, -2**31], "v": [0, 65, -4, 2**31 - 1, -2**31],
-       "dk": [0, 16, 48, 256, -32, 2**31 - 1], "dv": [0, 16, 96, 256, -2**31],
+       "dk": [0, 16, 48, 512, -32, 2**31 - 1], "dv": [0, 16, 96, 512, -2**31],
+       "fl": [2, 3, -1, 2**31 - 1],
        "conv_k": [0, 1, 9, -4, 2**31 - 1], "max_batch": [0, 1025, -1, 2**31 - 1, -2**31],
        "l2": [0.0, -1e-6, math.nan, -math.inf], "ne": [0.0, -1.0, math.nan],
        "qs": [math.nan]}
@@ -64,7 +65,7 @@ for field, values in bad.items():
     for val in values:
         c = dict(base, **{field: val})
         cfg = abi.dn_config(c["hidden"], c["qk"], c["v"], c["dk"], c["dv"], c["conv_k"], c["max_batch"],
-                            c["l2"], c["ne"], c["qs"])
+                            c["l2"], c["ne"], c["qs"], c["fl"])
         assert lib.dn_create(ctypes.byref(cfg), ctypes.byref(w), None, ctypes.byref(h)) == E, (field, val)
         assert h.value is None
         n += 1
