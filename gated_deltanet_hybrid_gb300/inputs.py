@@ -46,6 +46,7 @@ class DNConfig:
     norm_eps: float = 1e-6
     q_scale: float | None = None  # None: 1/sqrt(dk)
     key_gate: bool = False        # per-key-channel decay: g is [n_v_heads][dk] per sequence
+    device_gates: bool = False    # the a/b gate projections are int8 rows of the layer (no host gates)
 
     @property
     def gate_width(self) -> int:
@@ -72,6 +73,12 @@ class DNConfig:
     def in_rows(self) -> int:
         return self.conv_ch + self.v_dim
 
+    @property
+    def gate_rows(self) -> int:
+        """Rows of the a/b gate projections: n_v_heads * gate_width for a,
+        n_v_heads for b (0 when the gates come from the caller)."""
+        return self.n_v_heads * (self.gate_width + 1) if self.device_gates else 0
+
 
 TINY = DNConfig(hidden=256, n_qk_heads=2, n_v_heads=4, dk=32, dv=32)
 SHAPE_35B = DNConfig(hidden=2048, n_qk_heads=16, n_v_heads=32, dk=128, dv=128)
@@ -85,6 +92,12 @@ class DNWeights:
     w_norm: np.ndarray  # f32   [dv]
     w_out: np.ndarray   # int8  [hidden][v_dim]
     s_out: np.ndarray   # f32   [hidden]
+    # device gates only: the a rows (n_v_heads * gate_width) then the b rows
+    # (n_v_heads) of the gate projections, their row scales, and the decay
+    # coefficient A of each head (g = -A * softplus(a), beta = sigmoid(b))
+    w_ab: np.ndarray | None = None     # int8 [gate_rows][hidden]
+    s_ab: np.ndarray | None = None     # f32  [gate_rows]
+    gate_A: np.ndarray | None = None   # f32  [n_v_heads]
 
 
 @dataclasses.dataclass
@@ -101,7 +114,16 @@ def make_weights(cfg: DNConfig, rng: np.random.Generator) -> DNWeights:
     w_norm = rng.uniform(0.5, 1.5, size=cfg.dv).astype(np.float32)
     w_out = rng.integers(-127, 128, size=(cfg.hidden, cfg.v_dim), dtype=np.int8)
     s_out = rng.uniform(0.001, 0.01, size=cfg.hidden).astype(np.float32)
-    return DNWeights(w_in, s_in, w_conv, w_norm, w_out, s_out)
+    w = DNWeights(w_in, s_in, w_conv, w_norm, w_out, s_out)
+    if cfg.device_gates:
+        # drawn last, so layers without device gates keep their draws; the row
+        # scales put a and b near N(0, 1) for x ~ N(0, 1) (int8 uniform in
+        # [-127, 127] has standard deviation 73.3), as the configs' a, b are;
+        # A = 0.5, the configs' coefficient
+        w.w_ab = rng.integers(-127, 128, size=(cfg.gate_rows, cfg.hidden), dtype=np.int8)
+        w.s_ab = (rng.uniform(0.5, 1.5, size=cfg.gate_rows) / (73.3 * math.sqrt(cfg.hidden))).astype(np.float32)
+        w.gate_A = np.full(cfg.n_v_heads, 0.5, np.float32)
+    return w
 
 
 def zero_state(cfg: DNConfig, batch: int) -> DNState:

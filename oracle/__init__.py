@@ -9,11 +9,14 @@ from .dn_oracle import (  # noqa: F401
     OracleLayer,
     causal_conv_silu_step,
     gated_delta_rule_step,
+    gate_transform,
     gated_rmsnorm,
     int8_rowscaled_gemv,
     l2_normalize,
     normalize_qk,
     rms_prenorm,
+    sigmoid,
     silu,
+    softplus,
     stack_step,
 )

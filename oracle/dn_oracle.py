@@ -50,6 +50,30 @@ def silu(x: np.ndarray) -> np.ndarray:
         return x / (1.0 + np.exp(-x))
 
 
+def softplus(x: np.ndarray) -> np.ndarray:
+    """softplus(x) = log(1 + e^x), as max(x, 0) + log1p(e^-|x|) (no overflow)."""
+    x = np.asarray(x, F64)
+    return np.maximum(x, 0.0) + np.log1p(np.exp(-np.abs(x)))
+
+
+def sigmoid(x: np.ndarray) -> np.ndarray:
+    """sigmoid(x) = 1 / (1 + e^-x)."""
+    x = np.asarray(x, F64)
+    with np.errstate(over="ignore"):
+        return 1.0 / (1.0 + np.exp(-x))
+
+
+def gate_transform(a: np.ndarray, b: np.ndarray, A: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """The gates from the a/b projections: log-decay g = -A * softplus(a) and
+    write strength beta = sigmoid(b), A one coefficient per head (the
+    workloads' recipe, g = -softplus(a) * 0.5, beta = sigmoid(b), with A =
+    0.5).  a is [..., heads] or [..., heads, dk] (per-key gate), b [..., heads]."""
+    a = np.asarray(a, F64)
+    A = np.asarray(A, F64)
+    g = -(A[:, None] if a.ndim == np.ndim(b) + 1 else A) * softplus(a)
+    return g, sigmoid(b)
+
+
 def int8_rowscaled_gemv(w: np.ndarray, s: np.ndarray, x: np.ndarray) -> np.ndarray:
     """y[..., o] = s[o] * sum_i w[o, i] * x[..., i], in float64.
 
@@ -138,19 +162,33 @@ class OracleLayer:
         # float64 copies of the int8 matrices (exact), made once per layer
         self.w_in64 = weights.w_in.astype(F64)
         self.w_out64 = weights.w_out.astype(F64)
+        self.w_ab64 = weights.w_ab.astype(F64) if getattr(cfg, "device_gates", False) else None
         self.S = np.array(state.S, dtype=F64, copy=True)
         self.ring = np.array(state.ring, dtype=F64, copy=True)
         self.ring_pos = np.array(state.ring_pos, dtype=np.int64, copy=True)
 
-    def step(self, x: np.ndarray, g: np.ndarray, beta: np.ndarray, trace: dict | None = None) -> np.ndarray:
+    def step(self, x: np.ndarray, g: np.ndarray | None = None, beta: np.ndarray | None = None,
+             trace: dict | None = None) -> np.ndarray:
         """x [B][hidden], g [B][n_v_heads] (or [B][n_v_heads][dk] with the
         per-key gate), beta [B][n_v_heads] -> out [B][hidden] (float64).
 
         If ``trace`` is a dict it receives the intermediates: "y" (in_proj
         output), "u" (conv+SiLU output), "o" (readout per head) and "normed".
+
+        With device gates (cfg.device_gates) g and beta are not given: the
+        layer's a/b gate projections (int8 rows, one scale per row) of x give
+        a [B][heads] (or [B][heads][dk]) and b [B][heads], and gate_transform
+        turns them into g and beta.
         """
         c, w = self.cfg, self.w
         B = x.shape[0]
+        if getattr(c, "device_gates", False):
+            if g is not None or beta is not None:
+                raise ValueError("a layer with device gates takes no g / beta")
+            ab = int8_rowscaled_gemv(self.w_ab64, w.s_ab, x)          # [B][gate_rows]
+            na = c.n_v_heads * c.gate_width
+            a = ab[:, :na].reshape((B, c.n_v_heads) + ((c.dk,) if c.gate_width > 1 else ()))
+            g, beta = gate_transform(a, ab[:, na:], w.gate_A)
         qk, C = c.qk_dim, c.conv_ch
         group = c.n_v_heads // c.n_qk_heads
         y = int8_rowscaled_gemv(self.w_in64, w.s_in, x)     # [B][in_rows]

@@ -3,6 +3,7 @@ other than itself (exact integer arithmetic, a closed form, a hand-worked
 case, a brute-force unrolling of the recurrence, or an invariant of the
 definition), so that a dropped term, a wrong sign or index or a transposed
 operand in the oracle fails here.  CPU only."""
+import dataclasses
 import math
 import os
 
@@ -14,6 +15,9 @@ import oracle.dn_oracle as dn_oracle
 from gated_deltanet_hybrid_gb300.inputs import DNConfig, DNState, DNWeights, make_weights, zero_state
 from oracle import (
     OracleLayer,
+    gate_transform,
+    sigmoid,
+    softplus,
     causal_conv_silu_step,
     gated_delta_rule_step,
     gated_rmsnorm,
@@ -404,6 +408,61 @@ QSCALE_MUTANTS = {
 def test_pins_catch_qscale_mutant(name, monkeypatch):
     monkeypatch.setattr(dn_oracle, "normalize_qk", QSCALE_MUTANTS[name])
     assert not _layer_golden_ok()
+
+
+# ---------------------------------------------------------------- gate transform
+def test_softplus_closed_forms_and_library():
+    assert softplus(np.array(0.0)) == pytest.approx(math.log(2.0), rel=1e-16)
+    x = np.linspace(-30, 30, 241)
+    assert np.allclose(softplus(x) - softplus(-x), x, rtol=0, atol=1e-13)   # softplus(x) - softplus(-x) = x
+    assert np.allclose(softplus(x), np.logaddexp(0.0, x), rtol=1e-14, atol=0)
+    assert softplus(np.array(40.0)) == pytest.approx(40.0, rel=1e-16)
+    assert softplus(np.array(-40.0)) == pytest.approx(math.exp(-40.0), rel=1e-12)
+    assert softplus(np.array(-800.0)) == 0.0 and softplus(np.array(800.0)) == 800.0
+
+
+def test_sigmoid_closed_forms_and_library():
+    assert sigmoid(np.array(0.0)) == 0.5
+    assert sigmoid(np.array(math.log(3.0))) == pytest.approx(0.75, rel=1e-15)
+    x = np.linspace(-40, 40, 161)
+    assert np.allclose(sigmoid(x) + sigmoid(-x), 1.0, rtol=0, atol=1e-15)
+    assert np.allclose(sigmoid(x), expit(x), rtol=1e-14, atol=0)
+
+
+def test_gate_transform_handworked():
+    """a = (0, ln(e - 1)) -> softplus = (ln 2, 1); A = (0.5, 2) ->
+    g = (-0.5 ln 2, -2); b = (0, ln 3) -> beta = (0.5, 0.75).  With a per-key
+    gate each head's coefficient multiplies all of its dk values."""
+    a = np.array([[0.0, math.log(math.e - 1.0)]])
+    b = np.array([[0.0, math.log(3.0)]])
+    g, beta = gate_transform(a, b, np.array([0.5, 2.0]))
+    assert np.allclose(g, [[-0.5 * math.log(2.0), -2.0]], rtol=1e-15, atol=0)
+    assert np.allclose(beta, [[0.5, 0.75]], rtol=1e-15, atol=0)
+    ak = np.stack([np.zeros(3), np.full(3, math.log(math.e - 1.0))])[None]  # [1][2 heads][dk 3]
+    gk, _ = gate_transform(ak, b, np.array([0.5, 2.0]))
+    assert np.allclose(gk[0, 0], -0.5 * math.log(2.0), rtol=1e-15) and np.allclose(gk[0, 1], -2.0, rtol=1e-15)
+
+
+@pytest.mark.parametrize("key_gate", [False, True])
+def test_device_gates_are_the_a_b_rows_of_the_layer(key_gate):
+    """A layer with device gates steps exactly like the same layer given
+    host gates computed from its a rows (n_v * gate_width, first) and b rows
+    (n_v, after them) by an exact integer product and the pinned transform."""
+    cfg = DNConfig(hidden=24, n_qk_heads=2, n_v_heads=4, dk=4, dv=4, key_gate=key_gate, device_gates=True)
+    w = make_weights(cfg, np.random.default_rng(4))
+    rng = np.random.default_rng(5)
+    dev = OracleLayer(cfg, w, zero_state(cfg, 2))
+    host = OracleLayer(dataclasses.replace(cfg, device_gates=False), w, zero_state(cfg, 2))
+    for _ in range(3):
+        x = rng.integers(-3, 4, size=(2, cfg.hidden)).astype(np.float64)
+        ab = (x.astype(np.int64) @ w.w_ab.astype(np.int64).T) * w.s_ab.astype(np.float64)
+        na = cfg.n_v_heads * cfg.gate_width
+        a = ab[:, :na].reshape((2, 4, 4) if key_gate else (2, 4))
+        g, beta = gate_transform(a, ab[:, na:], w.gate_A)
+        out_d = dev.step(x)
+        out_h = host.step(x, g, beta)
+        assert np.allclose(out_d, out_h, rtol=1e-13, atol=1e-13)
+    assert np.allclose(dev.S, host.S, rtol=1e-13, atol=1e-13)
 
 
 # ---------------------------------------------------------------- whole step
