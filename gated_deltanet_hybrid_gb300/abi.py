@@ -22,6 +22,7 @@ DN_EINJECTED = -5
 DN_PTR_HOST = 0
 DN_PTR_DEVICE = 1
 DN_FLAG_KEY_GATE = 1
+DN_FLAG_DEVICE_GATES = 2
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdn.so")
 
@@ -48,7 +49,8 @@ class dn_config(ctypes.Structure):
 class dn_weights(ctypes.Structure):
     _fields_ = [("w_in", ctypes.c_void_p), ("s_in", ctypes.c_void_p),
                 ("w_conv", ctypes.c_void_p), ("w_norm", ctypes.c_void_p),
-                ("w_out", ctypes.c_void_p), ("s_out", ctypes.c_void_p)]
+                ("w_out", ctypes.c_void_p), ("s_out", ctypes.c_void_p),
+                ("w_ab", ctypes.c_void_p), ("s_ab", ctypes.c_void_p), ("gate_A", ctypes.c_void_p)]
 
 
 _lib = None
@@ -147,12 +149,16 @@ def dn_create(cfg, weights, max_batch: int, stream=None, check: bool = True):
     """Create a layer from a DNConfig-like object and host weight arrays.
     Returns the layer handle (ctypes.c_void_p)."""
     lib = load_library()
+    dev_gates = bool(getattr(cfg, "device_gates", False))
+    flags = (DN_FLAG_KEY_GATE if getattr(cfg, "key_gate", False) else 0) | (DN_FLAG_DEVICE_GATES if dev_gates else 0)
     c = dn_config(cfg.hidden, cfg.n_qk_heads, cfg.n_v_heads, cfg.dk, cfg.dv, cfg.conv_k,
-                  int(max_batch), cfg.l2_eps, cfg.norm_eps, cfg.qscale,
-                  DN_FLAG_KEY_GATE if getattr(cfg, "key_gate", False) else 0)
+                  int(max_batch), cfg.l2_eps, cfg.norm_eps, cfg.qscale, flags)
     arrs = [np.ascontiguousarray(weights.w_in, np.int8), np.ascontiguousarray(weights.s_in, np.float32),
             np.ascontiguousarray(weights.w_conv, np.float32), np.ascontiguousarray(weights.w_norm, np.float32),
             np.ascontiguousarray(weights.w_out, np.int8), np.ascontiguousarray(weights.s_out, np.float32)]
+    if dev_gates:
+        arrs += [np.ascontiguousarray(weights.w_ab, np.int8), np.ascontiguousarray(weights.s_ab, np.float32),
+                 np.ascontiguousarray(weights.gate_A, np.float32)]
     w = dn_weights(*[a.ctypes.data for a in arrs])
     if stream is None:
         try:

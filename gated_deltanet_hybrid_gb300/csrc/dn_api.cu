@@ -66,7 +66,7 @@ bool valid_cfg(const dn_config *c) {
     if (c->n_v_heads % c->n_qk_heads != 0) return false;
     if (!(c->dk == 32 || c->dk == 64 || c->dk == 128 || c->dk == 256)) return false;
     if (!(c->dv == 32 || c->dv == 64 || c->dv == 128 || c->dv == 256)) return false;
-    if (c->flags != 0 && c->flags != DN_FLAG_KEY_GATE) return false;
+    if ((c->flags & ~(DN_FLAG_KEY_GATE | DN_FLAG_DEVICE_GATES)) != 0) return false;
     if (c->conv_k < 2 || c->conv_k > 8) return false;
     if (c->max_batch < 1 || c->max_batch > 1024) return false;
     if (!(c->l2_eps > 0.f) || !(c->norm_eps > 0.f)) return false;
@@ -158,6 +158,7 @@ DN_API int dn_create(const dn_config *cfg, const dn_weights *w, void *stream, dn
     if (cfg == nullptr || w == nullptr || !valid_cfg(cfg)) return DN_EINVAL;
     if (!w->w_in || !w->s_in || !w->w_conv || !w->w_norm || !w->w_out || !w->s_out)
         return DN_EINVAL;
+    if ((cfg->flags & DN_FLAG_DEVICE_GATES) && (!w->w_ab || !w->s_ab || !w->gate_A)) return DN_EINVAL;
 
     dn_layer *l = new (std::nothrow) dn_layer();
     if (l == nullptr) return DN_ENOMEM;
@@ -177,6 +178,8 @@ DN_API int dn_create(const dn_config *cfg, const dn_weights *w, void *stream, dn
     d.norm_eps = cfg->norm_eps;
     d.q_scale = cfg->q_scale;
     d.gw = (cfg->flags & DN_FLAG_KEY_GATE) ? d.dk : 1;
+    d.dev_gates = (cfg->flags & DN_FLAG_DEVICE_GATES) ? 1 : 0;
+    d.proj_rows = d.in_rows + (d.dev_gates ? d.n_v * (d.gw + 1) : 0);
     l->stream = (cudaStream_t)stream;
     cudaGetDevice(&l->device);
 
@@ -186,12 +189,29 @@ DN_API int dn_create(const dn_config *cfg, const dn_weights *w, void *stream, dn
     int rc = DN_OK;
 #define ALLOC(ptr, bytes)                                               \
     if (rc == DN_OK) rc = layer_alloc(l, (void **)&(ptr), (size_t)(bytes));
-    const std::vector<uint8_t> wt_in = tile_weights(w->w_in, d.in_rows, d.hidden);
+    // the in_proj's rows, then (device gates) the a/b gate rows, one matrix
+    std::vector<int8_t> w_proj;
+    std::vector<float> s_proj;
+    const int8_t *w_in_all = w->w_in;
+    const float *s_in_all = w->s_in;
+    if (d.dev_gates) {
+        const size_t n_in = (size_t)d.in_rows * d.hidden, n_ab = (size_t)(d.proj_rows - d.in_rows) * d.hidden;
+        w_proj.resize(n_in + n_ab);
+        std::memcpy(w_proj.data(), w->w_in, n_in);
+        std::memcpy(w_proj.data() + n_in, w->w_ab, n_ab);
+        s_proj.resize((size_t)d.proj_rows);
+        std::memcpy(s_proj.data(), w->s_in, (size_t)d.in_rows * 4);
+        std::memcpy(s_proj.data() + d.in_rows, w->s_ab, (size_t)(d.proj_rows - d.in_rows) * 4);
+        w_in_all = w_proj.data();
+        s_in_all = s_proj.data();
+    }
+    const std::vector<uint8_t> wt_in = tile_weights(w_in_all, d.proj_rows, d.hidden);
     const std::vector<uint8_t> wt_out = tile_weights(w->w_out, d.hidden, d.v_dim);
     const size_t kt_in = (size_t)(d.hidden + dn::kTileK - 1) / dn::kTileK;
     const size_t kt_out = (size_t)(d.v_dim + dn::kTileK - 1) / dn::kTileK;
     ALLOC(L.w_in, wt_in.size());
-    ALLOC(L.s_in, (size_t)d.in_rows * 4);
+    ALLOC(L.s_in, (size_t)d.proj_rows * 4);
+    if (d.dev_gates) ALLOC(L.gate_A, (size_t)d.n_v * 4);
     ALLOC(L.wconv_t, (size_t)d.conv_k * d.conv_ch * 4);
     ALLOC(L.w_norm, (size_t)d.dv * 4);
     ALLOC(L.w_out, wt_out.size());
@@ -212,7 +232,7 @@ DN_API int dn_create(const dn_config *cfg, const dn_weights *w, void *stream, dn
     const size_t chunks = (MB + 63) / 64;
     size_t part_in = 0, part_out = 0, tiles_in = 0, tiles_out = 0, xb_bytes_in = 0, xb_bytes_out = 0;
     for (int b = 1; b <= (int)MB; ++b) {
-        const dn::GemmPlan gi = dn::plan_tc_gemm(d.in_rows, d.hidden, b);
+        const dn::GemmPlan gi = dn::plan_tc_gemm(d.proj_rows, d.hidden, b);
         const dn::GemmPlan go = dn::plan_tc_gemm(d.hidden, d.v_dim, b);
         part_in = std::max(part_in, (size_t)gi.tiles * gi.max_seg * 64 * 128);
         part_out = std::max(part_out, (size_t)go.tiles * go.max_seg * 64 * 128);
@@ -253,7 +273,8 @@ DN_API int dn_create(const dn_config *cfg, const dn_weights *w, void *stream, dn
     cudaError_t e = cudaSuccess;
     auto H2D = cudaMemcpyHostToDevice;
     if (e == cudaSuccess) e = cudaMemcpyAsync(L.w_in, wt_in.data(), wt_in.size(), H2D, st);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(L.s_in, w->s_in, (size_t)d.in_rows * 4, H2D, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(L.s_in, s_in_all, (size_t)d.proj_rows * 4, H2D, st);
+    if (e == cudaSuccess && d.dev_gates) e = cudaMemcpyAsync(L.gate_A, w->gate_A, (size_t)d.n_v * 4, H2D, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(L.wconv_t, wct.data(), wct.size() * 4, H2D, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(L.w_norm, w->w_norm, (size_t)d.dv * 4, H2D, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(L.w_out, wt_out.data(), wt_out.size(), H2D, st);
@@ -321,7 +342,7 @@ DN_API int dn_step_kernels(const dn_layer *l, int batch) {
 
 DN_API int dn_stack_step(dn_layer *const *layers, int n_layers, int batch, float *h, const float *g,
                          const float *beta, float eps, void *stream) {
-    if (layers == nullptr || n_layers < 1 || h == nullptr || g == nullptr || beta == nullptr) return DN_EINVAL;
+    if (layers == nullptr || n_layers < 1 || h == nullptr) return DN_EINVAL;
     if (!(eps >= 0.f)) return DN_EINVAL;
     dn_layer *first = layers[0];
     if (first == nullptr) return DN_EINVAL;
@@ -330,9 +351,12 @@ DN_API int dn_stack_step(dn_layer *const *layers, int n_layers, int batch, float
         const dn_layer *L = layers[l];
         if (L == nullptr || L->device != first->device) return DN_EINVAL;
         if (L->d.hidden != d0.hidden || L->d.n_v != d0.n_v || L->d.gw != d0.gw) return DN_EINVAL;
+        if (L->d.dev_gates != d0.dev_gates) return DN_EINVAL;
         if (batch < 1 || batch > L->d.max_batch) return DN_EINVAL;
         if (L->failed) return DN_EFAILED;
     }
+    // gates: from the caller, or (device gates) from the layers themselves
+    if (d0.dev_gates ? (g != nullptr || beta != nullptr) : (g == nullptr || beta == nullptr)) return DN_EINVAL;
     int cur = 0;
     if (cudaGetDevice(&cur) != cudaSuccess || cur != first->device) return DN_EINVAL;
     cudaStream_t st = stream != nullptr ? (cudaStream_t)stream : first->stream;
@@ -343,7 +367,9 @@ DN_API int dn_stack_step(dn_layer *const *layers, int n_layers, int batch, float
     if (dn::launch_residual_prenorm(h, nullptr, xn, batch, d0.hidden, eps, st) != cudaSuccess)
         return cuda_fail(first);
     for (int l = 0; l < n_layers; ++l) {
-        const int rc = dn_step(layers[l], batch, xn, g + l * gstride * d0.gw, beta + l * gstride, y, DN_PTR_DEVICE, st);
+        const float *gl = d0.dev_gates ? nullptr : g + l * gstride * d0.gw;
+        const float *bl = d0.dev_gates ? nullptr : beta + l * gstride;
+        const int rc = dn_step(layers[l], batch, xn, gl, bl, y, DN_PTR_DEVICE, st);
         if (rc != DN_OK) return rc;
         // h += y and the next layer's input (after the last layer: only the add matters)
         if (dn::launch_residual_prenorm(h, y, xn, batch, d0.hidden, eps, st) != cudaSuccess)
@@ -420,7 +446,8 @@ DN_API int dn_step(dn_layer *l, int batch, const float *x, const float *g, const
     const dn::Dims &d = l->d;
     if (ptr_kind != DN_PTR_HOST && ptr_kind != DN_PTR_DEVICE) return DN_EINVAL;
     if (batch < 1 || batch > d.max_batch) return DN_EINVAL;
-    if (x == nullptr || g == nullptr || beta == nullptr || out == nullptr) return DN_EINVAL;
+    if (x == nullptr || out == nullptr) return DN_EINVAL;
+    if (d.dev_gates ? (g != nullptr || beta != nullptr) : (g == nullptr || beta == nullptr)) return DN_EINVAL;
     if (!on_layer_device(l)) return DN_EINVAL;
     if (l->failed) return DN_EFAILED;
     if (l->fail_next != 0) {
@@ -435,11 +462,13 @@ DN_API int dn_step(dn_layer *l, int batch, const float *x, const float *g, const
     float *od = out;
     if (ptr_kind == DN_PTR_HOST) {
         DN_TRY(l, cudaMemcpyAsync(L.x_stage, x, (size_t)batch * d.hidden * 4, cudaMemcpyHostToDevice, st));
-        DN_TRY(l, cudaMemcpyAsync(L.g_stage, g, (size_t)batch * d.n_v * d.gw * 4, cudaMemcpyHostToDevice, st));
-        DN_TRY(l, cudaMemcpyAsync(L.beta_stage, beta, (size_t)batch * d.n_v * 4, cudaMemcpyHostToDevice, st));
+        if (!d.dev_gates) {
+            DN_TRY(l, cudaMemcpyAsync(L.g_stage, g, (size_t)batch * d.n_v * d.gw * 4, cudaMemcpyHostToDevice, st));
+            DN_TRY(l, cudaMemcpyAsync(L.beta_stage, beta, (size_t)batch * d.n_v * 4, cudaMemcpyHostToDevice, st));
+            gd = L.g_stage;
+            bd = L.beta_stage;
+        }
         xd = L.x_stage;
-        gd = L.g_stage;
-        bd = L.beta_stage;
         od = L.out_stage;
     }
     if (l->expire_us_next > 0) {
@@ -453,10 +482,10 @@ DN_API int dn_step(dn_layer *l, int batch, const float *x, const float *g, const
     const bool tc = batch >= dn::kTcMinBatch;
     if (tc) {
         DN_TRY(l, dn::launch_pack_b(xd, L.xb_in, batch, d.hidden, st));
-        DN_TRY(l, dn::launch_gemm_i8_tc(L.w_in, L.xb_in, L.part_in, L.nseg_in, L.err, d.in_rows,
+        DN_TRY(l, dn::launch_gemm_i8_tc(L.w_in, L.xb_in, L.part_in, L.nseg_in, L.err, d.proj_rows,
                                         d.hidden, batch, st));
     } else {
-        DN_TRY(l, dn::launch_gemv_i8(L.w_in, xd, L.part_in, L.nseg_in, L.err, d.in_rows, d.hidden,
+        DN_TRY(l, dn::launch_gemv_i8(L.w_in, xd, L.part_in, L.nseg_in, L.err, d.proj_rows, d.hidden,
                                      batch, st));
     }
     if (prof) DN_TRY(l, cudaEventRecord(l->prof[1], st));

@@ -49,10 +49,15 @@ struct CoreParams {
     const float *beta;     // [B][n_v]
     int n_qk, n_v, dv, conv_k, conv_ch, qk_dim, in_rows, v_dim, kt_out;
     int gw;                // log-decay values per head: 1, or dk (per-key-channel gate)
+    int dev_gates;         // g, beta from the a/b gate rows after the in_proj rows
+    const float *gate_A;   // [n_v] (device gates)
     float l2_eps, norm_eps, q_scale;
 };
 
 __device__ __forceinline__ float silu_f(float a) { return a / (1.0f + expf(-a)); }
+// softplus(a) = log(1 + e^a) as max(a, 0) + log1p(e^-|a|); sigmoid(b) = 1 / (1 + e^-b)
+__device__ __forceinline__ float softplus_f(float a) { return fmaxf(a, 0.f) + log1pf(expf(-fabsf(a))); }
+__device__ __forceinline__ float sigmoid_f(float b) { return 1.0f / (1.0f + expf(-b)); }
 
 // in_proj output row c of sequence b: read directly, or summed from the
 // tensor-core kernel's segment partials in slot order, then scaled
@@ -80,6 +85,7 @@ __global__ void __launch_bounds__(kThreads, 2) dn_core_kernel(const CoreParams p
     __shared__ __align__(16) float red[RPP][DJ];
     __shared__ __align__(16) float eg_s[DK];  // exp(log-decay) of each key row
     __shared__ float inv_s[2];
+    __shared__ float bt_s;
     __shared__ float ssq_s;
 
     const int tid = threadIdx.x;
@@ -154,13 +160,20 @@ __global__ void __launch_bounds__(kThreads, 2) dn_core_kernel(const CoreParams p
         else
             k_s[i - DK] = k_s[i - DK] * inv_s[1];
     }
-    // the decay of each key row: one gate per head, or one per key channel
-    for (int i = tid; i < DK; i += kThreads)
-        eg_s[i] = expf(p.gw == 1 ? p.g[b * p.n_v + h] : p.g[((size_t)b * p.n_v + h) * DK + i]);
+    // the decay of each key row (one gate per head, or one per key channel)
+    // and the write strength: from the caller, or from the layer's a/b rows
+    for (int i = tid; i < DK; i += kThreads) {
+        const int gi = p.gw == 1 ? 0 : i;
+        const float gl = p.dev_gates ? -p.gate_A[h] * softplus_f(in_proj_out(p, b, p.in_rows + h * p.gw + gi))
+                                     : p.g[((size_t)b * p.n_v + h) * p.gw + gi];
+        eg_s[i] = expf(gl);
+    }
+    if (tid == 0)
+        bt_s = p.dev_gates ? sigmoid_f(in_proj_out(p, b, p.in_rows + p.n_v * p.gw + h)) : p.beta[b * p.n_v + h];
     __syncthreads();
 
     // ---- 4. decay, then what the decayed state predicts for k ----------------
-    const float bt = p.beta[b * p.n_v + h];
+    const float bt = bt_s;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
@@ -335,7 +348,7 @@ cudaError_t launch_dn_core(const Dims &d, const LayerDev &L, int B, const float 
     cp.nseg_in = L.nseg_in;
     cp.s_in = L.s_in;
     {
-        const GemmPlan gp = plan_tc_gemm(d.in_rows, d.hidden, B);
+        const GemmPlan gp = plan_tc_gemm(d.proj_rows, d.hidden, B);
         cp.sv = SchedView{gp.U, gp.G, gp.UT, gp.MT, gp.max_seg};
     }
     cp.kt_out = (d.v_dim + kTileK - 1) / kTileK;
@@ -353,6 +366,8 @@ cudaError_t launch_dn_core(const Dims &d, const LayerDev &L, int B, const float 
     cp.norm_eps = d.norm_eps;
     cp.q_scale = d.q_scale;
     cp.gw = d.gw;
+    cp.dev_gates = d.dev_gates;
+    cp.gate_A = L.gate_A;
     const int js = choose_js(d, B);
     const int dj = d.dv / js;
     switch (d.dk) {

@@ -17,7 +17,8 @@
 //    with one bulk store (global stores from registers would hold up the
 //    load/store unit that the producers' loads need);
 //  * 4 producer warps build the next item's inputs meanwhile, in a
-//    double-buffered record, one warp per row kind (16-byte loads of four
+//    double-buffered record, one warp per conv row kind and one for the z
+//    rows and the gates (16-byte loads of four
 //    channels per lane): for each of the item's q, k, v and z rows the
 //    in_proj output (its segment partials summed in slot order, dn_sched.cuh,
 //    times the row scale), then the conv over the ring (K-1 history slots
@@ -53,7 +54,7 @@ namespace {
 
 constexpr int D = 128;               // dk = dv
 constexpr int NC = 512;              // consumer threads (16 warps)
-constexpr int NPW = 4;               // producer warps (one row kind each: q, k, v, z)
+constexpr int NPW = 4;               // producer warps (q, k, v; z and the gates)
 constexpr int NT = NC + 32 * NPW;    // 640
 constexpr int STAGES = 3;
 constexpr uint32_t kTileBytes = D * D * 4;
@@ -85,6 +86,8 @@ struct StreamParams {
     int MT, max_seg;       // in_proj row tiles and segment slots per tile
     int n_v, group, conv_ch, qk_dim, v_dim, kt_out, items;
     int gw;                // log-decay values per head: 1, or 128 (per-key-channel gate)
+    int dev_gates, in_rows; // g, beta from the a/b gate rows that follow the in_rows in_proj rows
+    const float *gate_A;   // [n_v] (device gates)
     float l2_eps, q_scale, norm_eps;
 };
 
@@ -310,36 +313,97 @@ __device__ __forceinline__ void store_norm(const StreamParams &p, const StreamSm
     }
 }
 
-// The log-decays of key rows cl .. cl+3 of `item`: one per head (repeated),
-// or one per key channel
-__device__ __forceinline__ float4 load_gate(const StreamParams &p, int item, int cl) {
-    if (p.gw == 1) {
-        const float g = ld_cg(p.g + item);
-        return make_float4(g, g, g, g);
+// softplus(a) = log(1 + e^a) as max(a, 0) + log1p(e^-|a|); sigmoid(b) = 1 / (1 + e^-b)
+__device__ __forceinline__ float softplus_f(float a) { return fmaxf(a, 0.f) + log1pf(expf(-fabsf(a))); }
+__device__ __forceinline__ float sigmoid_f(float b) { return 1.0f / (1.0f + expf(-b)); }
+
+// An item's gates as seen by lane l of producer warp 3: the log-decays of key
+// rows cl .. cl+3 (cl = 4l; one gate per head is repeated) and the write
+// strength.  From the caller (g, beta), or - device gates - from the layer's
+// a/b rows: the loads of a (four rows, or the head's one row) and b, which
+// are summed and transformed when the record is built.
+struct GateLoads {
+    float4 g4;      // caller's log-decays
+    float bv;       // caller's beta
+    float4 pa[PV];  // a partials
+    float4 sa;      // a row scales
+    float pb[PV], sb, A;
+    int nsa, nsb;
+};
+
+__device__ __forceinline__ int gate_a_row(const StreamParams &p, int h, int cl) {
+    return p.in_rows + h * p.gw + (p.gw == 1 ? 0 : cl);
+}
+__device__ __forceinline__ int gate_b_row(const StreamParams &p, int h) { return p.in_rows + p.n_v * p.gw + h; }
+__device__ __forceinline__ float4 splat(float v) { return make_float4(v, v, v, v); }
+
+// the loads the in_proj does not feed
+__device__ __forceinline__ void load_gates_fixed(const StreamParams &p, int h, int item, int cl, GateLoads &G) {
+    if (!p.dev_gates) {
+        G.g4 = p.gw == 1 ? splat(ld_cg(p.g + item)) : ld_cg4(p.g + (size_t)item * D + cl);
+        G.bv = ld_cg(p.beta + item);
+        return;
     }
-    return ld_cg4(p.g + (size_t)item * D + cl);
+    const int ca = gate_a_row(p, h, cl);
+    G.sa = p.gw == 1 ? splat(ld_nc(p.s_in + ca)) : ld_nc4(p.s_in + ca);
+    G.sb = ld_nc(p.s_in + gate_b_row(p, h));
+    G.A = ld_nc(p.gate_A + h);
+}
+// the in_proj's partials of the gate rows
+__device__ __forceinline__ void load_gates_part(const StreamParams &p, int b, int h, int cl, GateLoads &G) {
+    if (!p.dev_gates) return;
+    const int ca = gate_a_row(p, h, cl), cb = gate_b_row(p, h);
+    G.nsa = ld_cg_s32(p.nseg_in + (b >> 6) * p.MT + (ca >> 7));
+    G.nsb = ld_cg_s32(p.nseg_in + (b >> 6) * p.MT + (cb >> 7));
+    const float *pa = row_partials(p, b, ca), *pb = row_partials(p, b, cb);
+#pragma unroll
+    for (int k = 0; k < PV; ++k) {  // slots past max_seg fall back to slot 0
+        const size_t o = (size_t)(k < p.max_seg ? k : 0) * (64 * D);
+        G.pa[k] = p.gw == 1 ? splat(ld_cg(pa + o)) : ld_cg4(pa + o);
+        G.pb[k] = ld_cg(pb + o);
+    }
+}
+// the item's log-decays (four key rows) and beta
+__device__ __forceinline__ float4 gate_values(const StreamParams &p, int b, int h, int cl, const GateLoads &G,
+                                              float &beta) {
+    if (!p.dev_gates) {
+        beta = G.bv;
+        return G.g4;
+    }
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    float bs = 0.f;
+#pragma unroll
+    for (int k = 0; k < PV; ++k) {
+        if (k < G.nsa) add4(a, G.pa[k]);
+        if (k < G.nsb) bs += G.pb[k];
+    }
+    if (G.nsa > PV || G.nsb > PV) {
+        const float *pa = row_partials(p, b, gate_a_row(p, h, cl)), *pb = row_partials(p, b, gate_b_row(p, h));
+        for (int k = PV; k < G.nsa; ++k) add4(a, p.gw == 1 ? splat(__ldcg(pa + (size_t)k * (64 * D))) : ld_cg4(pa + (size_t)k * (64 * D)));
+        for (int k = PV; k < G.nsb; ++k) bs += __ldcg(pb + (size_t)k * (64 * D));
+    }
+    beta = sigmoid_f(G.sb * bs);
+    return make_float4(-G.A * softplus_f(G.sa.x * a.x), -G.A * softplus_f(G.sa.y * a.y),
+                       -G.A * softplus_f(G.sa.z * a.z), -G.A * softplus_f(G.sa.w * a.w));
 }
 
-// Producer warps: build the record (q^, k^, v, silu(z), gates) of every item
-// of the CTA's range, one item ahead of the consumers.  Warp `kind` builds
-// one row kind (0 q, 1 k, 2 v, 3 z), lane l channels 4l .. 4l+3 of the head,
+// Producer warps 0-2: build the conv rows of the record (q^, k^, v) of
+// every item of the CTA's range, one item ahead of the consumers.  Warp `kind` builds
+// one row kind (0 q, 1 k, 2 v), lane l channels 4l .. 4l+3 of the head,
 // so a q or k norm is one warp's sum.  The loads of item j+1 are issued as
 // soon as item j's values are computed (the registers are free again), so
 // their latency hides behind the rest of item j.
 template <int KC>
 __device__ void produce(const StreamParams &p, StreamSmem &sm, int i0, int n_items, int b0, int kind, int lane) {
     const int cl = 4 * lane;
-    const bool conv = kind < 3, qk = kind < 2;
-    const int base = kind == 0 ? 0 : kind == 1 ? p.qk_dim : kind == 2 ? 2 * p.qk_dim : p.conv_ch;
+    constexpr bool conv = true;
+    const bool qk = kind < 2;
+    const int base = kind == 0 ? 0 : kind == 1 ? p.qk_dim : 2 * p.qk_dim;
     int b = b0, h = i0 - b0 * p.n_v, hq = h / p.group;
     RowLoads<KC> r;
-    float bv = 0.f;
-    float4 gv = make_float4(0.f, 0.f, 0.f, 0.f);  // (warp 3) the item's log-decays of key rows cl .. cl+3
     // the first item's loads that the in_proj does not feed go out before the wait
     int c = base + (qk ? hq : h) * D + cl;
     load_row_fixed(p, sm, b0, b, c, conv, r);
-    if (kind == 0 && lane == 0) bv = ld_cg(p.beta + i0);
-    if (kind == 3) gv = load_gate(p, i0, cl);
     pdl_wait();
     load_row_part(p, b, c, r);
     bool reuse = false;  // item j has the q/k head of item j-1
@@ -348,16 +412,10 @@ __device__ void produce(const StreamParams &p, StreamSmem &sm, int i0, int n_ite
         c = base + (qk ? hq : h) * D + cl;
         float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
         if (!(qk && reuse)) {
-            const float4 xv = row_value(p, b, c, r);
-            if (conv) {
-                // v rows belong to one item; q/k rows are written by the q/k head's first value head
-                u = conv_silu(p, sm, b0, b, c, xv, kind == 2 || h == hq * p.group, r);
-            } else {
-                u = make_float4(silu_f(xv.x), silu_f(xv.y), silu_f(xv.z), silu_f(xv.w));
-            }
+            // v rows belong to one item; q/k rows are written by the q/k head's first value head
+            u = conv_silu(p, sm, b0, b, c, row_value(p, b, c, r), kind == 2 || h == hq * p.group, r);
         }
-        const float4 gj = gv;
-        const float bj = bv;
+
         // item j+1 and its loads
         const int bn = h + 1 == p.n_v ? b + 1 : b, hn = h + 1 == p.n_v ? 0 : h + 1, hqn = hn / p.group;
         const bool reuse_n = bn == b && hqn == hq;
@@ -367,8 +425,7 @@ __device__ void produce(const StreamParams &p, StreamSmem &sm, int i0, int n_ite
                 load_row_fixed(p, sm, b0, bn, cn, conv, r);
                 load_row_part(p, bn, cn, r);
             }
-            if (kind == 0 && lane == 0) bv = ld_cg(p.beta + i0 + j + 1);
-            if (kind == 3) gv = load_gate(p, i0 + j + 1, cl);
+
         }
         float4 outv = u;
         if (qk) {
@@ -386,16 +443,55 @@ __device__ void produce(const StreamParams &p, StreamSmem &sm, int i0, int n_ite
             break;
         }
         *reinterpret_cast<float4 *>(&sm.rec[rb][kind * D + cl]) = outv;
-        if (kind == 0 && lane == 0) sm.beta[rb] = bj;
-        if (kind == 3)
-            *reinterpret_cast<float4 *>(&sm.rec[rb][4 * D + cl]) =
-                make_float4(expf(gj.x), expf(gj.y), expf(gj.z), expf(gj.w));
+
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.rec_full[rb]);  // release: the record's writes come first
         b = bn;
         h = hn;
         hq = hqn;
         reuse = reuse_n;
+    }
+}
+
+// Producer warp 3: the z rows (silu(z)) and the gates (the decay of each
+// key row, the write strength) of every item, one item ahead of the
+// consumers, with their loads one item ahead of their use.  Its own loop, so
+// that its registers do not add to those of the conv-row warps.
+template <int KC>
+__device__ void produce_z_gates(const StreamParams &p, StreamSmem &sm, int i0, int n_items, int b0, int lane) {
+    const int cl = 4 * lane;
+    int b = b0, h = i0 - b0 * p.n_v;
+    RowLoads<KC> r;  // (conv fields unused)
+    GateLoads G;
+    load_row_fixed(p, sm, b0, b, p.conv_ch + h * D + cl, false, r);
+    load_gates_fixed(p, h, i0, cl, G);
+    pdl_wait();
+    load_row_part(p, b, p.conv_ch + h * D + cl, r);
+    load_gates_part(p, b, h, cl, G);
+    for (int j = 0; j < n_items; ++j) {
+        const int rb = j & 1;
+        const float4 xz = row_value(p, b, p.conv_ch + h * D + cl, r);
+        const float4 uz = make_float4(silu_f(xz.x), silu_f(xz.y), silu_f(xz.z), silu_f(xz.w));
+        float bj;
+        const float4 gj = gate_values(p, b, h, cl, G, bj);
+        const int bn = h + 1 == p.n_v ? b + 1 : b, hn = h + 1 == p.n_v ? 0 : h + 1;
+        if (j + 1 < n_items) {
+            load_row_fixed(p, sm, b0, bn, p.conv_ch + hn * D + cl, false, r);
+            load_row_part(p, bn, p.conv_ch + hn * D + cl, r);
+            load_gates_fixed(p, hn, i0 + j + 1, cl, G);
+            load_gates_part(p, bn, hn, cl, G);
+        }
+        if (j >= 2 && !mbar_wait(&sm.rec_empty[rb], ((j >> 1) - 1) & 1)) {
+            sm.failed = 1;
+            break;
+        }
+        *reinterpret_cast<float4 *>(&sm.rec[rb][3 * D + cl]) = uz;
+        *reinterpret_cast<float4 *>(&sm.rec[rb][4 * D + cl]) = make_float4(expf(gj.x), expf(gj.y), expf(gj.z), expf(gj.w));
+        if (lane == 0) sm.beta[rb] = bj;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.rec_full[rb]);
+        b = bn;
+        h = hn;
     }
 }
 
@@ -549,8 +645,10 @@ __global__ void __launch_bounds__(NT, 1) dn_core_stream_kernel(const StreamParam
         pdl_wait();  // (consumers read nothing the in_proj writes; the wait keeps completion transitive)
         if (t == 0) pdl_trigger();
         issued = consume(p, sm, i0, n_items, b0, t);
-    } else {
+    } else if (warp < NC / 32 + 3) {
         produce<KC>(p, sm, i0, n_items, b0, warp - NC / 32, lane);
+    } else {
+        produce_z_gates<KC>(p, sm, i0, n_items, b0, lane);
     }
     __syncthreads();
     if (t == kTma) {
@@ -568,8 +666,13 @@ cudaError_t launch_kc(const StreamParams &p, cudaStream_t st) {
     static std::atomic<uint64_t> attr_done{0};
     const size_t smem = sizeof(StreamSmem) + 128;
     const cudaError_t e = once_per_device(attr_done, [&](int) {
-        return cudaFuncSetAttribute(dn_core_stream_kernel<KC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)smem);
+        cudaError_t r = cudaFuncSetAttribute(dn_core_stream_kernel<KC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        // 640 threads at up to 96 registers and ~216 KB: one CTA must fit an SM
+        int fit = 0;
+        if (r == cudaSuccess) r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, dn_core_stream_kernel<KC>, NT, smem);
+        if (r == cudaSuccess && fit < 1) r = cudaErrorLaunchOutOfResources;
+        return r;
     });
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -605,7 +708,7 @@ cudaError_t launch_dn_core_stream(const Dims &d, const LayerDev &L, int B, const
     p.nrm = L.nrm;
     p.xb_out = tc ? L.xb_out : nullptr;
     p.err = L.err;
-    const GemmPlan gp = plan_tc_gemm(d.in_rows, d.hidden, B);
+    const GemmPlan gp = plan_tc_gemm(d.proj_rows, d.hidden, B);
     p.MT = gp.MT;
     p.max_seg = gp.max_seg;
     p.n_v = d.n_v;
@@ -619,6 +722,9 @@ cudaError_t launch_dn_core_stream(const Dims &d, const LayerDev &L, int B, const
     p.q_scale = d.q_scale;
     p.norm_eps = d.norm_eps;
     p.gw = d.gw;
+    p.dev_gates = d.dev_gates;
+    p.in_rows = d.in_rows;
+    p.gate_A = L.gate_A;
     switch (d.conv_k) {
         case 2: return launch_kc<2>(p, st);
         case 3: return launch_kc<3>(p, st);

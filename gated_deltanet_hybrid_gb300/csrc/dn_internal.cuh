@@ -11,8 +11,8 @@
 namespace dn {
 
 // Device-side layout of one layer.  All buffers are owned by the layer.
-//   w_in    int8 [in_rows][hidden]           (as given)
-//   s_in    f32  [in_rows]
+//   w_in    int8 [proj_rows][hidden]         (the in_proj rows, then the a/b gate rows)
+//   s_in    f32  [proj_rows]
 //   wconv_t f32  [conv_k][conv_ch]           (transposed: one tap is a contiguous row)
 //   w_norm  f32  [dv]
 //   w_out   int8 [hidden][v_dim]
@@ -30,12 +30,15 @@ struct Dims {
     int hidden, n_qk, n_v, dk, dv, conv_k, max_batch;
     int qk_dim, v_dim, conv_ch, in_rows;
     int gw;  // log-decay values per head and step: dk with the per-key gate, else 1
+    int dev_gates;  // the a/b gate rows follow the in_proj rows (DN_FLAG_DEVICE_GATES)
+    int proj_rows;  // rows of the in_proj GEMM: in_rows, plus n_v * (gw + 1) gate rows
     float l2_eps, norm_eps, q_scale;
 };
 
 struct LayerDev {
     uint8_t *w_in;  // tiled int8 (see kTileM / kTileK)
     float *s_in, *wconv_t, *w_norm;
+    float *gate_A;  // [n_v] (device gates only)
     uint8_t *w_out;  // tiled int8
     float *s_out;
     float *S, *ring;

@@ -206,13 +206,16 @@ class WorkloadStream:
 
     def next_step(self) -> tuple[np.ndarray, list[tuple[np.ndarray, np.ndarray]]]:
         """x [B][hidden] f32 and, per layer, (g, beta): g [B][n_v_heads] f32
-        ([B][n_v_heads][dk] with the per-key gate), beta [B][n_v_heads] f32."""
+        ([B][n_v_heads][dk] with the per-key gate), beta [B][n_v_heads] f32;
+        (None, None) for a layer with device gates."""
         cfg, B = self.wl.cfg, self.wl.batch
         x = self.rng.standard_normal((B, cfg.hidden)).astype(np.float32)
         gates = []
         gshape = (B, cfg.n_v_heads, cfg.dk) if cfg.key_gate else (B, cfg.n_v_heads)
         for _ in range(self.wl.layers):
-            if self.wl.gate == "softplus":
+            if cfg.device_gates:  # the layer computes its gates from x
+                gates.append((None, None))
+            elif self.wl.gate == "softplus":
                 a = self.rng.standard_normal(gshape)
                 b = self.rng.standard_normal((B, cfg.n_v_heads))
                 g, _ = gates_from_ab(a, a)

@@ -50,6 +50,12 @@ extern "C" {
  * (g[b][h][i] scales row i of that head's state), the gate of the page's
  * KDA engines; without it one log-decay per head scales the whole state */
 #define DN_FLAG_KEY_GATE 1
+/* device-side gates: the layer holds the a/b gate projections as int8 rows
+ * (dn_weights.w_ab / s_ab / gate_A) and computes g = -A[h] * softplus(a) and
+ * beta = sigmoid(b) itself from each step's x, so dn_step and dn_stack_step
+ * take no g or beta (pass NULL); the page keeps these two small projections
+ * on the host and passes their values to the kernels */
+#define DN_FLAG_DEVICE_GATES 2
 
 /* ---- where a pointer argument lives ------------------------------------ */
 #define DN_PTR_HOST   0
@@ -70,7 +76,7 @@ typedef struct dn_layer dn_layer; /* opaque; owns all of its device memory */
  *   l2_eps      eps inside the square root of the q/k L2 norms (> 0)
  *   norm_eps    eps of the gated RMSNorm (> 0)
  *   q_scale     multiplies the normalised q (e.g. 1/sqrt(dk))
- *   flags       0 or DN_FLAG_KEY_GATE
+ *   flags       0, or DN_FLAG_KEY_GATE and / or DN_FLAG_DEVICE_GATES
  * Derived: conv_ch = 2*n_qk_heads*dk + n_v_heads*dv,
  *          in_rows = conv_ch + n_v_heads*dv, v_dim = n_v_heads*dv.
  */
@@ -93,6 +99,12 @@ typedef struct dn_config {
  *   w_norm [dv]; one gated-RMSNorm weight vector shared by all value heads
  *   w_out  int8 [hidden][v_dim]; out[o] = s_out[o]*sum_i w_out[o][i]*n[i]
  *   s_out  [hidden]
+ *   w_ab   (DN_FLAG_DEVICE_GATES only, else NULL) int8 [gate_rows][hidden]:
+ *          the a rows (n_v_heads * gw, gw = dk with DN_FLAG_KEY_GATE, else
+ *          1; head-major) then the b rows (n_v_heads);
+ *          a = s_ab * (w_ab x), b likewise
+ *   s_ab   [gate_rows] row scales, gate_rows = n_v_heads * (gw + 1)
+ *   gate_A [n_v_heads] decay coefficients: g = -gate_A[h] * softplus(a)
  * Value head h reads q/k head h / (n_v_heads / n_qk_heads).
  */
 typedef struct dn_weights {
@@ -102,6 +114,9 @@ typedef struct dn_weights {
     const float  *w_norm;
     const int8_t *w_out;
     const float  *s_out;
+    const int8_t *w_ab;
+    const float  *s_ab;
+    const float  *gate_A;
 } dn_weights;
 
 /*
@@ -158,6 +173,8 @@ int dn_get_state(dn_layer *layer, int seq0, int n, float *S, float *ring, int32_
  *        state is scaled by exp(g[b][h][i]))
  *   beta [batch][n_v_heads]  write strength per head
  *   out  [batch][hidden]     layer output (written)
+ * With DN_FLAG_DEVICE_GATES, g and beta must be NULL (the layer computes
+ * them from x).
  * ptr_kind DN_PTR_DEVICE: all four are device pointers; the call only
  *   enqueues kernels on `stream` (NULL: the layer's stream) and returns; it
  *   allocates nothing and does not synchronise, so it can be captured in a
@@ -191,7 +208,8 @@ void dn_destroy(dn_layer *layer);
  *           current device, each with max_batch >= batch
  *   h       [batch][hidden] device, read and overwritten
  *   g, beta [n_layers][batch][n_v_heads] device, each layer's gates (g has a
- *           trailing [dk] with DN_FLAG_KEY_GATE; all layers then share it)
+ *           trailing [dk] with DN_FLAG_KEY_GATE; all layers then share it);
+ *           both NULL when the layers have DN_FLAG_DEVICE_GATES (all or none)
  * Device pointers only; the call enqueues on `stream` (NULL: the first
  * layer's stream) and uses the first layer's staging buffers for the
  * normalised input and each layer's output.  Errors: DN_EINVAL (NULL, bad

@@ -101,10 +101,14 @@ def run_parity(wl: Workload, steps: int | None = None, sample=None, checkpoints=
             x, gates = st.next_step()
             g, beta = gates[0]
             x_d.copy_(torch.from_numpy(x))
-            g_d.copy_(torch.from_numpy(g))
-            b_d.copy_(torch.from_numpy(beta))
-            abi.dn_step(gpu.handle, B, x_d, g_d, b_d, out_d)
-            ref = ora.step(x[sample], g[sample], beta[sample])
+            if g is None:  # device gates
+                abi.dn_step(gpu.handle, B, x_d, None, None, out_d)
+                ref = ora.step(x[sample])
+            else:
+                g_d.copy_(torch.from_numpy(g))
+                b_d.copy_(torch.from_numpy(beta))
+                abi.dn_step(gpu.handle, B, x_d, g_d, b_d, out_d)
+                ref = ora.step(x[sample], g[sample], beta[sample])
             got = out_d.cpu().numpy()[sample]
             worst["out"] = max(worst["out"], rel_err(got, ref))
             worst["elementwise_out"] = max(worst["elementwise_out"], elementwise_rel(got, ref))

@@ -188,3 +188,52 @@ def test_key_gate_35b_batch16_256_steps():
     cfg = DNConfig(hidden=2048, n_qk_heads=16, n_v_heads=32, dk=128, dv=128, key_gate=True)
     wl = custom_workload("kgate_35b_b16", cfg, batch=16, steps=256, seed=716, init_std=0.02, gate="decay_band")
     _assert_ok(run_parity(wl, sample=np.array([0, 15]), checkpoints=(64, 256)))
+
+
+# ---- device-side gates: the a/b gate projections as int8 rows of the layer --
+@pytest.mark.parametrize("batch", [1, 8, 64])
+def test_device_gates_35b(batch):
+    """The a/b gate rows ride in the in_proj (CUDA-core and tensor-core
+    projections, 12288 + 64 rows) and the streaming state kernel turns them
+    into the decay and the write strength."""
+    cfg = DNConfig(hidden=2048, n_qk_heads=16, n_v_heads=32, dk=128, dv=128, device_gates=True)
+    wl = custom_workload(f"devg_b{batch}", cfg, batch=batch, steps=32, seed=900 + batch, init_std=0.02)
+    _assert_ok(run_parity(wl, sample=np.array(sorted({0, batch - 1}))))
+
+
+@pytest.mark.parametrize("dims,batch", [
+    (dict(hidden=256, n_qk_heads=2, n_v_heads=4, dk=32, dv=32), 3),
+    (dict(hidden=256, n_qk_heads=2, n_v_heads=4, dk=32, dv=32, key_gate=True), 9),
+    (dict(hidden=512, n_qk_heads=2, n_v_heads=4, dk=256, dv=128, key_gate=True), 2),
+    (dict(hidden=2048, n_qk_heads=16, n_v_heads=32, dk=128, dv=128, key_gate=True), 16),
+])
+def test_device_gates_other_shapes(dims, batch):
+    """Device gates on the generic state kernel (32- and 256-wide keys), with
+    one gate per head and with the per-key gate (a rows per key channel), and
+    on the streaming kernel with the per-key gate."""
+    cfg = DNConfig(device_gates=True, **dims)
+    wl = custom_workload("devg", cfg, batch=batch, steps=24, seed=950 + batch, init_std=0.02)
+    _assert_ok(run_parity(wl, sample=np.array(sorted({0, batch - 1}))))
+
+
+def test_device_gates_reject_host_gates():
+    """A layer with device gates refuses g / beta, and a layer without them
+    refuses NULL gates, before any device work."""
+    import torch
+    from gated_deltanet_hybrid_gb300 import abi
+    from gated_deltanet_hybrid_gb300.inputs import make_weights
+    from harness import GpuLayer
+
+    for dev in (True, False):
+        cfg = DNConfig(hidden=256, n_qk_heads=2, n_v_heads=4, dk=32, dv=32, device_gates=dev)
+        layer = GpuLayer.create(cfg, make_weights(cfg, np.random.default_rng(1)), 2)
+        try:
+            x = torch.zeros((2, 256), device="cuda")
+            out = torch.empty_like(x)
+            g = torch.zeros((2, 4), device="cuda")
+            if dev:
+                assert abi.dn_step(layer.handle, 2, x, g, g, out, check=False) == abi.DN_EINVAL
+            else:
+                assert abi.dn_step(layer.handle, 2, x, None, None, out, check=False) == abi.DN_EINVAL
+        finally:
+            layer.destroy()
