@@ -27,7 +27,7 @@ DN_FLAG_DEVICE_GATES = 2
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdn.so")
 
 #: every call the header declares, in declaration order
-ABI_SYMBOLS = ("dn_create", "dn_set_state", "dn_get_state", "dn_step", "dn_stack_step", "dn_destroy",
+ABI_SYMBOLS = ("dn_create", "dn_set_state", "dn_get_state", "dn_step", "dn_stack_step", "dn_prefill", "dn_destroy",
                "dn_debug_fail_next", "dn_debug_expire_wait", "dn_profile_next_step", "dn_proj_i8_noalloc",
                "dn_device_bytes", "dn_step_kernels", "dn_strerror")
 
@@ -76,6 +76,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dn_step.restype = i32
     lib.dn_stack_step.argtypes = [ctypes.POINTER(vp), i32, i32, f32p, f32p, f32p, ctypes.c_float, vp]
     lib.dn_stack_step.restype = i32
+    lib.dn_prefill.argtypes = [vp, i32, i32, f32p, f32p, f32p, f32p, vp]
+    lib.dn_prefill.restype = i32
     lib.dn_destroy.argtypes = [vp]
     lib.dn_destroy.restype = None
     lib.dn_debug_fail_next.argtypes = [vp, i32]
@@ -217,6 +219,21 @@ def dn_stack_step(layers, batch: int, h, g, beta, eps: float = 1e-6, stream=None
     arr = (ctypes.c_void_p * len(layers))(*[ctypes.c_void_p(getattr(l, "value", l)) for l in layers])
     rc = lib.dn_stack_step(arr, len(layers), int(batch), ph, pg, pb, float(eps), _stream_of(stream, DN_PTR_DEVICE))
     return _check("dn_stack_step", rc, check)
+
+
+def dn_prefill(layer, batch: int, n_tokens: int, x, g, beta, out, stream=None, check: bool = True) -> int:
+    """A prompt of n_tokens tokens for sequences [0, batch): x, out
+    [batch][n_tokens][hidden], g [batch][n_tokens][heads](dk), beta
+    [batch][n_tokens][heads] CUDA tensors (g, beta None with device gates)."""
+    lib = load_library()
+    px, kx = _ptr(x, "float32")
+    pg, kg = _ptr(g, "float32")
+    pb, kb = _ptr(beta, "float32")
+    po, ko = _ptr(out, "float32")
+    if _same_kind(kx, kg, kb, ko) != DN_PTR_DEVICE:
+        raise TypeError("dn_prefill takes device tensors")
+    rc = lib.dn_prefill(layer, int(batch), int(n_tokens), px, pg, pb, po, _stream_of(stream, DN_PTR_DEVICE))
+    return _check("dn_prefill", rc, check)
 
 
 def dn_destroy(layer) -> None:

@@ -28,6 +28,8 @@ struct dn_layer {
     // (state copies wait for it); not recorded while that stream captures
     cudaEvent_t step_done;
     int step_done_pending;
+    dn::PrefillDev P;  // dn_prefill's scratch (allocated on its first call)
+    int prefill_ready;
     size_t bytes;
     std::vector<void *> allocs;
 };
@@ -440,6 +442,104 @@ DN_API int dn_get_state(dn_layer *l, int seq0, int n, float *S, float *ring, int
     return DN_OK;
 }
 
+namespace {
+
+// dn_prefill's scratch, for blocks of up to kPrefillCols token columns
+int ensure_prefill(dn_layer *l) {
+    if (l->prefill_ready) return DN_OK;
+    const dn::Dims &d = l->d;
+    dn::PrefillDev &P = l->P;
+    const size_t C = dn::kPrefillCols;
+    size_t part_in = 0, part_out = 0, tiles_in = 0, tiles_out = 0;
+    for (int c = 1; c <= (int)C; ++c) {
+        const dn::GemmPlan gi = dn::plan_tc_gemm(d.proj_rows, d.hidden, c);
+        const dn::GemmPlan go = dn::plan_tc_gemm(d.hidden, d.v_dim, c);
+        part_in = std::max(part_in, (size_t)gi.tiles * gi.max_seg * 64 * 128);
+        part_out = std::max(part_out, (size_t)go.tiles * go.max_seg * 64 * 128);
+        tiles_in = std::max(tiles_in, (size_t)gi.tiles);
+        tiles_out = std::max(tiles_out, (size_t)go.tiles);
+    }
+    const size_t chunks = (C + 63) / 64;
+    const size_t kt_in = (size_t)(d.hidden + dn::kTileK - 1) / dn::kTileK;
+    const size_t kt_out = (size_t)(d.v_dim + dn::kTileK - 1) / dn::kTileK;
+    int rc = DN_OK;
+#define PALLOC(ptr, bytes) \
+    if (rc == DN_OK) rc = layer_alloc(l, (void **)&(ptr), (size_t)(bytes));
+    PALLOC(P.xg, C * d.hidden * 4);
+    PALLOC(P.xb_in, chunks * kt_in * dn::kOpTile);
+    PALLOC(P.part_in, part_in * 4);
+    PALLOC(P.nseg_in, tiles_in * 4);
+    PALLOC(P.xin, C * d.proj_rows * 4);
+    PALLOC(P.qn, C * d.qk_dim * 4);
+    PALLOC(P.kn, C * d.qk_dim * 4);
+    PALLOC(P.vv, C * d.v_dim * 4);
+    PALLOC(P.zs, C * d.v_dim * 4);
+    PALLOC(P.gg, C * d.n_v * d.gw * 4);
+    PALLOC(P.bb, C * d.n_v * 4);
+    PALLOC(P.o, C * d.v_dim * 4);
+    PALLOC(P.nrm, C * d.v_dim * 4);
+    PALLOC(P.xb_out, chunks * kt_out * dn::kOpTile);
+    PALLOC(P.part_out, part_out * 4);
+    PALLOC(P.nseg_out, tiles_out * 4);
+#undef PALLOC
+    if (rc != DN_OK) return rc;  // (what was allocated stays with the layer and is freed with it)
+    // the padded operand rows must read as zero
+    if (cudaMemsetAsync(P.xb_in, 0, chunks * kt_in * dn::kOpTile, l->stream) != cudaSuccess ||
+        cudaMemsetAsync(P.xb_out, 0, chunks * kt_out * dn::kOpTile, l->stream) != cudaSuccess ||
+        cudaStreamSynchronize(l->stream) != cudaSuccess)
+        return DN_ECUDA;
+    l->prefill_ready = 1;
+    return DN_OK;
+}
+
+// after work enqueued on a stream other than the layer's: state copies wait
+// for it (a stream that captures a graph is ordered by whoever launches it)
+cudaError_t note_foreign_stream(dn_layer *l, cudaStream_t st) {
+    if (st == l->stream) return cudaSuccess;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(st, &cs);
+    if (e == cudaSuccess && cs == cudaStreamCaptureStatusNone) {
+        e = cudaEventRecord(l->step_done, st);
+        if (e == cudaSuccess) l->step_done_pending = 1;
+    }
+    return e;
+}
+
+}  // namespace
+
+DN_API int dn_prefill(dn_layer *l, int batch, int n_tokens, const float *x, const float *g, const float *beta,
+                      float *out, void *stream) {
+    if (l == nullptr) return DN_EINVAL;
+    const dn::Dims &d = l->d;
+    if (batch < 1 || batch > d.max_batch || n_tokens < 1) return DN_EINVAL;
+    if (x == nullptr || out == nullptr) return DN_EINVAL;
+    if (((uintptr_t)x & 15u) != 0) return DN_EINVAL;  // rows are gathered with 16-byte loads
+    if (d.dev_gates ? (g != nullptr || beta != nullptr) : (g == nullptr || beta == nullptr)) return DN_EINVAL;
+    if ((size_t)batch * n_tokens > (size_t)INT32_MAX / 4) return DN_EINVAL;
+    if (!on_layer_device(l)) return DN_EINVAL;
+    if (l->failed) return DN_EFAILED;
+    if (l->fail_next != 0) {
+        const int code = l->fail_next;
+        l->fail_next = 0;
+        l->failed = 1;
+        return code;
+    }
+    const int rc = ensure_prefill(l);
+    if (rc == DN_ECUDA) return cuda_fail(l);
+    if (rc != DN_OK) return rc;
+    cudaStream_t st = stream != nullptr ? (cudaStream_t)stream : l->stream;
+    for (int b0 = 0; b0 < batch; b0 += dn::kPrefillCols) {
+        const int nb = std::min(dn::kPrefillCols, batch - b0);
+        const int T = std::max(1, dn::kPrefillCols / nb);
+        for (int t0 = 0; t0 < n_tokens; t0 += T) {
+            const dn::PrefillBlock blk{b0, nb, t0, std::min(T, n_tokens - t0), n_tokens, x, g, beta, out};
+            DN_TRY(l, dn::launch_prefill_block(d, l->L, l->P, blk, st));
+        }
+    }
+    DN_TRY(l, note_foreign_stream(l, st));
+    return DN_OK;
+}
+
 DN_API int dn_step(dn_layer *l, int batch, const float *x, const float *g, const float *beta,
                    float *out, int ptr_kind, void *stream) {
     if (l == nullptr) return DN_EINVAL;
@@ -504,16 +604,7 @@ DN_API int dn_step(dn_layer *l, int batch, const float *x, const float *g, const
     DN_TRY(l, dn::launch_splitk_reduce(L.part_out, L.nseg_out, L.s_out, od, d.hidden, d.v_dim, batch,
                                        L.rpos, d.conv_k, st));
     if (prof) DN_TRY(l, cudaEventRecord(l->prof[4], st));
-    if (st != l->stream) {
-        // let later state copies on the layer's stream wait for this step
-        // (a step captured into a graph is ordered by whoever launches it)
-        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-        DN_TRY(l, cudaStreamIsCapturing(st, &cs));
-        if (cs == cudaStreamCaptureStatusNone) {
-            DN_TRY(l, cudaEventRecord(l->step_done, st));
-            l->step_done_pending = 1;
-        }
-    }
+    DN_TRY(l, note_foreign_stream(l, st));  // later state copies wait for this step
     if (ptr_kind == DN_PTR_HOST) {
         DN_TRY(l, cudaMemcpyAsync(out, L.out_stage, (size_t)batch * d.hidden * 4, cudaMemcpyDeviceToHost, st));
         DN_TRY(l, cudaStreamSynchronize(st));

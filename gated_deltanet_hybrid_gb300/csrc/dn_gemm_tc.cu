@@ -587,19 +587,23 @@ __global__ void pack_b_kernel(const float *__restrict__ x, uint8_t *__restrict__
     }
 }
 
-// y[b][m] = s[m] * (sum of the tile's segment partials, in slot order)
-// Also advances the ring positions of `rpos` (block 0), once per step.
+// y[row(j)][m] = s[m] * (sum of the tile's segment partials, in slot order)
+// for column j of the projection; row(j) = (j / T) * Sr + t0 + j % T (a
+// decode step: T = Sr = 1, t0 = 0, row(j) = j; a block of T prompt tokens
+// of each sequence: the token's row of the [sequence][token] output).
+// Also advances the ring positions of `rpos` by `adv` (block 0) for the
+// B / T sequences of the launch.
 __global__ void splitk_reduce_kernel(const float *__restrict__ part, const int *__restrict__ nseg_tab,
                                      const float *__restrict__ s, float *__restrict__ y,
                                      SchedView sv, int M, int B, int32_t *__restrict__ rpos,
-                                     int conv_k) {
+                                     int conv_k, int T, int Sr, int t0, int adv) {
     pdl_trigger();  // the next step's first kernels may be launched already
     pdl_wait();
     if (rpos != nullptr && blockIdx.x == 0 && blockIdx.y == 0) {
-        for (int b = threadIdx.x; b < B; b += blockDim.x) {
+        for (int b = threadIdx.x; b < B / T; b += blockDim.x) {
             int2 q = reinterpret_cast<int2 *>(rpos)[b];
-            q.x = (q.x + 1) % conv_k;
-            q.y = (q.y + 1) % (conv_k - 1);
+            q.x = (q.x + adv) % conv_k;
+            q.y = (q.y + adv) % (conv_k - 1);
             reinterpret_cast<int2 *>(rpos)[b] = q;
         }
     }
@@ -615,7 +619,8 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ part, const int *
     float acc = 0.f;
 #pragma unroll 8
     for (int k = 0; k < nseg; ++k) acc += __ldcg(pt + (size_t)k * (NB_CHUNK * BM));
-    y[(size_t)(chunk * NB_CHUNK + b) * M + m] = s[m] * acc;
+    const int j = chunk * NB_CHUNK + b;
+    y[(size_t)((j / T) * Sr + t0 + j % T) * M + m] = s[m] * acc;
 }
 
 }  // namespace
@@ -699,7 +704,8 @@ cudaError_t launch_gemm_i8_tc(const uint8_t *Wt, const uint8_t *xb, float *part,
 }
 
 cudaError_t launch_splitk_reduce(const float *part, const int *nseg, const float *s, float *y, int M,
-                                 int K, int B, int32_t *rpos_advance, int conv_k, cudaStream_t st) {
+                                 int K, int B, int32_t *rpos_advance, int conv_k, cudaStream_t st, int T,
+                                 int Sr, int t0, int adv) {
     const GemmPlan g = plan_tc_gemm(M, K, B);
     const SchedView sv{g.U, g.G, g.UT, g.MT, g.max_seg};
     cudaLaunchConfig_t cfg = {};
@@ -709,7 +715,7 @@ cudaError_t launch_splitk_reduce(const float *part, const int *nseg, const float
     PdlAttr pdl;
     pdl.apply(cfg);
     return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, part, nseg, s, y, sv, M, B, rpos_advance,
-                              conv_k);
+                              conv_k, T, Sr, t0, adv);
 }
 
 }  // namespace dn

@@ -56,6 +56,37 @@ struct LayerDev {
     int *err;              // device-side error word (bounded waits that gave up)
 };
 
+// Prompt processing (dn_prefill) works on blocks of up to kPrefillCols token
+// columns: nb sequences x T tokens each, column j = sequence j / T, token
+// j % T of the block.  Its scratch is allocated on the first dn_prefill call.
+constexpr int kPrefillCols = 256;
+struct PrefillDev {
+    float *xg;                 // [cols][hidden] the block's x rows
+    uint8_t *xb_in;            // packed bf16 hi/lo tiles of xg (tensor-core in_proj)
+    float *part_in;            // in_proj segment partials, and their counts
+    int *nseg_in;
+    float *xin;                // [cols][proj_rows] in_proj output, scaled
+    float *qn, *kn;            // [nb][n_qk][T][dk] normalised q (times q_scale) and k
+    float *vv, *zs;            // [nb][n_v][T][dv] v after conv + SiLU, silu(z)
+    float *gg, *bb;            // [nb][n_v][T][gw] log-decays, [nb][n_v][T] write strengths
+    float *o;                  // [nb][n_v][T][dv] readouts
+    float *nrm;                // [cols][v_dim] gated-norm output (CUDA-core out_proj)
+    uint8_t *xb_out;           // its packed tiles (tensor-core out_proj)
+    float *part_out;
+    int *nseg_out;
+};
+
+// One block of a prompt: sequences [b0, b0 + nb) of the layer, tokens
+// [t0, t0 + T) of S; x, g, beta, out are the caller's [batch][S][...] arrays
+// (g, beta NULL with device gates).
+struct PrefillBlock {
+    int b0, nb, t0, T, S;
+    const float *x, *g, *beta;
+    float *out;
+};
+cudaError_t launch_prefill_block(const Dims &d, const LayerDev &L, const PrefillDev &P, const PrefillBlock &blk,
+                                 cudaStream_t st);
+
 // Weight tiles used by every projection kernel: W [M][K] int8 is stored as
 // [ceil(M/128)][ceil(K/64)][4 k parts][128 rows][16 int8], zero-padded, one
 // 8 KB contiguous block per (m tile, k tile); k part p holds k 16p..16p+15 of
@@ -89,9 +120,13 @@ GemmPlan plan_tc_gemm(int M, int K, int B);
 cudaError_t launch_pack_b(const float *x, uint8_t *xb, int B, int K, cudaStream_t st);
 cudaError_t launch_gemm_i8_tc(const uint8_t *Wt, const uint8_t *xb, float *part, int *nseg, int *err,
                               int M, int K, int B, cudaStream_t st);
-// y = s * (sum of partials); also advances ring positions (rpos_advance != NULL)
+// y = s * (sum of partials); also advances ring positions (rpos_advance !=
+// NULL).  Column j of the projection goes to row (j / T) * Sr + t0 + j % T of
+// y and the B / T sequences' ring positions advance by `adv` (decode: the
+// defaults, row j, one step).
 cudaError_t launch_splitk_reduce(const float *part, const int *nseg, const float *s, float *y, int M,
-                                 int K, int B, int32_t *rpos_advance, int conv_k, cudaStream_t st);
+                                 int K, int B, int32_t *rpos_advance, int conv_k, cudaStream_t st, int T = 1,
+                                 int Sr = 1, int t0 = 0, int adv = 1);
 constexpr int kTcMinBatch = 8;
 constexpr size_t kOpTile = 16384;  // bytes of one packed B-operand tile (64 seqs x 64 k, hi+lo)
 // Byte offset, inside a packed B-operand tile (128 operand rows x 64 bf16;

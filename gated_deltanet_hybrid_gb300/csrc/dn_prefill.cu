@@ -1,0 +1,459 @@
+// Prompt processing: S > 1 tokens of each sequence through one layer, with
+// the result of S decode steps (the page "qwen36: run the DeltaNet layer end
+// to end on the card (Q36_DN_GPU=1)", section "What the PR does", keeps a
+// prompt on its batched CPU path; here it runs on the card).
+//
+// The prompt goes through in blocks of up to kPrefillCols token columns (nb
+// sequences x T tokens).  Per block:
+//   1. the block's x rows are gathered, and the in_proj runs once over all
+//      of its columns: a real GEMM, on the tensor cores (the decode kernels
+//      with the columns as the batch; the CUDA-core GEMV below 8 columns);
+//   2. one kernel scales and sums the in_proj partials into xin;
+//   3. one kernel per (column, head) runs the causal conv over the tokens
+//      (the first K-1 reach back into the ring), SiLU, the q/k L2 norms and
+//      the query scale, silu(z) and the gates (the caller's, or from the
+//      layer's a/b rows), written head-major and token-contiguous;
+//   4. one kernel moves the ring to the block's last K-1 inputs;
+//   5. the recurrence kernel: one block per (column slice, value head,
+//      sequence) holds its dk x DJ slice of the state in registers for all T
+//      tokens (read once and written once per block instead of once per
+//      token) and walks them in order: decay, delta against the decayed
+//      state, write-back, readout over the updated state; the next token's
+//      inputs are loaded while the current one is computed;
+//   6. the gated RMSNorm of every readout, written as the out_proj's input;
+//   7. the out_proj over all columns, its reduction writing each token's row
+//      of the caller's output and advancing the ring positions by T.
+// Every reduction runs in a fixed order, so results do not depend on
+// scheduling.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "dn_internal.cuh"
+#include "dn_sched.cuh"
+
+namespace dn {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ float silu_f(float a) { return a / (1.0f + expf(-a)); }
+__device__ __forceinline__ float softplus_f(float a) { return fmaxf(a, 0.f) + log1pf(expf(-fabsf(a))); }
+__device__ __forceinline__ float sigmoid_f(float b) { return 1.0f / (1.0f + expf(-b)); }
+
+struct Geo {
+    int b0, nb, t0, T, S, cols;
+};
+
+// 1. xg[j] = x[(b0 + j / T) * S + t0 + j % T]
+__global__ void gather_rows_kernel(const float *__restrict__ x, float *__restrict__ xg, int hidden, Geo g) {
+    const int j = blockIdx.y;
+    const float4 *src = reinterpret_cast<const float4 *>(
+        x + ((size_t)(g.b0 + j / g.T) * g.S + g.t0 + j % g.T) * hidden);
+    float4 *dst = reinterpret_cast<float4 *>(xg + (size_t)j * hidden);
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < hidden / 4; i += gridDim.x * blockDim.x) dst[i] = src[i];
+}
+
+// 2. xin[j][c] = s[c] * (column j's segment partials of row c, in slot order)
+__global__ void sum_rows_kernel(const float *__restrict__ part, const int *__restrict__ nseg,
+                                const float *__restrict__ s, float *__restrict__ xin, int rows, int MT,
+                                int max_seg) {
+    pdl_wait();  // the projection before it
+    const int j = blockIdx.y;
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= rows) return;
+    const int tile = (j >> 6) * MT + (c >> 7);
+    const int ns = nseg[tile];
+    const float *pp = part + (size_t)tile * max_seg * (64 * 128) + (j & 63) * 128 + (c & 127);
+    float acc = 0.f;
+    for (int k = 0; k < ns; ++k) acc += __ldcg(pp + (size_t)k * (64 * 128));
+    xin[(size_t)j * rows + c] = s[c] * acc;
+}
+
+struct PrepParams {
+    const float *xin;      // [cols][proj_rows]
+    const float *ring;     // [max_batch][K][conv_ch]
+    const int32_t *rpos;   // [max_batch][2]
+    const float *wconv_t;  // [K][conv_ch]
+    const float *g, *beta; // caller's [batch][S][n_v][gw], [batch][S][n_v] (host gates)
+    const float *gate_A;   // [n_v] (device gates)
+    float *qn, *kn, *vv, *zs, *gg, *bb;
+    Geo geo;
+    int K, conv_ch, qk_dim, in_rows, proj_rows, n_qk, n_v, dk, dv, gw, dev_gates;
+    float l2_eps, q_scale;
+};
+
+// the conv input of channel c at block token tau of local sequence b: a block
+// column (tau >= 0) or the ring's history (tau < 0; history index tau + K - 1)
+__device__ __forceinline__ float conv_in(const PrepParams &p, int b, int tau, int c, int dpos) {
+    if (tau >= 0) return p.xin[(size_t)(b * p.geo.T + tau) * p.proj_rows + c];
+    int slot = dpos + tau + p.K - 1;
+    if (slot >= p.K) slot -= p.K;
+    return p.ring[((size_t)(p.geo.b0 + b) * p.K + slot) * p.conv_ch + c];
+}
+
+__device__ __forceinline__ float conv_silu_at(const PrepParams &p, int b, int t, int c, int dpos) {
+    float acc = 0.f;
+    for (int m = 0; m < p.K; ++m)  // tap m meets token t - (K - 1) + m; tap K-1 the current one
+        acc = fmaf(p.wconv_t[(size_t)m * p.conv_ch + c], conv_in(p, b, t - (p.K - 1) + m, c, dpos), acc);
+    return silu_f(acc);
+}
+
+__device__ __forceinline__ float block_sum(float v, float *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int w = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) red[w] = v;
+    __syncthreads();
+    float t = 0.f;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) t += red[i];  // fixed order
+    __syncthreads();
+    return t;
+}
+
+// 3. grid (n_qk + n_v, cols): block x < n_qk is q/k head x of column j;
+// the others value head x - n_qk (v, silu(z), gates).  dk, dv <= 256 = threads.
+__global__ void __launch_bounds__(kThreads) prep_kernel(const PrepParams p) {
+    __shared__ float red[kThreads / 32];
+    const int j = blockIdx.y, b = j / p.geo.T, t = j % p.geo.T;
+    const int dpos = p.rpos[2 * (p.geo.b0 + b)];
+    const int i = threadIdx.x;
+    const int T = p.geo.T;
+    if ((int)blockIdx.x < p.n_qk) {
+        const int hq = blockIdx.x;
+        float uq = 0.f, uk = 0.f;
+        if (i < p.dk) {
+            uq = conv_silu_at(p, b, t, hq * p.dk + i, dpos);
+            uk = conv_silu_at(p, b, t, p.qk_dim + hq * p.dk + i, dpos);
+        }
+        const float sq = block_sum(uq * uq, red), sk = block_sum(uk * uk, red);
+        if (i < p.dk) {
+            const size_t o = (((size_t)b * p.n_qk + hq) * T + t) * p.dk + i;
+            p.qn[o] = uq * (1.0f / sqrtf(sq + p.l2_eps)) * p.q_scale;
+            p.kn[o] = uk * (1.0f / sqrtf(sk + p.l2_eps));
+        }
+        return;
+    }
+    const int h = blockIdx.x - p.n_qk;
+    const size_t hv = ((size_t)b * p.n_v + h) * T + t;
+    if (i < p.dv) {
+        p.vv[hv * p.dv + i] = conv_silu_at(p, b, t, 2 * p.qk_dim + h * p.dv + i, dpos);
+        p.zs[hv * p.dv + i] = silu_f(p.xin[(size_t)j * p.proj_rows + p.conv_ch + h * p.dv + i]);
+    }
+    const size_t tok = (size_t)(p.geo.b0 + b) * p.geo.S + p.geo.t0 + t;  // the caller's row
+    for (int k = i; k < p.gw; k += kThreads) {
+        p.gg[hv * p.gw + k] =
+            p.dev_gates ? -p.gate_A[h] * softplus_f(p.xin[(size_t)j * p.proj_rows + p.in_rows + h * p.gw + k])
+                        : p.g[(tok * p.n_v + h) * p.gw + k];
+    }
+    if (i == 0)
+        p.bb[hv] = p.dev_gates ? sigmoid_f(p.xin[(size_t)j * p.proj_rows + p.in_rows + p.n_v * p.gw + h])
+                               : p.beta[tok * p.n_v + h];
+}
+
+// 4. the ring after the block: the last K-1 of (history ++ the block's
+// inputs), at the slots the advanced ring position (dpos + T) names.  One
+// thread per (sequence, channel) reads everything before it writes.
+__global__ void ring_block_kernel(const float *__restrict__ xin, float *__restrict__ ring,
+                                  const int32_t *__restrict__ rpos, Geo g, int K, int conv_ch, int proj_rows) {
+    const int b = blockIdx.y;
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= conv_ch) return;
+    const int dpos = rpos[2 * (g.b0 + b)];
+    float *rb = ring + (size_t)(g.b0 + b) * K * conv_ch + c;
+    float hist[7], nw[7];  // K <= 8
+    for (int m = 0; m < K - 1; ++m) {
+        int slot = dpos + m;
+        if (slot >= K) slot -= K;
+        hist[m] = rb[(size_t)slot * conv_ch];
+    }
+    for (int m = 0; m < K - 1; ++m) {  // combined index T + m of history (K-1) ++ block (T)
+        const int ci = g.T + m;
+        nw[m] = ci < K - 1 ? hist[ci] : xin[(size_t)(b * g.T + ci - (K - 1)) * proj_rows + c];
+    }
+    const int dn = (dpos + g.T) % K;
+    for (int m = 0; m < K - 1; ++m) {
+        int slot = dn + m;
+        if (slot >= K) slot -= K;
+        rb[(size_t)slot * conv_ch] = nw[m];
+    }
+}
+
+// 5. the recurrence over the block's T tokens for one column slice of one
+// value head of one sequence: the dk x 32 slice of the state lives in
+// registers (thread: rows r0 + 32 i, columns 4 c4 .. 4 c4 + 3).
+constexpr int DJ = 32;
+
+struct RecParams {
+    float *S;  // layer state [max_batch][n_v][dk][dv]
+    const float *qn, *kn, *vv, *gg, *bb;
+    float *o;
+    Geo geo;
+    int n_v, n_qk, group, dv, gw;
+};
+
+template <int DK>
+__global__ void __launch_bounds__(kThreads, 2) recur_kernel(const RecParams p) {
+    constexpr int LPR = DJ / 4;          // 8 lanes across a row of the slice
+    constexpr int RPP = kThreads / LPR;  // 32 rows per pass
+    constexpr int NP = DK / RPP;         // float4 of the state per thread
+    static_assert(NP >= 1 && DK % RPP == 0, "tile");
+    __shared__ __align__(16) float red[2][RPP][DJ];
+    __shared__ __align__(16) float delta_s[DJ];
+
+    const int tid = threadIdx.x;
+    const int jc = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int hq = h / p.group, col0 = jc * DJ, T = p.geo.T;
+    const int c4 = tid % LPR, r0 = tid / LPR;
+    float *Sh = p.S + ((size_t)(p.geo.b0 + b) * p.n_v + h) * DK * p.dv + col0 + c4 * 4;
+    float4 s[NP];
+#pragma unroll
+    for (int i = 0; i < NP; ++i) s[i] = *reinterpret_cast<const float4 *>(Sh + (size_t)(r0 + i * RPP) * p.dv);
+
+    const float *qb = p.qn + ((size_t)b * p.n_qk + hq) * T * DK;
+    const float *kb = p.kn + ((size_t)b * p.n_qk + hq) * T * DK;
+    const size_t hv = ((size_t)b * p.n_v + h) * T;
+    // token t's inputs for this thread: its rows of k^, q^ and the decay,
+    // and (threads < 32) its column of v and the write strength
+    float kr[NP], qr[NP], eg[NP], vj = 0.f, bt = 0.f;
+    float nkr[NP], nqr[NP], neg[NP], nvj = 0.f, nbt = 0.f;
+    auto load = [&](int t, float *k_, float *q_, float *e_, float &v_, float &b_) {
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+            const int r = r0 + i * RPP;
+            k_[i] = kb[(size_t)t * DK + r];
+            q_[i] = qb[(size_t)t * DK + r];
+            e_[i] = p.gg[(hv + t) * p.gw + (p.gw == 1 ? 0 : r)];
+        }
+        if (tid < DJ) {
+            v_ = p.vv[(hv + t) * p.dv + col0 + tid];
+            b_ = p.bb[hv + t];
+        }
+    };
+    load(0, nkr, nqr, neg, nvj, nbt);
+    for (int t = 0; t < T; ++t) {
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+            kr[i] = nkr[i];
+            qr[i] = nqr[i];
+            eg[i] = expf(neg[i]);
+        }
+        vj = nvj;
+        bt = nbt;
+        if (t + 1 < T) load(t + 1, nkr, nqr, neg, nvj, nbt);
+        // decay, then what the decayed state predicts for k
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+            s[i].x *= eg[i];
+            s[i].y *= eg[i];
+            s[i].z *= eg[i];
+            s[i].w *= eg[i];
+            acc.x = fmaf(s[i].x, kr[i], acc.x);
+            acc.y = fmaf(s[i].y, kr[i], acc.y);
+            acc.z = fmaf(s[i].z, kr[i], acc.z);
+            acc.w = fmaf(s[i].w, kr[i], acc.w);
+        }
+        *reinterpret_cast<float4 *>(&red[0][r0][c4 * 4]) = acc;
+        __syncthreads();
+        if (tid < DJ) {  // delta against the decayed state
+            float kv = 0.f;
+#pragma unroll 8
+            for (int r = 0; r < RPP; ++r) kv += red[0][r][tid];
+            delta_s[tid] = bt * (vj - kv);
+        }
+        __syncthreads();
+        // write-back and the readout partials over the updated state
+        const float4 d4 = *reinterpret_cast<const float4 *>(&delta_s[c4 * 4]);
+        acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+            s[i].x = fmaf(kr[i], d4.x, s[i].x);
+            s[i].y = fmaf(kr[i], d4.y, s[i].y);
+            s[i].z = fmaf(kr[i], d4.z, s[i].z);
+            s[i].w = fmaf(kr[i], d4.w, s[i].w);
+            acc.x = fmaf(s[i].x, qr[i], acc.x);
+            acc.y = fmaf(s[i].y, qr[i], acc.y);
+            acc.z = fmaf(s[i].z, qr[i], acc.z);
+            acc.w = fmaf(s[i].w, qr[i], acc.w);
+        }
+        *reinterpret_cast<float4 *>(&red[1][r0][c4 * 4]) = acc;
+        __syncthreads();
+        if (tid < DJ) {
+            float o = 0.f;
+#pragma unroll 8
+            for (int r = 0; r < RPP; ++r) o += red[1][r][tid];
+            p.o[(hv + t) * p.dv + col0 + tid] = o;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < NP; ++i) *reinterpret_cast<float4 *>(Sh + (size_t)(r0 + i * RPP) * p.dv) = s[i];
+}
+
+// 6. gated RMSNorm of every readout of the block: fp32 rows for the CUDA-core
+// out_proj, or bf16 hi/lo B-operand tiles (column j = operand rows 2j, 2j+1
+// of its 64-column chunk) for the tensor-core one.  grid (n_v, cols).
+__global__ void __launch_bounds__(kThreads) norm_block_kernel(const float *__restrict__ o, const float *__restrict__ zs,
+                                                              const float *__restrict__ w_norm, float *__restrict__ nrm,
+                                                              uint8_t *__restrict__ xb_out, Geo g, int n_v, int dv,
+                                                              int v_dim, int kt_out, float norm_eps) {
+    __shared__ float red[kThreads / 32];
+    const int h = blockIdx.x, j = blockIdx.y, b = j / g.T, t = j % g.T;
+    const size_t row = (((size_t)b * n_v + h) * g.T + t) * dv;
+    const int i = threadIdx.x;
+    const float ov = i < dv ? o[row + i] : 0.f;
+    const float ss = block_sum(ov * ov, red);
+    if (i >= dv) return;
+    const float n = ov * (1.0f / sqrtf(ss / (float)dv + norm_eps)) * w_norm[i] * zs[row + i];
+    const int k = h * dv + i;
+    if (xb_out == nullptr) {
+        nrm[(size_t)j * v_dim + k] = n;
+    } else {
+        const __nv_bfloat16 hi = __float2bfloat16_rn(n);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(n - __bfloat162float(hi));
+        uint8_t *ot = xb_out + ((size_t)(j >> 6) * kt_out + (k >> 6)) * kOpTile;
+        const int kc = (k & 63) >> 3, e = k & 7;
+        const int rh = 2 * (j & 63), rl = rh + 1;
+        *reinterpret_cast<__nv_bfloat16 *>(ot + op_chunk_offset(rh, kc) + e * 2) = hi;
+        *reinterpret_cast<__nv_bfloat16 *>(ot + op_chunk_offset(rl, kc) + e * 2) = lo;
+    }
+}
+
+template <int DK>
+cudaError_t launch_recur(const RecParams &rp, int dv, int n_v, int nb, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(dv / DJ), (unsigned)n_v, (unsigned)nb);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = st;
+    return cudaLaunchKernelEx(&cfg, recur_kernel<DK>, rp);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_block(const Dims &d, const LayerDev &L, const PrefillDev &P, const PrefillBlock &blk,
+                                 cudaStream_t st) {
+    const Geo g{blk.b0, blk.nb, blk.t0, blk.T, blk.S, blk.nb * blk.T};
+    const int cols = g.cols;
+    const bool tc = cols >= kTcMinBatch;
+    cudaError_t e;
+    // 1. the block's x rows, the in_proj over all columns
+    {
+        cudaLaunchConfig_t c = {};
+        c.gridDim = dim3((unsigned)((d.hidden / 4 + 255) / 256), (unsigned)cols);
+        c.blockDim = dim3(256);
+        c.stream = st;
+        if ((e = cudaLaunchKernelEx(&c, gather_rows_kernel, blk.x, P.xg, d.hidden, g)) != cudaSuccess) return e;
+    }
+    if (tc) {
+        if ((e = launch_pack_b(P.xg, P.xb_in, cols, d.hidden, st)) != cudaSuccess) return e;
+        e = launch_gemm_i8_tc(L.w_in, P.xb_in, P.part_in, P.nseg_in, L.err, d.proj_rows, d.hidden, cols, st);
+    } else {
+        e = launch_gemv_i8(L.w_in, P.xg, P.part_in, P.nseg_in, L.err, d.proj_rows, d.hidden, cols, st);
+    }
+    if (e != cudaSuccess) return e;
+    // 2. scaled rows
+    {
+        const GemmPlan gp = plan_tc_gemm(d.proj_rows, d.hidden, cols);
+        cudaLaunchConfig_t c = {};
+        c.gridDim = dim3((unsigned)((d.proj_rows + 255) / 256), (unsigned)cols);
+        c.blockDim = dim3(256);
+        c.stream = st;
+        if ((e = cudaLaunchKernelEx(&c, sum_rows_kernel, (const float *)P.part_in, (const int *)P.nseg_in,
+                                    (const float *)L.s_in, P.xin, d.proj_rows, gp.MT, gp.max_seg)) != cudaSuccess)
+            return e;
+    }
+    // 3. conv, SiLU, norms, gates
+    {
+        PrepParams pp;
+        pp.xin = P.xin;
+        pp.ring = L.ring;
+        pp.rpos = L.rpos;
+        pp.wconv_t = L.wconv_t;
+        pp.g = blk.g;
+        pp.beta = blk.beta;
+        pp.gate_A = L.gate_A;
+        pp.qn = P.qn;
+        pp.kn = P.kn;
+        pp.vv = P.vv;
+        pp.zs = P.zs;
+        pp.gg = P.gg;
+        pp.bb = P.bb;
+        pp.geo = g;
+        pp.K = d.conv_k;
+        pp.conv_ch = d.conv_ch;
+        pp.qk_dim = d.qk_dim;
+        pp.in_rows = d.in_rows;
+        pp.proj_rows = d.proj_rows;
+        pp.n_qk = d.n_qk;
+        pp.n_v = d.n_v;
+        pp.dk = d.dk;
+        pp.dv = d.dv;
+        pp.gw = d.gw;
+        pp.dev_gates = d.dev_gates;
+        pp.l2_eps = d.l2_eps;
+        pp.q_scale = d.q_scale;
+        cudaLaunchConfig_t c = {};
+        c.gridDim = dim3((unsigned)(d.n_qk + d.n_v), (unsigned)cols);
+        c.blockDim = dim3(kThreads);
+        c.stream = st;
+        if ((e = cudaLaunchKernelEx(&c, prep_kernel, pp)) != cudaSuccess) return e;
+    }
+    // 4. the ring moves on by T inputs (its positions move with the reduction in 7.)
+    {
+        cudaLaunchConfig_t c = {};
+        c.gridDim = dim3((unsigned)((d.conv_ch + 255) / 256), (unsigned)blk.nb);
+        c.blockDim = dim3(256);
+        c.stream = st;
+        if ((e = cudaLaunchKernelEx(&c, ring_block_kernel, (const float *)P.xin, L.ring, (const int32_t *)L.rpos, g,
+                                    d.conv_k, d.conv_ch, d.proj_rows)) != cudaSuccess)
+            return e;
+    }
+    // 5. the recurrence
+    {
+        RecParams rp;
+        rp.S = L.S;
+        rp.qn = P.qn;
+        rp.kn = P.kn;
+        rp.vv = P.vv;
+        rp.gg = P.gg;
+        rp.bb = P.bb;
+        rp.o = P.o;
+        rp.geo = g;
+        rp.n_v = d.n_v;
+        rp.n_qk = d.n_qk;
+        rp.group = d.n_v / d.n_qk;
+        rp.dv = d.dv;
+        rp.gw = d.gw;
+        switch (d.dk) {
+            case 32: e = launch_recur<32>(rp, d.dv, d.n_v, blk.nb, st); break;
+            case 64: e = launch_recur<64>(rp, d.dv, d.n_v, blk.nb, st); break;
+            case 128: e = launch_recur<128>(rp, d.dv, d.n_v, blk.nb, st); break;
+            case 256: e = launch_recur<256>(rp, d.dv, d.n_v, blk.nb, st); break;
+            default: e = cudaErrorInvalidValue;
+        }
+        if (e != cudaSuccess) return e;
+    }
+    // 6. gated RMSNorm -> the out_proj's input
+    const int kt_out = (d.v_dim + kTileK - 1) / kTileK;
+    {
+        cudaLaunchConfig_t c = {};
+        c.gridDim = dim3((unsigned)d.n_v, (unsigned)cols);
+        c.blockDim = dim3(kThreads);
+        c.stream = st;
+        if ((e = cudaLaunchKernelEx(&c, norm_block_kernel, (const float *)P.o, (const float *)P.zs,
+                                    (const float *)L.w_norm, P.nrm, tc ? P.xb_out : (uint8_t *)nullptr, g, d.n_v,
+                                    d.dv, d.v_dim, kt_out, d.norm_eps)) != cudaSuccess)
+            return e;
+    }
+    // 7. the out_proj, each token's row of the output, ring positions + T
+    if (tc)
+        e = launch_gemm_i8_tc(L.w_out, P.xb_out, P.part_out, P.nseg_out, L.err, d.hidden, d.v_dim, cols, st);
+    else
+        e = launch_gemv_i8(L.w_out, P.nrm, P.part_out, P.nseg_out, L.err, d.hidden, d.v_dim, cols, st);
+    if (e != cudaSuccess) return e;
+    return launch_splitk_reduce(P.part_out, P.nseg_out, L.s_out, blk.out + (size_t)blk.b0 * blk.S * d.hidden,
+                                d.hidden, d.v_dim, cols, L.rpos + 2 * blk.b0, d.conv_k, st, blk.T, blk.S, blk.t0,
+                                blk.T);
+}
+
+}  // namespace dn

@@ -193,6 +193,30 @@ int dn_get_state(dn_layer *layer, int seq0, int n, float *S, float *ring, int32_
 int dn_step(dn_layer *layer, int batch, const float *x, const float *g, const float *beta,
             float *out, int ptr_kind, void *stream);
 
+/*
+ * dn_prefill — advance sequences [0, batch) by n_tokens tokens each (a
+ * prompt), with the result of n_tokens successive dn_step calls: every
+ * token's output, the state, the conv ring and ring_pos end as they would.
+ * (The page, section "What the PR does", keeps prompts on its batched CPU
+ * path; this is the same step on the card.)
+ *   x    [batch][n_tokens][hidden]          device, 16-byte aligned
+ *   g    [batch][n_tokens][n_v_heads](gw)   device (NULL with device gates)
+ *   beta [batch][n_tokens][n_v_heads]       device (NULL with device gates)
+ *   out  [batch][n_tokens][hidden]          device (written)
+ * The prompt runs in blocks of up to 256 token columns (sequences x
+ * tokens): per block the in_proj and the out_proj run once over all of its
+ * columns (tensor cores from 8 columns), and each head's state stays on chip
+ * for all of the block's tokens.  Device pointers only; the call enqueues on
+ * `stream` (NULL: the layer's stream) and returns.  The first call on a layer
+ * allocates its scratch (about 80 MB for the 35B shape; counted by
+ * dn_device_bytes, freed by dn_destroy), so make it before any stream
+ * capture.  Errors: DN_EINVAL (sizes, NULL or misaligned pointers, gates
+ * against the layer's flags, another device current), DN_ENOMEM,
+ * DN_EFAILED, DN_EINJECTED, DN_ECUDA.
+ */
+int dn_prefill(dn_layer *layer, int batch, int n_tokens, const float *x, const float *g, const float *beta,
+               float *out, void *stream);
+
 /* dn_destroy — free the layer and all its device memory.  NULL-safe.  Waits
  * for the layer's outstanding work first. */
 void dn_destroy(dn_layer *layer);

@@ -14,6 +14,7 @@ from .dn_oracle import (  # noqa: F401
     int8_rowscaled_gemv,
     l2_normalize,
     normalize_qk,
+    prefill,
     rms_prenorm,
     sigmoid,
     silu,

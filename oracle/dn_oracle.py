@@ -215,6 +215,18 @@ class OracleLayer:
         return int8_rowscaled_gemv(self.w_out64, w.s_out, normed)
 
 
+def prefill(layer: "OracleLayer", x: np.ndarray, g: np.ndarray | None = None,
+            beta: np.ndarray | None = None) -> np.ndarray:
+    """A prompt: x [B][S][hidden] (g [B][S][heads](dk), beta [B][S][heads],
+    or None with device gates) through the layer token by token, the
+    definition of processing S tokens; returns out [B][S][hidden]."""
+    B, S = x.shape[0], x.shape[1]
+    out = np.zeros((B, S, x.shape[2]), F64)
+    for t in range(S):
+        out[:, t] = layer.step(x[:, t], None if g is None else g[:, t], None if beta is None else beta[:, t])
+    return out
+
+
 def rms_prenorm(x: np.ndarray, eps: float = 1e-6) -> np.ndarray:
     """Unweighted RMSNorm of each row, used between the layers of a stack."""
     x = np.asarray(x, F64)

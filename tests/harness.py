@@ -120,3 +120,49 @@ def run_parity(wl: Workload, steps: int | None = None, sample=None, checkpoints=
     finally:
         gpu.destroy()
     return worst
+
+
+def run_prefill_parity(wl: Workload, n_tokens: int, sample=None, max_batch: int | None = None,
+                       decode_after: int = 0):
+    """A prompt of n_tokens tokens through dn_prefill (all sequences) and
+    through the oracle token by token (the sampled sequences), then
+    `decode_after` dn_step calls on both; returns the worst errors of the
+    outputs (every token), and of S and the ring at the end, and whether the
+    ring positions match."""
+    import torch
+    from oracle import OracleLayer, prefill
+
+    B = wl.batch
+    sample = np.arange(B) if sample is None else np.asarray(sample)
+    st = WorkloadStream(wl)
+    w, s0 = st.weights[0], st.states[0]
+    gpu = GpuLayer.create(wl.cfg, w, max_batch or B, s0 if wl.init_std > 0 else None)
+    ora = OracleLayer(wl.cfg, w, DNState(s0.S[sample], s0.ring[sample], s0.ring_pos[sample]))
+    steps = [st.next_step() for _ in range(n_tokens)]
+    x = np.stack([s_[0] for s_ in steps], axis=1)                       # [B][S][hidden]
+    dev = getattr(wl.cfg, "device_gates", False)
+    g = None if dev else np.stack([s_[1][0][0] for s_ in steps], axis=1)
+    beta = None if dev else np.stack([s_[1][0][1] for s_ in steps], axis=1)
+    worst = {"out": 0.0, "S": 0.0, "ring": 0.0, "ring_pos_equal": True}
+    try:
+        cuda = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).cuda()
+        out_d = torch.empty((B, n_tokens, wl.cfg.hidden), dtype=torch.float32, device="cuda")
+        abi.dn_prefill(gpu.handle, B, n_tokens, cuda(x), cuda(g), cuda(beta), out_d)
+        ref = prefill(ora, x[sample], None if g is None else g[sample], None if beta is None else beta[sample])
+        got = out_d.cpu().numpy()[sample]
+        for t in range(n_tokens):
+            worst["out"] = max(worst["out"], rel_err(got[:, t], ref[:, t]))
+        for _ in range(decode_after):
+            xs, gates = st.next_step()
+            gs, bs = gates[0]
+            o = torch.empty((B, wl.cfg.hidden), dtype=torch.float32, device="cuda")
+            abi.dn_step(gpu.handle, B, cuda(xs), cuda(gs), cuda(bs), o)
+            r = ora.step(xs[sample], None if gs is None else gs[sample], None if bs is None else bs[sample])
+            worst["out"] = max(worst["out"], rel_err(o.cpu().numpy()[sample], r))
+        gs_ = gpu.get_seqs(sample)
+        worst["S"] = rel_err(gs_.S, ora.S)
+        worst["ring"] = rel_err(gs_.ring, ora.ring)
+        worst["ring_pos_equal"] = bool(np.array_equal(gs_.ring_pos, ora.ring_pos))
+    finally:
+        gpu.destroy()
+    return worst

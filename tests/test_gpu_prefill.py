@@ -1,0 +1,59 @@
+"""GPU parity of dn_prefill (a prompt of S tokens per sequence in one call)
+against the oracle stepping the same tokens one by one: every token's output,
+and the state, the conv ring and its positions after the prompt (and after
+decode steps that follow it), within the same 2e-3 bar as the decode step."""
+import numpy as np
+import pytest
+
+from gated_deltanet_hybrid_gb300.inputs import SHAPE_35B, TINY, WORKLOADS, DNConfig, custom_workload
+
+from harness import REL_TOL, run_prefill_parity
+
+pytestmark = pytest.mark.gpu
+
+
+def _assert_ok(w):
+    assert w["out"] <= REL_TOL, w
+    assert w["S"] <= REL_TOL, w
+    assert w["ring"] <= REL_TOL, w
+    assert w["ring_pos_equal"], w
+
+
+def test_prefill_49_token_prompt_35b():
+    """The 30-layer stack's prompt length (49 tokens) on the 35B-shape layer
+    at batch 1: one block of 49 columns (tensor-core projections)."""
+    wl = custom_workload("pf49", SHAPE_35B, batch=1, steps=49, seed=3)
+    _assert_ok(run_prefill_parity(wl, 49, decode_after=3))
+
+
+def test_prefill_2048_token_prompt_batch8():
+    """The long-prompt workload as one prompt: batch 8, 2048 tokens with
+    exp(g) in [0.9, 1] (64 blocks of 8 x 32 columns), sequences 0 and 7
+    recomputed by the oracle."""
+    wl = WORKLOADS["long_prompt_b8"]
+    _assert_ok(run_prefill_parity(wl, 2048, sample=np.array([0, 7])))
+
+
+@pytest.mark.parametrize("batch,n_tokens", [(1, 1), (1, 7), (3, 100), (5, 60), (64, 9), (300, 2)])
+def test_prefill_tiny_blocks(batch, n_tokens):
+    """Block shapes: one token, fewer than 8 columns (CUDA-core projections),
+    ragged last blocks (3 x 100 -> 85 + 15 tokens), 64 sequences, more than
+    256 sequences (two sequence groups); random initial state, so the first
+    tokens' convolution reads the ring."""
+    wl = custom_workload("pft", TINY, batch=batch, steps=n_tokens, seed=40 + batch, init_std=0.1)
+    sample = np.array(sorted({0, batch // 2, batch - 1}))
+    _assert_ok(run_prefill_parity(wl, n_tokens, sample=sample, decode_after=2))
+
+
+@pytest.mark.parametrize("dims", [
+    dict(hidden=256, n_qk_heads=1, n_v_heads=2, dk=256, dv=128, conv_k=3),
+    dict(hidden=128, n_qk_heads=2, n_v_heads=6, dk=64, dv=32, conv_k=2),
+    dict(hidden=256, n_qk_heads=2, n_v_heads=4, dk=32, dv=256, conv_k=5),
+    dict(hidden=256, n_qk_heads=2, n_v_heads=4, dk=128, dv=128, key_gate=True),
+    dict(hidden=256, n_qk_heads=2, n_v_heads=4, dk=128, dv=128, device_gates=True),
+    dict(hidden=256, n_qk_heads=2, n_v_heads=4, dk=32, dv=32, key_gate=True, device_gates=True),
+])
+def test_prefill_other_dimensions_and_gates(dims):
+    cfg = DNConfig(**dims)
+    wl = custom_workload("pfd", cfg, batch=3, steps=40, seed=60, init_std=0.05)
+    _assert_ok(run_prefill_parity(wl, 40, decode_after=2))
