@@ -592,6 +592,50 @@ def bench_stack(cfg, batches, n_layers, steps, warmup, seed, use_graph, dist_ctx
     return res
 
 
+def bench_prefill(cfg, B, S, n_layers, seed, dist_ctx, torch, abi, init_std=0.0, repeats_min=3):
+    """Prompts through dn_prefill: each timed region runs one prompt of S
+    tokens for all B sequences on each of n_layers layer objects (distinct
+    weights and states, so consecutive prompts do not find each other's data
+    in L2), replayed from a CUDA graph.  Returns the median ms per prompt."""
+    dev = torch.device("cuda")
+    layers = setup_layers(cfg, B, n_layers, init_std, seed, torch, abi)
+    rng = np.random.Generator(np.random.PCG64(seed + 11))
+    x = torch.from_numpy(rng.standard_normal((B, S, cfg.hidden)).astype(np.float32)).to(dev)
+    g, beta = gates_from_ab(rng.standard_normal((B, S, cfg.n_v_heads)), rng.standard_normal((B, S, cfg.n_v_heads)))
+    g, beta = torch.from_numpy(g).to(dev), torch.from_numpy(beta).to(dev)
+    out = torch.empty((B, S, cfg.hidden), dtype=torch.float32, device=dev)
+
+    def run(i):
+        abi.dn_prefill(layers[i % n_layers], B, S, x, g, beta, out)
+
+    for i in range(n_layers):  # first calls allocate the prefill scratch
+        run(i)
+    torch.cuda.synchronize()
+    graph = capture_steps(n_layers, run, torch)
+
+    def region():
+        if graph is not None:
+            graph.replay()
+        else:
+            for i in range(n_layers):
+                run(i)
+
+    ms_list, t0, t1 = timed_regions(region, n_layers, dist_ctx, torch, min_repeats=repeats_min, min_total_s=0.3)
+    # kernels per prompt: per block of up to 256 token columns, gather, (pack +)
+    # in_proj, row sums, prep, ring, recurrence, norm, out_proj, reduction
+    launches = 0
+    for b0 in range(0, B, 256):
+        nb = min(256, B - b0)
+        T = max(1, 256 // nb)
+        for t0 in range(0, S, T):
+            launches += 10 if nb * min(T, S - t0) >= 8 else 9
+    del graph
+    for h in layers:
+        abi.dn_destroy(h)
+    return {"ms": statistics.median(ms_list) / n_layers, "region": region_stats(ms_list, n_layers),
+            "t_wall": (t0, t1), "launches": launches * n_layers * len(ms_list)}
+
+
 def stack_summary(cfg, B, n_layers, steps, r, n, hbm_peak):
     s = r["ms"] / 1e3
     ms_layer = r["ms"] / (steps * n_layers)
@@ -703,6 +747,14 @@ def run_ours(args, torch, dist_ctx):
         for Bs, rr in rs.items():
             line[f"stack30_b{Bs}"] = stack_summary(cs, Bs, nl, 200, rr, n, hbm_peak)
             line["gpu_launches"] += rr["launches"] * n
+        # prompts through dn_prefill: the stack's 49-token prompt at batch 1 and
+        # the long-prompt workload's 2048 tokens at batch 8, one layer
+        for key, (Bp, Sp, nl) in (("prefill_b1_s49", (1, 49, 8)), ("prefill_b8_s2048", (8, 2048, 4))):
+            rp = bench_prefill(SHAPE_35B, Bp, Sp, nl, 5, dist_ctx, torch, abi)
+            line[key] = {"tokens_per_s": n * Bp * Sp / (rp["ms"] / 1e3), "ms_per_prompt": rp["ms"],
+                         "batch": Bp, "prompt_tokens": Sp, "layers_rotated": nl, "region": rp["region"],
+                         "api": "dn_prefill (one call per prompt), cuda graph"}
+            line["gpu_launches"] += rp["launches"] * n
     if dist_ctx.rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, B, init_std, args.cpu_seconds, args.workload)
     return line
