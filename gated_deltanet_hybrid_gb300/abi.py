@@ -23,6 +23,18 @@ DN_PTR_HOST = 0
 DN_PTR_DEVICE = 1
 DN_FLAG_KEY_GATE = 1
 DN_FLAG_DEVICE_GATES = 2
+DN_FLAG_INT4_WEIGHTS = 4
+
+
+def pack_int4(w: np.ndarray) -> np.ndarray:
+    """int4 weights (integers in [-8, 7], [rows][K], K even) in the ABI's
+    packed form: byte i of a row holds k = 2i in its low and k = 2i + 1 in
+    its high four bits, two's complement."""
+    w = np.asarray(w)
+    if w.ndim != 2 or w.shape[1] % 2 or w.min(initial=0) < -8 or w.max(initial=0) > 7:
+        raise ValueError("int4 weights: a [rows][K] array, K even, values in [-8, 7]")
+    u = (w.astype(np.int16) & 0xF).astype(np.uint8)
+    return np.ascontiguousarray((u[:, 0::2] | (u[:, 1::2] << 4)).astype(np.uint8).view(np.int8))
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdn.so")
 
@@ -152,14 +164,17 @@ def dn_create(cfg, weights, max_batch: int, stream=None, check: bool = True):
     Returns the layer handle (ctypes.c_void_p)."""
     lib = load_library()
     dev_gates = bool(getattr(cfg, "device_gates", False))
-    flags = (DN_FLAG_KEY_GATE if getattr(cfg, "key_gate", False) else 0) | (DN_FLAG_DEVICE_GATES if dev_gates else 0)
+    int4 = bool(getattr(cfg, "int4", False))
+    flags = ((DN_FLAG_KEY_GATE if getattr(cfg, "key_gate", False) else 0) | (DN_FLAG_DEVICE_GATES if dev_gates else 0)
+             | (DN_FLAG_INT4_WEIGHTS if int4 else 0))
+    mat = pack_int4 if int4 else (lambda a: np.ascontiguousarray(a, np.int8))
     c = dn_config(cfg.hidden, cfg.n_qk_heads, cfg.n_v_heads, cfg.dk, cfg.dv, cfg.conv_k,
                   int(max_batch), cfg.l2_eps, cfg.norm_eps, cfg.qscale, flags)
-    arrs = [np.ascontiguousarray(weights.w_in, np.int8), np.ascontiguousarray(weights.s_in, np.float32),
+    arrs = [mat(weights.w_in), np.ascontiguousarray(weights.s_in, np.float32),
             np.ascontiguousarray(weights.w_conv, np.float32), np.ascontiguousarray(weights.w_norm, np.float32),
-            np.ascontiguousarray(weights.w_out, np.int8), np.ascontiguousarray(weights.s_out, np.float32)]
+            mat(weights.w_out), np.ascontiguousarray(weights.s_out, np.float32)]
     if dev_gates:
-        arrs += [np.ascontiguousarray(weights.w_ab, np.int8), np.ascontiguousarray(weights.s_ab, np.float32),
+        arrs += [mat(weights.w_ab), np.ascontiguousarray(weights.s_ab, np.float32),
                  np.ascontiguousarray(weights.gate_A, np.float32)]
     w = dn_weights(*[a.ctypes.data for a in arrs])
     if stream is None:

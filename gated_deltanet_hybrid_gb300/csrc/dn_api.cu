@@ -68,12 +68,25 @@ bool valid_cfg(const dn_config *c) {
     if (c->n_v_heads % c->n_qk_heads != 0) return false;
     if (!(c->dk == 32 || c->dk == 64 || c->dk == 128 || c->dk == 256)) return false;
     if (!(c->dv == 32 || c->dv == 64 || c->dv == 128 || c->dv == 256)) return false;
-    if ((c->flags & ~(DN_FLAG_KEY_GATE | DN_FLAG_DEVICE_GATES)) != 0) return false;
+    if ((c->flags & ~(DN_FLAG_KEY_GATE | DN_FLAG_DEVICE_GATES | DN_FLAG_INT4_WEIGHTS)) != 0) return false;
     if (c->conv_k < 2 || c->conv_k > 8) return false;
     if (c->max_batch < 1 || c->max_batch > 1024) return false;
     if (!(c->l2_eps > 0.f) || !(c->norm_eps > 0.f)) return false;
     if (c->q_scale != c->q_scale) return false;  // NaN
     return true;
+}
+
+// int4 rows packed two per byte ([M][K/2], low nibble first) -> int8 [M][K]
+std::vector<int8_t> unpack_int4(const int8_t *W, int M, int K) {
+    std::vector<int8_t> out((size_t)M * K);
+    for (size_t m = 0; m < (size_t)M; ++m)
+        for (int i = 0; i < K / 2; ++i) {
+            const uint8_t byte = (uint8_t)W[m * (K / 2) + i];
+            // sign-extend each nibble: (n ^ 8) - 8
+            out[m * K + 2 * i] = (int8_t)(((byte & 0xF) ^ 8) - 8);
+            out[m * K + 2 * i + 1] = (int8_t)(((byte >> 4) ^ 8) - 8);
+        }
+    return out;
 }
 
 // W [M][K] int8 -> [ceil(M/128)][ceil(K/64)][128][64], zero-padded
@@ -182,6 +195,7 @@ DN_API int dn_create(const dn_config *cfg, const dn_weights *w, void *stream, dn
     d.gw = (cfg->flags & DN_FLAG_KEY_GATE) ? d.dk : 1;
     d.dev_gates = (cfg->flags & DN_FLAG_DEVICE_GATES) ? 1 : 0;
     d.proj_rows = d.in_rows + (d.dev_gates ? d.n_v * (d.gw + 1) : 0);
+    d.i4 = (cfg->flags & DN_FLAG_INT4_WEIGHTS) ? 1 : 0;
     l->stream = (cudaStream_t)stream;
     cudaGetDevice(&l->device);
 
@@ -196,8 +210,9 @@ DN_API int dn_create(const dn_config *cfg, const dn_weights *w, void *stream, dn
     std::vector<float> s_proj;
     const int8_t *w_in_all = w->w_in;
     const float *s_in_all = w->s_in;
+    const size_t rb = d.i4 ? (size_t)d.hidden / 2 : (size_t)d.hidden;  // bytes per in_proj row as given
     if (d.dev_gates) {
-        const size_t n_in = (size_t)d.in_rows * d.hidden, n_ab = (size_t)(d.proj_rows - d.in_rows) * d.hidden;
+        const size_t n_in = (size_t)d.in_rows * rb, n_ab = (size_t)(d.proj_rows - d.in_rows) * rb;
         w_proj.resize(n_in + n_ab);
         std::memcpy(w_proj.data(), w->w_in, n_in);
         std::memcpy(w_proj.data() + n_in, w->w_ab, n_ab);
@@ -207,8 +222,22 @@ DN_API int dn_create(const dn_config *cfg, const dn_weights *w, void *stream, dn
         w_in_all = w_proj.data();
         s_in_all = s_proj.data();
     }
+    // int4: the packed rows tile like int8 rows of K/2 bytes (128 k per 8 KB
+    // tile) for the CUDA-core GEMV, and an exact int8 expansion feeds the
+    // tensor-core path
+    std::vector<uint8_t> wt_in4, wt_out4;
+    std::vector<int8_t> w_in8, w_out8;
+    const int8_t *w_out_all = w->w_out;
+    if (d.i4) {
+        wt_in4 = tile_weights(w_in_all, d.proj_rows, d.hidden / 2);
+        wt_out4 = tile_weights(w->w_out, d.hidden, d.v_dim / 2);
+        w_in8 = unpack_int4(w_in_all, d.proj_rows, d.hidden);
+        w_out8 = unpack_int4(w->w_out, d.hidden, d.v_dim);
+        w_in_all = w_in8.data();
+        w_out_all = w_out8.data();
+    }
     const std::vector<uint8_t> wt_in = tile_weights(w_in_all, d.proj_rows, d.hidden);
-    const std::vector<uint8_t> wt_out = tile_weights(w->w_out, d.hidden, d.v_dim);
+    const std::vector<uint8_t> wt_out = tile_weights(w_out_all, d.hidden, d.v_dim);
     const size_t kt_in = (size_t)(d.hidden + dn::kTileK - 1) / dn::kTileK;
     const size_t kt_out = (size_t)(d.v_dim + dn::kTileK - 1) / dn::kTileK;
     ALLOC(L.w_in, wt_in.size());
@@ -217,6 +246,10 @@ DN_API int dn_create(const dn_config *cfg, const dn_weights *w, void *stream, dn
     ALLOC(L.wconv_t, (size_t)d.conv_k * d.conv_ch * 4);
     ALLOC(L.w_norm, (size_t)d.dv * 4);
     ALLOC(L.w_out, wt_out.size());
+    if (d.i4) {
+        ALLOC(L.w_in4, wt_in4.size());
+        ALLOC(L.w_out4, wt_out4.size());
+    }
     ALLOC(L.s_out, (size_t)d.hidden * 4);
     ALLOC(L.S, s_elems * 4);
     ALLOC(L.ring, MB * d.conv_k * d.conv_ch * 4);
@@ -234,8 +267,8 @@ DN_API int dn_create(const dn_config *cfg, const dn_weights *w, void *stream, dn
     const size_t chunks = (MB + 63) / 64;
     size_t part_in = 0, part_out = 0, tiles_in = 0, tiles_out = 0, xb_bytes_in = 0, xb_bytes_out = 0;
     for (int b = 1; b <= (int)MB; ++b) {
-        const dn::GemmPlan gi = dn::plan_tc_gemm(d.proj_rows, d.hidden, b);
-        const dn::GemmPlan go = dn::plan_tc_gemm(d.hidden, d.v_dim, b);
+        const dn::GemmPlan gi = dn::plan_tc_gemm(d.proj_rows, dn::plan_k(d, d.hidden, b), b);
+        const dn::GemmPlan go = dn::plan_tc_gemm(d.hidden, dn::plan_k(d, d.v_dim, b), b);
         part_in = std::max(part_in, (size_t)gi.tiles * gi.max_seg * 64 * 128);
         part_out = std::max(part_out, (size_t)go.tiles * go.max_seg * 64 * 128);
         tiles_in = std::max(tiles_in, (size_t)gi.tiles);
@@ -280,6 +313,8 @@ DN_API int dn_create(const dn_config *cfg, const dn_weights *w, void *stream, dn
     if (e == cudaSuccess) e = cudaMemcpyAsync(L.wconv_t, wct.data(), wct.size() * 4, H2D, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(L.w_norm, w->w_norm, (size_t)d.dv * 4, H2D, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(L.w_out, wt_out.data(), wt_out.size(), H2D, st);
+    if (e == cudaSuccess && d.i4) e = cudaMemcpyAsync(L.w_in4, wt_in4.data(), wt_in4.size(), H2D, st);
+    if (e == cudaSuccess && d.i4) e = cudaMemcpyAsync(L.w_out4, wt_out4.data(), wt_out4.size(), H2D, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(L.s_out, w->s_out, (size_t)d.hidden * 4, H2D, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(L.S, 0, s_elems * 4, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(L.ring, 0, MB * d.conv_k * d.conv_ch * 4, st);
@@ -452,8 +487,8 @@ int ensure_prefill(dn_layer *l) {
     const size_t C = dn::kPrefillCols;
     size_t part_in = 0, part_out = 0, tiles_in = 0, tiles_out = 0;
     for (int c = 1; c <= (int)C; ++c) {
-        const dn::GemmPlan gi = dn::plan_tc_gemm(d.proj_rows, d.hidden, c);
-        const dn::GemmPlan go = dn::plan_tc_gemm(d.hidden, d.v_dim, c);
+        const dn::GemmPlan gi = dn::plan_tc_gemm(d.proj_rows, dn::plan_k(d, d.hidden, c), c);
+        const dn::GemmPlan go = dn::plan_tc_gemm(d.hidden, dn::plan_k(d, d.v_dim, c), c);
         part_in = std::max(part_in, (size_t)gi.tiles * gi.max_seg * 64 * 128);
         part_out = std::max(part_out, (size_t)go.tiles * go.max_seg * 64 * 128);
         tiles_in = std::max(tiles_in, (size_t)gi.tiles);
@@ -585,8 +620,8 @@ DN_API int dn_step(dn_layer *l, int batch, const float *x, const float *g, const
         DN_TRY(l, dn::launch_gemm_i8_tc(L.w_in, L.xb_in, L.part_in, L.nseg_in, L.err, d.proj_rows,
                                         d.hidden, batch, st));
     } else {
-        DN_TRY(l, dn::launch_gemv_i8(L.w_in, xd, L.part_in, L.nseg_in, L.err, d.proj_rows, d.hidden,
-                                     batch, st));
+        DN_TRY(l, dn::launch_gemv_i8(d.i4 ? L.w_in4 : L.w_in, xd, L.part_in, L.nseg_in, L.err, d.proj_rows,
+                                     d.hidden, batch, st, d.i4 != 0));
     }
     if (prof) DN_TRY(l, cudaEventRecord(l->prof[1], st));
     if (prof) DN_TRY(l, cudaEventRecord(l->prof[2], st));  // no separate preparation kernel
@@ -599,9 +634,9 @@ DN_API int dn_step(dn_layer *l, int batch, const float *x, const float *g, const
         DN_TRY(l, dn::launch_gemm_i8_tc(L.w_out, L.xb_out, L.part_out, L.nseg_out, L.err, d.hidden,
                                         d.v_dim, batch, st));
     else
-        DN_TRY(l, dn::launch_gemv_i8(L.w_out, L.nrm, L.part_out, L.nseg_out, L.err, d.hidden,
-                                     d.v_dim, batch, st));
-    DN_TRY(l, dn::launch_splitk_reduce(L.part_out, L.nseg_out, L.s_out, od, d.hidden, d.v_dim, batch,
+        DN_TRY(l, dn::launch_gemv_i8(d.i4 ? L.w_out4 : L.w_out, L.nrm, L.part_out, L.nseg_out, L.err, d.hidden,
+                                     d.v_dim, batch, st, d.i4 != 0));
+    DN_TRY(l, dn::launch_splitk_reduce(L.part_out, L.nseg_out, L.s_out, od, d.hidden, dn::plan_k(d, d.v_dim, batch), batch,
                                        L.rpos, d.conv_k, st));
     if (prof) DN_TRY(l, cudaEventRecord(l->prof[4], st));
     DN_TRY(l, note_foreign_stream(l, st));  // later state copies wait for this step

@@ -348,7 +348,7 @@ cudaError_t launch_dn_core(const Dims &d, const LayerDev &L, int B, const float 
     cp.nseg_in = L.nseg_in;
     cp.s_in = L.s_in;
     {
-        const GemmPlan gp = plan_tc_gemm(d.proj_rows, d.hidden, B);
+        const GemmPlan gp = plan_tc_gemm(d.proj_rows, plan_k(d, d.hidden, B), B);
         cp.sv = SchedView{gp.U, gp.G, gp.UT, gp.MT, gp.max_seg};
     }
     cp.kt_out = (d.v_dim + kTileK - 1) / kTileK;

@@ -708,7 +708,7 @@ cudaError_t launch_dn_core_stream(const Dims &d, const LayerDev &L, int B, const
     p.nrm = L.nrm;
     p.xb_out = tc ? L.xb_out : nullptr;
     p.err = L.err;
-    const GemmPlan gp = plan_tc_gemm(d.proj_rows, d.hidden, B);
+    const GemmPlan gp = plan_tc_gemm(d.proj_rows, plan_k(d, d.hidden, B), B);
     p.MT = gp.MT;
     p.max_seg = gp.max_seg;
     p.n_v = d.n_v;

@@ -1,5 +1,7 @@
-// int8 row-scaled GEMV on the CUDA cores for small batches:
+// int8 (or int4) row-scaled GEMV on the CUDA cores for small batches:
 //   y[b][o] = s[o] * sum_k W[o][k] * x[b][k]
+// (int4 layers: the same 8 KB tiles hold 128 k, 32 weights per 16-byte
+// chunk, decoded exactly to fp32 in registers; the bytes to stream halve)
 //
 // The projections of the gated-DeltaNet step are int8 matrices with one fp32
 // scale per output row (page "feat(qwen36): the dense trunk places itself",
@@ -72,6 +74,20 @@ __device__ __forceinline__ void i8x4_to_f32(uint32_t w, float *f) {
     f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653)) - 8388736.0f;
 }
 
+// Exact int4 -> fp32 for the eight nibbles of a 32-bit word (byte i: k = 2i
+// in the low, k = 2i + 1 in the high nibble, two's complement): each nibble
+// n taken as n ^ 8 (= n + 8) goes into the mantissa of 2^23 as above, and
+// 2^23 + 8 comes off.
+__device__ __forceinline__ void i4x8_to_f32(uint32_t w, float *f) {
+    const uint32_t u = w ^ 0x88888888u;
+    const uint32_t lo = u & 0x0F0F0F0Fu, hi = (u >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7650 + i)) - 8388616.0f;
+        f[2 * i + 1] = __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7650 + i)) - 8388616.0f;
+    }
+}
+
 // 16-term dot product in four interleaved chains of four (fixed order)
 __device__ __forceinline__ float dot16(const float w[16], const float *xp) {
     const float4 a = *reinterpret_cast<const float4 *>(xp);
@@ -105,8 +121,10 @@ __device__ __forceinline__ void load_unit(const GemvParams &p, int u, int kp, in
     for (int i = 0; i < KU; ++i) w[i] = ld_stream(row + (size_t)min(kt0 + i, p.KTt - 1) * kTile);
 }
 
-template <int NB>
+template <int NB, bool I4>
 __global__ void __launch_bounds__(kThreads, Pipe<NB>::CTAS) gemv_i8_stream_kernel(const GemvParams p) {
+    constexpr int TK = I4 ? 128 : kTileK;  // k per tile
+    constexpr int PK = TK / 4;             // k per 16-byte part
     constexpr int D = Pipe<NB>::D;
     const int t = threadIdx.x;
     const int c = blockIdx.x;
@@ -159,16 +177,33 @@ __global__ void __launch_bounds__(kThreads, Pipe<NB>::CTAS) gemv_i8_stream_kerne
             const int kt0 = (u % KT) * KU;
 #pragma unroll
             for (int i = 0; i < KU; ++i) {
-                const int k0 = (kt0 + i) * kTileK + kp * 16;
+                const int k0 = (kt0 + i) * TK + kp * PK;
                 if (kt0 + i < p.KTt && k0 < p.K) {
-                    float fa[16];
-                    i8x4_to_f32(w[d][i].x, fa);
-                    i8x4_to_f32(w[d][i].y, fa + 4);
-                    i8x4_to_f32(w[d][i].z, fa + 8);
-                    i8x4_to_f32(w[d][i].w, fa + 12);
+                    if constexpr (!I4) {
+                        float fa[16];
+                        i8x4_to_f32(w[d][i].x, fa);
+                        i8x4_to_f32(w[d][i].y, fa + 4);
+                        i8x4_to_f32(w[d][i].z, fa + 8);
+                        i8x4_to_f32(w[d][i].w, fa + 12);
 #pragma unroll
-                    for (int jb = 0; jb < NB; ++jb)
-                        if (jb < p.B) acc[jb] += dot16(fa, p.x + (size_t)jb * p.K + k0);
+                        for (int jb = 0; jb < NB; ++jb)
+                            if (jb < p.B) acc[jb] += dot16(fa, p.x + (size_t)jb * p.K + k0);
+                    } else {
+                        // 32 weights: k0 .. k0+15 (K is a multiple of 16), then k0+16 ..
+                        float fa[16];
+                        i4x8_to_f32(w[d][i].x, fa);
+                        i4x8_to_f32(w[d][i].y, fa + 8);
+#pragma unroll
+                        for (int jb = 0; jb < NB; ++jb)
+                            if (jb < p.B) acc[jb] += dot16(fa, p.x + (size_t)jb * p.K + k0);
+                        if (k0 + 16 < p.K) {
+                            i4x8_to_f32(w[d][i].z, fa);
+                            i4x8_to_f32(w[d][i].w, fa + 8);
+#pragma unroll
+                            for (int jb = 0; jb < NB; ++jb)
+                                if (jb < p.B) acc[jb] += dot16(fa, p.x + (size_t)jb * p.K + k0 + 16);
+                        }
+                    }
                 }
             }
             // refill the slot with the unit D ahead
@@ -194,10 +229,10 @@ __global__ void __launch_bounds__(kThreads, Pipe<NB>::CTAS) gemv_i8_stream_kerne
     }
 }
 
-template <int NB>
+template <int NB, bool I4>
 cudaError_t launch_nb(const uint8_t *Wt, const float *x, float *part, int *nseg, int M, int K, int B,
                       cudaStream_t st) {
-    const GemmPlan g = plan_tc_gemm(M, K, B);
+    const GemmPlan g = plan_tc_gemm(M, I4 ? K / 2 : K, B);  // int4: 128 k per tile
     GemvParams p;
     p.Wt = Wt;
     p.x = x;
@@ -213,18 +248,25 @@ cudaError_t launch_nb(const uint8_t *Wt, const float *x, float *part, int *nseg,
     cfg.stream = st;
     PdlAttr pdl;
     pdl.apply(cfg);
-    return cudaLaunchKernelEx(&cfg, gemv_i8_stream_kernel<NB>, p);
+    return cudaLaunchKernelEx(&cfg, gemv_i8_stream_kernel<NB, I4>, p);
+}
+
+template <bool I4>
+cudaError_t launch_gemv_b(const uint8_t *Wt, const float *x, float *part, int *nseg, int M, int K, int B,
+                          cudaStream_t st) {
+    if (B == 1) return launch_nb<1, I4>(Wt, x, part, nseg, M, K, B, st);
+    if (B == 2) return launch_nb<2, I4>(Wt, x, part, nseg, M, K, B, st);
+    if (B <= 4) return launch_nb<4, I4>(Wt, x, part, nseg, M, K, B, st);
+    return launch_nb<8, I4>(Wt, x, part, nseg, M, K, B, st);
 }
 
 }  // namespace
 
 cudaError_t launch_gemv_i8(const uint8_t *Wt, const float *x, float *part, int *nseg, int *err,
-                           int M, int K, int B, cudaStream_t st) {
+                           int M, int K, int B, cudaStream_t st, bool i4) {
     (void)err;  // no waits: nothing to report
-    if (B == 1) return launch_nb<1>(Wt, x, part, nseg, M, K, B, st);
-    if (B == 2) return launch_nb<2>(Wt, x, part, nseg, M, K, B, st);
-    if (B <= 4) return launch_nb<4>(Wt, x, part, nseg, M, K, B, st);
-    return launch_nb<8>(Wt, x, part, nseg, M, K, B, st);
+    return i4 ? launch_gemv_b<true>(Wt, x, part, nseg, M, K, B, st)
+              : launch_gemv_b<false>(Wt, x, part, nseg, M, K, B, st);
 }
 
 }  // namespace dn

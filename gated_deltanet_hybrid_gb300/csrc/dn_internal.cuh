@@ -32,11 +32,13 @@ struct Dims {
     int gw;  // log-decay values per head and step: dk with the per-key gate, else 1
     int dev_gates;  // the a/b gate rows follow the in_proj rows (DN_FLAG_DEVICE_GATES)
     int proj_rows;  // rows of the in_proj GEMM: in_rows, plus n_v * (gw + 1) gate rows
+    int i4;         // int4 weights (DN_FLAG_INT4_WEIGHTS)
     float l2_eps, norm_eps, q_scale;
 };
 
 struct LayerDev {
     uint8_t *w_in;  // tiled int8 (see kTileM / kTileK)
+    uint8_t *w_in4, *w_out4;  // int4 layers: the packed int4 tiles the CUDA-core GEMV streams
     float *s_in, *wconv_t, *w_norm;
     float *gate_A;  // [n_v] (device gates only)
     uint8_t *w_out;  // tiled int8
@@ -102,8 +104,10 @@ constexpr int kTileK = 64;
 // in_proj, launch_splitk_reduce for the out_proj.
 //
 // CUDA-core version for batches < kTcMinBatch (fp32 activations x [B][K]).
+// i4: Wt holds int4 tiles ([ceil(M/128)][ceil(K/128)][4 parts][128 rows][16 B],
+// each 16-byte chunk 32 weights of one row, low nibble first).
 cudaError_t launch_gemv_i8(const uint8_t *Wt, const float *x, float *part, int *nseg, int *err,
-                           int M, int K, int B, cudaStream_t st);
+                           int M, int K, int B, cudaStream_t st, bool i4 = false);
 
 // Tensor-core (tcgen05) version for batches >= kTcMinBatch: x arrives packed
 // as bf16 hi/lo B-operand tiles (launch_pack_b, or written so by the core
@@ -117,6 +121,10 @@ struct GemmPlan {
     int MT, TP, MP, KT, KU, UT, nchunks, U, G, max_seg, tiles;
 };
 GemmPlan plan_tc_gemm(int M, int K, int B);
+// The k extent a projection of `B` columns is planned with: the CUDA-core
+// GEMV of an int4 layer streams int4 tiles, 8 KB of which hold 128 k (the
+// schedule of K/2 int8 columns); every other projection plans K.
+inline int plan_k(const Dims &d, int K, int B) { return (d.i4 && B < 8) ? K / 2 : K; }
 cudaError_t launch_pack_b(const float *x, uint8_t *xb, int B, int K, cudaStream_t st);
 cudaError_t launch_gemm_i8_tc(const uint8_t *Wt, const uint8_t *xb, float *part, int *nseg, int *err,
                               int M, int K, int B, cudaStream_t st);

@@ -348,12 +348,13 @@ cudaError_t launch_prefill_block(const Dims &d, const LayerDev &L, const Prefill
         if ((e = launch_pack_b(P.xg, P.xb_in, cols, d.hidden, st)) != cudaSuccess) return e;
         e = launch_gemm_i8_tc(L.w_in, P.xb_in, P.part_in, P.nseg_in, L.err, d.proj_rows, d.hidden, cols, st);
     } else {
-        e = launch_gemv_i8(L.w_in, P.xg, P.part_in, P.nseg_in, L.err, d.proj_rows, d.hidden, cols, st);
+        e = launch_gemv_i8(d.i4 ? L.w_in4 : L.w_in, P.xg, P.part_in, P.nseg_in, L.err, d.proj_rows, d.hidden, cols,
+                           st, d.i4 != 0);
     }
     if (e != cudaSuccess) return e;
     // 2. scaled rows
     {
-        const GemmPlan gp = plan_tc_gemm(d.proj_rows, d.hidden, cols);
+        const GemmPlan gp = plan_tc_gemm(d.proj_rows, plan_k(d, d.hidden, cols), cols);
         cudaLaunchConfig_t c = {};
         c.gridDim = dim3((unsigned)((d.proj_rows + 255) / 256), (unsigned)cols);
         c.blockDim = dim3(256);
@@ -449,10 +450,11 @@ cudaError_t launch_prefill_block(const Dims &d, const LayerDev &L, const Prefill
     if (tc)
         e = launch_gemm_i8_tc(L.w_out, P.xb_out, P.part_out, P.nseg_out, L.err, d.hidden, d.v_dim, cols, st);
     else
-        e = launch_gemv_i8(L.w_out, P.nrm, P.part_out, P.nseg_out, L.err, d.hidden, d.v_dim, cols, st);
+        e = launch_gemv_i8(d.i4 ? L.w_out4 : L.w_out, P.nrm, P.part_out, P.nseg_out, L.err, d.hidden, d.v_dim, cols,
+                           st, d.i4 != 0);
     if (e != cudaSuccess) return e;
     return launch_splitk_reduce(P.part_out, P.nseg_out, L.s_out, blk.out + (size_t)blk.b0 * blk.S * d.hidden,
-                                d.hidden, d.v_dim, cols, L.rpos + 2 * blk.b0, d.conv_k, st, blk.T, blk.S, blk.t0,
+                                d.hidden, plan_k(d, d.v_dim, cols), cols, L.rpos + 2 * blk.b0, d.conv_k, st, blk.T, blk.S, blk.t0,
                                 blk.T);
 }
 

@@ -47,6 +47,7 @@ class DNConfig:
     q_scale: float | None = None  # None: 1/sqrt(dk)
     key_gate: bool = False        # per-key-channel decay: g is [n_v_heads][dk] per sequence
     device_gates: bool = False    # the a/b gate projections are int8 rows of the layer (no host gates)
+    int4: bool = False            # projection weights are per-row int4 (integers in [-8, 7]) instead of int8
 
     @property
     def gate_width(self) -> int:
@@ -108,20 +109,24 @@ class DNState:
 
 
 def make_weights(cfg: DNConfig, rng: np.random.Generator) -> DNWeights:
-    w_in = rng.integers(-127, 128, size=(cfg.in_rows, cfg.hidden), dtype=np.int8)
-    s_in = rng.uniform(0.001, 0.01, size=cfg.in_rows).astype(np.float32)
+    # int4 layers: integers in [-8, 7] (held in int8 arrays) with scales 16x
+    # larger, so that the projections' outputs have the int8 layers' size
+    lo, hi, sm = (-8, 8, 16.0) if cfg.int4 else (-127, 128, 1.0)
+    w_in = rng.integers(lo, hi, size=(cfg.in_rows, cfg.hidden), dtype=np.int8)
+    s_in = (rng.uniform(0.001, 0.01, size=cfg.in_rows) * sm).astype(np.float32)
     w_conv = rng.uniform(-0.5, 0.5, size=(cfg.conv_ch, cfg.conv_k)).astype(np.float32)
     w_norm = rng.uniform(0.5, 1.5, size=cfg.dv).astype(np.float32)
-    w_out = rng.integers(-127, 128, size=(cfg.hidden, cfg.v_dim), dtype=np.int8)
-    s_out = rng.uniform(0.001, 0.01, size=cfg.hidden).astype(np.float32)
+    w_out = rng.integers(lo, hi, size=(cfg.hidden, cfg.v_dim), dtype=np.int8)
+    s_out = (rng.uniform(0.001, 0.01, size=cfg.hidden) * sm).astype(np.float32)
     w = DNWeights(w_in, s_in, w_conv, w_norm, w_out, s_out)
     if cfg.device_gates:
         # drawn last, so layers without device gates keep their draws; the row
         # scales put a and b near N(0, 1) for x ~ N(0, 1) (int8 uniform in
         # [-127, 127] has standard deviation 73.3), as the configs' a, b are;
         # A = 0.5, the configs' coefficient
-        w.w_ab = rng.integers(-127, 128, size=(cfg.gate_rows, cfg.hidden), dtype=np.int8)
-        w.s_ab = (rng.uniform(0.5, 1.5, size=cfg.gate_rows) / (73.3 * math.sqrt(cfg.hidden))).astype(np.float32)
+        w.w_ab = rng.integers(lo, hi, size=(cfg.gate_rows, cfg.hidden), dtype=np.int8)
+        sd = 4.61 if cfg.int4 else 73.3  # standard deviation of the uniform integers
+        w.s_ab = (rng.uniform(0.5, 1.5, size=cfg.gate_rows) / (sd * math.sqrt(cfg.hidden))).astype(np.float32)
         w.gate_A = np.full(cfg.n_v_heads, 0.5, np.float32)
     return w
 

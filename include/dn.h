@@ -56,6 +56,11 @@ extern "C" {
  * take no g or beta (pass NULL); the page keeps these two small projections
  * on the host and passes their values to the kernels */
 #define DN_FLAG_DEVICE_GATES 2
+/* int4 projection weights (the page's model is a per-row int4 container):
+ * w_in, w_out and w_ab hold two weights per byte, [rows][K/2]; byte i of a
+ * row holds k = 2i in its low and k = 2i + 1 in its high four bits, two's
+ * complement (values -8 .. 7), with one fp32 scale per row as for int8 */
+#define DN_FLAG_INT4_WEIGHTS 4
 
 /* ---- where a pointer argument lives ------------------------------------ */
 #define DN_PTR_HOST   0
@@ -76,7 +81,8 @@ typedef struct dn_layer dn_layer; /* opaque; owns all of its device memory */
  *   l2_eps      eps inside the square root of the q/k L2 norms (> 0)
  *   norm_eps    eps of the gated RMSNorm (> 0)
  *   q_scale     multiplies the normalised q (e.g. 1/sqrt(dk))
- *   flags       0, or DN_FLAG_KEY_GATE and / or DN_FLAG_DEVICE_GATES
+ *   flags       any combination of DN_FLAG_KEY_GATE, DN_FLAG_DEVICE_GATES,
+ *               DN_FLAG_INT4_WEIGHTS
  * Derived: conv_ch = 2*n_qk_heads*dk + n_v_heads*dv,
  *          in_rows = conv_ch + n_v_heads*dv, v_dim = n_v_heads*dv.
  */

@@ -6,6 +6,7 @@ import re
 import shutil
 import subprocess
 
+import numpy as np
 import pytest
 
 from gated_deltanet_hybrid_gb300 import abi
@@ -71,3 +72,22 @@ def test_host_side_argument_checks_need_no_gpu(lib_path):
     assert lib.dn_step_kernels(None, 1) == 0
     assert lib.dn_stack_step(None, 1, 1, None, None, None, 1e-6, None) == abi.DN_EINVAL
     lib.dn_destroy(None)  # NULL-safe
+
+
+def test_int4_packing_layout():
+    """The binding's int4 packing (the ABI's layout): byte i of a row holds
+    k = 2i in its low and k = 2i + 1 in its high nibble, two's complement;
+    checked on a hand-made row and by unpacking a random matrix with shifts."""
+    row = np.array([[1, 2, -8, -1, 7, 0]], np.int8)
+    packed = abi.pack_int4(row).view(np.uint8)
+    assert packed.tolist() == [[0x21, 0xF8, 0x07]]
+    rng = np.random.default_rng(0)
+    w = rng.integers(-8, 8, size=(5, 38)).astype(np.int8)
+    p = abi.pack_int4(w).view(np.uint8).astype(np.int16)
+    lo, hi = p & 0xF, p >> 4
+    un = np.empty_like(w, dtype=np.int16)
+    un[:, 0::2] = np.where(lo >= 8, lo - 16, lo)
+    un[:, 1::2] = np.where(hi >= 8, hi - 16, hi)
+    assert np.array_equal(un, w)
+    with pytest.raises(ValueError):
+        abi.pack_int4(np.array([[8, 0]]))

@@ -237,3 +237,50 @@ def test_device_gates_reject_host_gates():
                 assert abi.dn_step(layer.handle, 2, x, None, None, out, check=False) == abi.DN_EINVAL
         finally:
             layer.destroy()
+
+
+# ---- per-row int4 weights (the page's model container) -----------------------
+SHAPE_35B_I4 = DNConfig(hidden=2048, n_qk_heads=16, n_v_heads=32, dk=128, dv=128, int4=True)
+
+
+@pytest.mark.parametrize("batch", [1, 3, 8, 64])
+def test_int4_weights_35b(batch):
+    """int4 weights: the CUDA-core GEMV streams the packed int4 tiles (batch
+    1 and 3), the tensor-core projections their exact int8 expansion."""
+    wl = custom_workload(f"i4_b{batch}", SHAPE_35B_I4, batch=batch, steps=24, seed=440 + batch, init_std=0.02)
+    _assert_ok(run_parity(wl, sample=np.array(sorted({0, batch - 1}))))
+
+
+def test_int4_with_device_gates_and_odd_sizes():
+    """int4 in_proj with the a/b gate rows appended (16 + 64 rows past the
+    q|k|v|z rows), a hidden size that is not a multiple of 128, batch 2."""
+    cfg = DNConfig(hidden=208, n_qk_heads=2, n_v_heads=4, dk=64, dv=64, int4=True, device_gates=True)
+    wl = custom_workload("i4_odd", cfg, batch=2, steps=20, seed=444, init_std=0.05)
+    _assert_ok(run_parity(wl))
+
+
+@pytest.mark.parametrize("batch", [1, 5])
+def test_int4_in_proj_exact_integer_case(batch):
+    """Integer x in [-3, 3], int4 weights and power-of-two row scales: every
+    partial sum is an exact integer, so the ring's newest slot (the in_proj's
+    q|k|v rows) equals numpy's int64 matmul bitwise."""
+    import torch
+    from gated_deltanet_hybrid_gb300 import abi
+    from gated_deltanet_hybrid_gb300.inputs import make_weights
+    from harness import GpuLayer
+
+    cfg = SHAPE_35B_I4
+    rng = np.random.default_rng(200 + batch)
+    w = make_weights(cfg, rng)
+    w.s_in[:] = (2.0 ** rng.integers(-3, 2, size=cfg.in_rows)).astype(np.float32)
+    x = rng.integers(-3, 4, size=(batch, cfg.hidden)).astype(np.float32)
+    exact = (x.astype(np.int64) @ w.w_in.astype(np.int64).T) * w.s_in.astype(np.float64)
+    layer = GpuLayer.create(cfg, w, batch)
+    try:
+        out = torch.empty((batch, cfg.hidden), device="cuda")
+        g = torch.zeros((batch, cfg.n_v_heads), device="cuda")
+        abi.dn_step(layer.handle, batch, torch.from_numpy(x).cuda(), g, g.clone(), out)
+        newest = layer.get_state().ring[:, 0, :]
+        assert np.array_equal(newest.astype(np.float64), exact[:, :cfg.conv_ch])
+    finally:
+        layer.destroy()

@@ -57,3 +57,12 @@ def test_prefill_other_dimensions_and_gates(dims):
     cfg = DNConfig(**dims)
     wl = custom_workload("pfd", cfg, batch=3, steps=40, seed=60, init_std=0.05)
     _assert_ok(run_prefill_parity(wl, 40, decode_after=2))
+
+
+@pytest.mark.parametrize("batch,n_tokens", [(1, 5), (1, 49)])
+def test_prefill_int4(batch, n_tokens):
+    """A prompt on an int4 layer: 5 columns (the int4 GEMV) and 49 columns
+    (tensor cores on the int8 expansion)."""
+    cfg = DNConfig(hidden=2048, n_qk_heads=16, n_v_heads=32, dk=128, dv=128, int4=True)
+    wl = custom_workload("pf_i4", cfg, batch=batch, steps=n_tokens, seed=470 + n_tokens, init_std=0.02)
+    _assert_ok(run_prefill_parity(wl, n_tokens, decode_after=2))
