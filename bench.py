@@ -36,6 +36,7 @@ dn_stack_step; the line adds tokens_per_s and ms_per_token).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -65,11 +66,17 @@ STAGE_EVENTS = {"in_proj": (0, 1), "dn_state": (1, 3), "out_proj": (3, 4)}
 
 
 # --------------------------------------------------------------------- bytes
+def weight_bytes(cfg: DNConfig) -> int:
+    """The two projections' weight bytes (int8, or int4 at half a byte)."""
+    n = cfg.in_rows * cfg.hidden + cfg.hidden * cfg.v_dim
+    return n // 2 if getattr(cfg, "int4", False) else n
+
+
 def step_bytes(cfg: DNConfig, B: int) -> int:
     """Algorithmic HBM bytes of one layer-step: weights once, plus per
     sequence the state read and written, the ring's conv_k-1 slots read and
     one slot written, x, out and the two gates.  Scratch is not counted."""
-    shared = (cfg.in_rows * cfg.hidden + cfg.in_rows * 4 + cfg.hidden * cfg.v_dim + cfg.hidden * 4
+    shared = (weight_bytes(cfg) + cfg.in_rows * 4 + cfg.hidden * 4
               + cfg.conv_ch * cfg.conv_k * 4 + cfg.dv * 4)
     per_seq = (2 * cfg.n_v_heads * cfg.dk * cfg.dv * 4 + (cfg.conv_k - 1) * cfg.conv_ch * 4
                + cfg.conv_ch * 4 + 2 * cfg.hidden * 4 + 2 * cfg.n_v_heads * 4)
@@ -86,11 +93,12 @@ def kernel_bytes(cfg: DNConfig, B: int) -> dict[str, int]:
     weights, the gates, the state read and written, the gated-norm output
     out, the norm weight.  out_proj: W_out, s_out, its input in, the layer
     output out."""
-    k1 = cfg.in_rows * cfg.hidden + cfg.in_rows * 4 + B * (cfg.hidden + cfg.in_rows) * 4
+    half = 2 if getattr(cfg, "int4", False) else 1
+    k1 = cfg.in_rows * cfg.hidden // half + cfg.in_rows * 4 + B * (cfg.hidden + cfg.in_rows) * 4
     ks = (B * (cfg.in_rows * 4 + (cfg.conv_k - 1) * cfg.conv_ch * 4 + cfg.conv_ch * 4
                + 2 * cfg.n_v_heads * 4 + 2 * cfg.n_v_heads * cfg.dk * cfg.dv * 4 + cfg.v_dim * 4)
           + cfg.conv_ch * cfg.conv_k * 4 + cfg.dv * 4)
-    k3 = cfg.hidden * cfg.v_dim + cfg.hidden * 4 + B * (cfg.v_dim + cfg.hidden) * 4
+    k3 = cfg.hidden * cfg.v_dim // half + cfg.hidden * 4 + B * (cfg.v_dim + cfg.hidden) * 4
     return {"in_proj": k1, "dn_state": ks, "out_proj": k3}
 
 
@@ -526,6 +534,7 @@ WORKLOAD_SPECS = {
     "35b_b64": (SHAPE_35B, 64, 0.02),
     "35b_b1": (SHAPE_35B, 1, 0.0),
     "35b_b8": (SHAPE_35B, 8, 0.0),  # the batch of the 2048-token long-prompt parity case
+    "35b_b1_int4": (dataclasses.replace(SHAPE_35B, int4=True), 1, 0.0),  # the page's per-row int4 model
 }
 # stacks of distinct layers driven through dn_stack_step (zero initial state)
 STACK_SPECS = {
@@ -724,7 +733,7 @@ def run_ours(args, torch, dist_ctx):
                 "steps": r["n_e2e"], "api": "dn_step with pinned host pointers (copies + sync inside)"},
     }
     if args.secondary and args.workload == "35b_b64":
-        for key, wl in (("batch1", "35b_b1"), ("batch8", "35b_b8")):
+        for key, wl in (("batch1", "35b_b1"), ("batch8", "35b_b8"), ("batch1_int4", "35b_b1_int4")):
             c2, B2, std2 = WORKLOAD_SPECS[wl]
             st2 = max(args.steps, 2000)
             r2 = bench_gpu(c2, B2, std2, st2, args.warmup, args.layers, 1, True, dist_ctx, torch, abi,
@@ -747,6 +756,11 @@ def run_ours(args, torch, dist_ctx):
         for Bs, rr in rs.items():
             line[f"stack30_b{Bs}"] = stack_summary(cs, Bs, nl, 200, rr, n, hbm_peak)
             line["gpu_launches"] += rr["launches"] * n
+        # the page's measured setup: 30 layers with per-row int4 weights, batch 1
+        c4 = dataclasses.replace(cs, int4=True)
+        rr = bench_stack(c4, [1], nl, 200, 49, 3, True, dist_ctx, torch, abi)[1]
+        line["stack30_b1_int4"] = stack_summary(c4, 1, nl, 200, rr, n, hbm_peak)
+        line["gpu_launches"] += rr["launches"] * n
         # prompts through dn_prefill: the stack's 49-token prompt at batch 1 and
         # the long-prompt workload's 2048 tokens at batch 8, one layer
         for key, (Bp, Sp, nl) in (("prefill_b1_s49", (1, 49, 8)), ("prefill_b8_s2048", (8, 2048, 4))):
