@@ -582,6 +582,7 @@ DN_API int dn_step(dn_layer *l, int batch, const float *x, const float *g, const
     if (ptr_kind != DN_PTR_HOST && ptr_kind != DN_PTR_DEVICE) return DN_EINVAL;
     if (batch < 1 || batch > d.max_batch) return DN_EINVAL;
     if (x == nullptr || out == nullptr) return DN_EINVAL;
+    if (ptr_kind == DN_PTR_DEVICE && ((uintptr_t)x & 15u) != 0) return DN_EINVAL;  // read 16 bytes at a time
     if (d.dev_gates ? (g != nullptr || beta != nullptr) : (g == nullptr || beta == nullptr)) return DN_EINVAL;
     if (!on_layer_device(l)) return DN_EINVAL;
     if (l->failed) return DN_EFAILED;

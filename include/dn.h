@@ -181,7 +181,7 @@ int dn_get_state(dn_layer *layer, int seq0, int n, float *S, float *ring, int32_
  *   out  [batch][hidden]     layer output (written)
  * With DN_FLAG_DEVICE_GATES, g and beta must be NULL (the layer computes
  * them from x).
- * ptr_kind DN_PTR_DEVICE: all four are device pointers; the call only
+ * ptr_kind DN_PTR_DEVICE: all four are device pointers (x 16-byte aligned); the call only
  *   enqueues kernels on `stream` (NULL: the layer's stream) and returns; it
  *   allocates nothing and does not synchronise, so it can be captured in a
  *   CUDA graph.  x/g/beta must stay valid until the work has run.
