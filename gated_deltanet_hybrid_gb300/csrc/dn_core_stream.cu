@@ -46,11 +46,17 @@
 
 #include <algorithm>
 
+#include "dn_device.cuh"
 #include "dn_internal.cuh"
 #include "dn_sched.cuh"
 
 namespace dn {
 namespace {
+
+using dev::global_ns;
+using dev::mbar_arrive;
+using dev::smem_u32;
+using dev::warp_sum;
 
 constexpr int D = 128;               // dk = dv
 constexpr int NC = 512;              // consumer threads (16 warps)
@@ -109,14 +115,6 @@ struct __align__(128) StreamSmem {
     int failed;                 // a role gave up on a wait
 };
 
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -135,9 +133,6 @@ __device__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
     }
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 // named barrier over `n` threads
 __device__ __forceinline__ void bar_sync(int id, int n) {
@@ -166,11 +161,6 @@ __device__ __forceinline__ void load_tile(StreamSmem &sm, int st, const StreamPa
             smem_u32(sm.tile[st])),
         "l"(p.S + (size_t)item * (D * D)), "r"(kTileBytes), "r"(smem_u32(&sm.full[st]))
         : "memory");
-}
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
 }
 // silu(a) = a / (1 + e^-a) with the hardware exponential and divide
 // (__expf, __fdividef: a few ulp, far inside the step's tolerance; for

@@ -60,11 +60,19 @@
 
 #include <algorithm>
 
+#include "dn_device.cuh"
 #include "dn_internal.cuh"
 #include "dn_sched.cuh"
 
 namespace dn {
 namespace {
+
+using dev::bulk_g2s;
+using dev::global_ns;
+using dev::mbar_arrive;
+using dev::mbar_arrive_expect_tx;
+using dev::mbar_init;
+using dev::smem_u32;
 
 constexpr int BM = 128;          // weight rows per tile (MMA M)
 constexpr int BK = 64;           // k per weight tile
@@ -119,30 +127,6 @@ struct GemmParams {
                                                           // KT: k tiles; UT: units per group
 };
 
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -168,15 +152,6 @@ __device__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_fl
             if (global_ns() - t0 > kWaitLimitNs) return false;
         }
     }
-}
-
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
-                                         uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            dst),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {

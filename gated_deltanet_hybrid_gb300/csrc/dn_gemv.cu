@@ -30,11 +30,15 @@
 // and scaled by the consumer in slot order (bitwise-reproducible results).
 #include <algorithm>
 
+#include "dn_device.cuh"
 #include "dn_internal.cuh"
 #include "dn_sched.cuh"
 
 namespace dn {
 namespace {
+
+using dev::dot16;
+using dev::i8x4_to_f32;
 
 constexpr int KU = 4;                    // 64-wide k tiles per unit (32 KB of weights)
 // units in flight per thread, and CTAs per SM: one sequence leaves registers
@@ -62,21 +66,10 @@ __device__ __forceinline__ uint4 ld_stream(const uint8_t *ptr) {
     return v;
 }
 
-// Exact int8 -> fp32 for the four bytes of a 32-bit word: byte b taken as
-// u = b ^ 0x80 (= b + 128) is placed in the mantissa of 2^23 (bit pattern
-// 0x4B000000 | u, the float 8388608 + u); subtracting 8388608 + 128 is exact
-// and leaves b (binary32 holds every integer below 2^24 exactly).
-__device__ __forceinline__ void i8x4_to_f32(uint32_t w, float *f) {
-    const uint32_t u = w ^ 0x80808080u;
-    f[0] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)) - 8388736.0f;
-    f[1] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651)) - 8388736.0f;
-    f[2] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652)) - 8388736.0f;
-    f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653)) - 8388736.0f;
-}
-
 // Exact int4 -> fp32 for the eight nibbles of a 32-bit word (byte i: k = 2i
 // in the low, k = 2i + 1 in the high nibble, two's complement): each nibble
-// n taken as n ^ 8 (= n + 8) goes into the mantissa of 2^23 as above, and
+// n taken as n ^ 8 (= n + 8) goes into the mantissa of 2^23, as for int8
+// in dev::i8x4_to_f32, and
 // 2^23 + 8 comes off.
 __device__ __forceinline__ void i4x8_to_f32(uint32_t w, float *f) {
     const uint32_t u = w ^ 0x88888888u;
@@ -86,28 +79,6 @@ __device__ __forceinline__ void i4x8_to_f32(uint32_t w, float *f) {
         f[2 * i] = __uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7650 + i)) - 8388616.0f;
         f[2 * i + 1] = __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7650 + i)) - 8388616.0f;
     }
-}
-
-// 16-term dot product in four interleaved chains of four (fixed order)
-__device__ __forceinline__ float dot16(const float w[16], const float *xp) {
-    const float4 a = *reinterpret_cast<const float4 *>(xp);
-    const float4 b = *reinterpret_cast<const float4 *>(xp + 4);
-    const float4 c = *reinterpret_cast<const float4 *>(xp + 8);
-    const float4 d = *reinterpret_cast<const float4 *>(xp + 12);
-    float t0 = w[0] * a.x, t1 = w[1] * a.y, t2 = w[2] * a.z, t3 = w[3] * a.w;
-    t0 = fmaf(w[4], b.x, t0);
-    t1 = fmaf(w[5], b.y, t1);
-    t2 = fmaf(w[6], b.z, t2);
-    t3 = fmaf(w[7], b.w, t3);
-    t0 = fmaf(w[8], c.x, t0);
-    t1 = fmaf(w[9], c.y, t1);
-    t2 = fmaf(w[10], c.z, t2);
-    t3 = fmaf(w[11], c.w, t3);
-    t0 = fmaf(w[12], d.x, t0);
-    t1 = fmaf(w[13], d.y, t1);
-    t2 = fmaf(w[14], d.z, t2);
-    t3 = fmaf(w[15], d.w, t3);
-    return (t0 + t1) + (t2 + t3);
 }
 
 // this thread's 16-byte chunk of each k tile of unit u.  The loads are

@@ -20,11 +20,15 @@
 #include <algorithm>
 #include <mutex>
 
+#include "dn_device.cuh"
 #include "dn_internal.cuh"
 #include "dn_sched.cuh"
 
 namespace dn {
 namespace {
+
+using dev::dot16;
+using dev::i8x4_to_f32;
 
 constexpr int kNaKU = 4;            // k tiles per unit
 constexpr int kNaThreads = 512;     // one 16-byte chunk of a 128 x 64 tile each
@@ -47,37 +51,6 @@ struct NaParams {
     SchedView sv;      // units per row tile in sv.KT
     int M, K, KT, B;   // KT: 64-wide k tiles
 };
-
-__device__ __forceinline__ void i8x4_to_f32(uint32_t w, float *f) {
-    // byte ^ 0x80 in the mantissa of 2^23 is the float 2^23 + b + 128;
-    // subtracting 2^23 + 128 is exact and leaves the integer b
-    const uint32_t u = w ^ 0x80808080u;
-    f[0] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)) - 8388736.0f;
-    f[1] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651)) - 8388736.0f;
-    f[2] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652)) - 8388736.0f;
-    f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653)) - 8388736.0f;
-}
-
-__device__ __forceinline__ float dot16(const float w[16], const float *xp) {
-    const float4 a = *reinterpret_cast<const float4 *>(xp);
-    const float4 b = *reinterpret_cast<const float4 *>(xp + 4);
-    const float4 c = *reinterpret_cast<const float4 *>(xp + 8);
-    const float4 d = *reinterpret_cast<const float4 *>(xp + 12);
-    float t0 = w[0] * a.x, t1 = w[1] * a.y, t2 = w[2] * a.z, t3 = w[3] * a.w;
-    t0 = fmaf(w[4], b.x, t0);
-    t1 = fmaf(w[5], b.y, t1);
-    t2 = fmaf(w[6], b.z, t2);
-    t3 = fmaf(w[7], b.w, t3);
-    t0 = fmaf(w[8], c.x, t0);
-    t1 = fmaf(w[9], c.y, t1);
-    t2 = fmaf(w[10], c.z, t2);
-    t3 = fmaf(w[11], c.w, t3);
-    t0 = fmaf(w[12], d.x, t0);
-    t1 = fmaf(w[13], d.y, t1);
-    t2 = fmaf(w[14], d.z, t2);
-    t3 = fmaf(w[15], d.w, t3);
-    return (t0 + t1) + (t2 + t3);
-}
 
 // Stream-K partial sums: CTA c takes units [c*U/G, (c+1)*U/G); thread t
 // covers row t/4 and 16 of the 64 k of each k tile of a unit.
