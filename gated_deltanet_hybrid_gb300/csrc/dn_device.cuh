@@ -52,6 +52,20 @@ __device__ __forceinline__ void i8x4_to_f32(uint32_t w, float *f) {
     f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653)) - 8388736.0f;
 }
 
+// Exact int4 -> fp32 for the eight nibbles of a 32-bit word (byte i: k = 2i
+// in the low, k = 2i + 1 in the high nibble, two's complement): each nibble
+// n taken as n ^ 8 (= n + 8) goes into the mantissa of 2^23, as in
+// i8x4_to_f32, and 2^23 + 8 comes off.
+__device__ __forceinline__ void i4x8_to_f32(uint32_t w, float *f) {
+    const uint32_t u = w ^ 0x88888888u;
+    const uint32_t lo = u & 0x0F0F0F0Fu, hi = (u >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7650 + i)) - 8388616.0f;
+        f[2 * i + 1] = __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7650 + i)) - 8388616.0f;
+    }
+}
+
 // 16-term dot product of w with 16 consecutive floats at xp (16-byte
 // aligned) in four interleaved chains of four, combined in a fixed order
 __device__ __forceinline__ float dot16(const float w[16], const float *xp) {

@@ -38,6 +38,7 @@ namespace dn {
 namespace {
 
 using dev::dot16;
+using dev::i4x8_to_f32;
 using dev::i8x4_to_f32;
 
 constexpr int KU = 4;                    // 64-wide k tiles per unit (32 KB of weights)
@@ -64,21 +65,6 @@ __device__ __forceinline__ uint4 ld_stream(const uint8_t *ptr) {
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(ptr));
     return v;
-}
-
-// Exact int4 -> fp32 for the eight nibbles of a 32-bit word (byte i: k = 2i
-// in the low, k = 2i + 1 in the high nibble, two's complement): each nibble
-// n taken as n ^ 8 (= n + 8) goes into the mantissa of 2^23, as for int8
-// in dev::i8x4_to_f32, and
-// 2^23 + 8 comes off.
-__device__ __forceinline__ void i4x8_to_f32(uint32_t w, float *f) {
-    const uint32_t u = w ^ 0x88888888u;
-    const uint32_t lo = u & 0x0F0F0F0Fu, hi = (u >> 4) & 0x0F0F0F0Fu;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7650 + i)) - 8388616.0f;
-        f[2 * i + 1] = __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7650 + i)) - 8388616.0f;
-    }
 }
 
 // this thread's 16-byte chunk of each k tile of unit u.  The loads are
