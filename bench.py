@@ -58,6 +58,9 @@ from gated_deltanet_hybrid_gb300.inputs import (SHAPE_35B, WORKLOADS, DNConfig, 
 
 METRIC = "DeltaNet layer-steps/s and achieved HBM GB/s (% of roofline) at batch 1 and 64"
 UNIT = "layer-steps/s"
+# the library's projections take the tensor cores (and a packing kernel) from
+# this many columns (sequences of a step, token columns of a prompt block)
+TC_MIN_COLS = 2
 KERNELS = ("in_proj", "dn_state", "out_proj")
 # stage -> (first, last) index of the five events dn_profile_next_step records
 # (events 1 -> 2 bracket a separate preparation kernel, which this library
@@ -637,7 +640,7 @@ def bench_prefill(cfg, B, S, n_layers, seed, dist_ctx, torch, abi, init_std=0.0,
         nb = min(256, B - b0)
         T = max(1, 256 // nb)
         for t0 in range(0, S, T):
-            launches += 10 if nb * min(T, S - t0) >= 8 else 9
+            launches += 10 if nb * min(T, S - t0) >= TC_MIN_COLS else 9
     del graph
     for h in layers:
         abi.dn_destroy(h)

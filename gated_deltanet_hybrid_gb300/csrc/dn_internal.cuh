@@ -109,6 +109,14 @@ constexpr int kTileK = 64;
 cudaError_t launch_gemv_i8(const uint8_t *Wt, const float *x, float *part, int *nseg, int *err,
                            int M, int K, int B, cudaStream_t st, bool i4 = false);
 
+// Batches from kTcMinBatch sequences (or prompt columns) take the tensor-core
+// projections; below, the CUDA-core GEMV.  Measured on the 35B-shape layer:
+// at batch 1 the GEMV step takes 20.5 us against 29.6 on the tensor cores,
+// from batch 2 the tensor cores win (23.5 against 29.9 us at batch 2, 27.6
+// against 83.0 at batch 7: the GEMV's conversion and FMA work grows with the
+// batch, the tensor-core pipeline's does not).
+constexpr int kTcMinBatch = 2;
+
 // Tensor-core (tcgen05) version for batches >= kTcMinBatch: x arrives packed
 // as bf16 hi/lo B-operand tiles (launch_pack_b, or written so by the core
 // kernel).
@@ -124,7 +132,7 @@ GemmPlan plan_tc_gemm(int M, int K, int B);
 // The k extent a projection of `B` columns is planned with: the CUDA-core
 // GEMV of an int4 layer streams int4 tiles, 8 KB of which hold 128 k (the
 // schedule of K/2 int8 columns); every other projection plans K.
-inline int plan_k(const Dims &d, int K, int B) { return (d.i4 && B < 8) ? K / 2 : K; }
+inline int plan_k(const Dims &d, int K, int B) { return (d.i4 && B < kTcMinBatch) ? K / 2 : K; }
 cudaError_t launch_pack_b(const float *x, uint8_t *xb, int B, int K, cudaStream_t st);
 cudaError_t launch_gemm_i8_tc(const uint8_t *Wt, const uint8_t *xb, float *part, int *nseg, int *err,
                               int M, int K, int B, cudaStream_t st);
@@ -135,7 +143,6 @@ cudaError_t launch_gemm_i8_tc(const uint8_t *Wt, const uint8_t *xb, float *part,
 cudaError_t launch_splitk_reduce(const float *part, const int *nseg, const float *s, float *y, int M,
                                  int K, int B, int32_t *rpos_advance, int conv_k, cudaStream_t st, int T = 1,
                                  int Sr = 1, int t0 = 0, int adv = 1);
-constexpr int kTcMinBatch = 8;
 constexpr size_t kOpTile = 16384;  // bytes of one packed B-operand tile (64 seqs x 64 k, hi+lo)
 // Byte offset, inside a packed B-operand tile (128 operand rows x 64 bf16;
 // row 2b = hi, row 2b+1 = lo of sequence b), of the 16-byte chunk holding

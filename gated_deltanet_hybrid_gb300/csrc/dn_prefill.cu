@@ -7,7 +7,7 @@
 // sequences x T tokens).  Per block:
 //   1. the block's x rows are gathered, and the in_proj runs once over all
 //      of its columns: a real GEMM, on the tensor cores (the decode kernels
-//      with the columns as the batch; the CUDA-core GEMV below 8 columns);
+//      with the columns as the batch; the CUDA-core GEMV for one column);
 //   2. one kernel scales and sums the in_proj partials into xin;
 //   3. one kernel per (column, head) runs the causal conv over the tokens
 //      (the first K-1 reach back into the ring), SiLU, the q/k L2 norms and

@@ -211,7 +211,7 @@ int dn_step(dn_layer *layer, int batch, const float *x, const float *g, const fl
  *   out  [batch][n_tokens][hidden]          device (written)
  * The prompt runs in blocks of up to 256 token columns (sequences x
  * tokens): per block the in_proj and the out_proj run once over all of its
- * columns (tensor cores from 8 columns), and each head's state stays on chip
+ * columns (tensor cores from 2 columns), and each head's state stays on chip
  * for all of the block's tokens.  Device pointers only; the call enqueues on
  * `stream` (NULL: the layer's stream) and returns.  The first call on a layer
  * allocates its scratch (about 80 MB for the 35B shape; counted by

@@ -81,10 +81,11 @@ def test_35b_small_batch_in_a_layer_sized_for_64(batch):
     _assert_ok(run_parity(wl, sample=np.array(sorted({0, batch - 1})), max_batch=64))
 
 
-@pytest.mark.parametrize("batch", [8, 9, 40, 64, 65, 130])
+@pytest.mark.parametrize("batch", [2, 3, 8, 9, 40, 64, 65, 130])
 def test_tiny_tensor_core_batches(batch):
-    """Batches >= 8 take the tensor-core projections: padded batch columns
-    (9 -> 16), several 64-sequence chunks (65, 130) and split-K tiles."""
+    """Batches from 2 take the tensor-core projections: padded batch columns
+    (2, 3 -> 8; 9 -> 16), several 64-sequence chunks (65, 130) and split-K
+    tiles."""
     wl = custom_workload(f"tiny_b{batch}", TINY, batch=batch, steps=10, seed=30 + batch, init_std=0.05)
     sample = np.array(sorted({0, batch // 2, batch - 1}))
     _assert_ok(run_parity(wl, sample=sample))
@@ -246,16 +247,18 @@ SHAPE_35B_I4 = DNConfig(hidden=2048, n_qk_heads=16, n_v_heads=32, dk=128, dv=128
 @pytest.mark.parametrize("batch", [1, 3, 8, 64])
 def test_int4_weights_35b(batch):
     """int4 weights: the CUDA-core GEMV streams the packed int4 tiles (batch
-    1 and 3), the tensor-core projections their exact int8 expansion."""
+    1), the tensor-core projections their exact int8 expansion (3, 8, 64)."""
     wl = custom_workload(f"i4_b{batch}", SHAPE_35B_I4, batch=batch, steps=24, seed=440 + batch, init_std=0.02)
     _assert_ok(run_parity(wl, sample=np.array(sorted({0, batch - 1}))))
 
 
-def test_int4_with_device_gates_and_odd_sizes():
+@pytest.mark.parametrize("batch", [1, 2])
+def test_int4_with_device_gates_and_odd_sizes(batch):
     """int4 in_proj with the a/b gate rows appended (16 + 64 rows past the
-    q|k|v|z rows), a hidden size that is not a multiple of 128, batch 2."""
+    q|k|v|z rows), a hidden size that is not a multiple of 128, batch 1
+    (the int4 GEMV) and 2 (the tensor cores on the int8 expansion)."""
     cfg = DNConfig(hidden=208, n_qk_heads=2, n_v_heads=4, dk=64, dv=64, int4=True, device_gates=True)
-    wl = custom_workload("i4_odd", cfg, batch=2, steps=20, seed=444, init_std=0.05)
+    wl = custom_workload("i4_odd", cfg, batch=batch, steps=20, seed=443 + batch, init_std=0.05)
     _assert_ok(run_parity(wl))
 
 

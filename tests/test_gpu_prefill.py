@@ -36,7 +36,7 @@ def test_prefill_2048_token_prompt_batch8():
 
 @pytest.mark.parametrize("batch,n_tokens", [(1, 1), (1, 7), (3, 100), (5, 60), (64, 9), (300, 2)])
 def test_prefill_tiny_blocks(batch, n_tokens):
-    """Block shapes: one token, fewer than 8 columns (CUDA-core projections),
+    """Block shapes: one token (the CUDA-core projections), a few columns,
     ragged last blocks (3 x 100 -> 85 + 15 tokens), 64 sequences, more than
     256 sequences (two sequence groups); random initial state, so the first
     tokens' convolution reads the ring."""

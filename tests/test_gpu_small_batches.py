@@ -1,9 +1,9 @@
-"""GPU parity of small-batch decode steps (the CUDA-core projections below
-8 sequences) against the float64 oracle on the same seeded inputs: more
-(sequence, head) state items than SMs, every conv width of the streaming
-state kernel, per-key gates with int4 weights, one layer stepped at CUDA-core
-and tensor-core batch sizes in turn, and a captured CUDA graph of several
-steps replayed several times."""
+"""GPU parity of small-batch decode steps (the CUDA-core projections at one
+sequence, the tensor-core ones from two) against the float64 oracle on the
+same seeded inputs: more (sequence, head) state items than SMs, every conv
+width of the streaming state kernel, per-key gates with int4 weights, one
+layer stepped at CUDA-core and tensor-core batch sizes in turn, and a
+captured CUDA graph of several steps replayed several times."""
 import numpy as np
 import pytest
 
@@ -52,8 +52,8 @@ def _oracle_layers(cfg, w, s0, n):
 
 
 def test_cuda_core_and_tensor_core_batches_on_one_layer():
-    """Steps of 3 sequences (CUDA-core projections) and of 9 (tensor-core
-    projections) on one layer, in turn: both read and advance the same state,
+    """Steps of 1 sequence (CUDA-core projections) and of 3 and 9 (tensor-core
+    projections) on one layer, in turn: all read and advance the same state,
     ring and ring positions."""
     import torch
     cfg = DNConfig(**SMALL_128)
@@ -64,13 +64,13 @@ def test_cuda_core_and_tensor_core_batches_on_one_layer():
     ora = _oracle_layers(cfg, w, s0, 9)
     dev = torch.device("cuda")
     try:
-        assert abi.dn_step_kernels(gpu.handle, 3) == 4
-        assert abi.dn_step_kernels(gpu.handle, 9) == 5
+        assert abi.dn_step_kernels(gpu.handle, 1) == 4
+        assert abi.dn_step_kernels(gpu.handle, 3) == 5
         worst = 0.0
         for t in range(wl.steps):
             x, gates = st.next_step()
             g, beta = gates[0]
-            B = 3 if t % 3 != 2 else 9
+            B = (1, 3, 9)[t % 3]
             x_d = torch.from_numpy(np.ascontiguousarray(x[:B])).to(dev)
             g_d = torch.from_numpy(np.ascontiguousarray(g[:B])).to(dev)
             b_d = torch.from_numpy(np.ascontiguousarray(beta[:B])).to(dev)
