@@ -37,9 +37,9 @@
 namespace dn {
 namespace {
 
-using dev::dot16;
-using dev::i4x8_to_f32;
-using dev::i8x4_to_f32;
+using dev::dot16x2;
+using dev::i4x8_to_f32x2;
+using dev::i8x4_to_f32x2;
 
 constexpr int KU = 4;                    // 64-wide k tiles per unit (32 KB of weights)
 // units in flight per thread, and CTAs per SM: one sequence leaves registers
@@ -136,29 +136,31 @@ __global__ void __launch_bounds__(kThreads, Pipe<NB>::CTAS) gemv_i8_stream_kerne
             for (int i = 0; i < KU; ++i) {
                 const int k0 = (kt0 + i) * TK + kp * PK;
                 if (kt0 + i < p.KTt && k0 < p.K) {
+                    // weights as fp32 pairs and pair FMAs (dev::dot16x2: the bits
+                    // of the scalar chains in half the instructions)
                     if constexpr (!I4) {
-                        float fa[16];
-                        i8x4_to_f32(w[d][i].x, fa);
-                        i8x4_to_f32(w[d][i].y, fa + 4);
-                        i8x4_to_f32(w[d][i].z, fa + 8);
-                        i8x4_to_f32(w[d][i].w, fa + 12);
+                        uint64_t wp[8];
+                        i8x4_to_f32x2(w[d][i].x, wp[0], wp[1]);
+                        i8x4_to_f32x2(w[d][i].y, wp[2], wp[3]);
+                        i8x4_to_f32x2(w[d][i].z, wp[4], wp[5]);
+                        i8x4_to_f32x2(w[d][i].w, wp[6], wp[7]);
 #pragma unroll
                         for (int jb = 0; jb < NB; ++jb)
-                            if (jb < p.B) acc[jb] += dot16(fa, p.x + (size_t)jb * p.K + k0);
+                            if (jb < p.B) acc[jb] += dot16x2(wp, p.x + (size_t)jb * p.K + k0);
                     } else {
                         // 32 weights: k0 .. k0+15 (K is a multiple of 16), then k0+16 ..
-                        float fa[16];
-                        i4x8_to_f32(w[d][i].x, fa);
-                        i4x8_to_f32(w[d][i].y, fa + 8);
+                        uint64_t wp[8];
+                        i4x8_to_f32x2(w[d][i].x, wp);
+                        i4x8_to_f32x2(w[d][i].y, wp + 4);
 #pragma unroll
                         for (int jb = 0; jb < NB; ++jb)
-                            if (jb < p.B) acc[jb] += dot16(fa, p.x + (size_t)jb * p.K + k0);
+                            if (jb < p.B) acc[jb] += dot16x2(wp, p.x + (size_t)jb * p.K + k0);
                         if (k0 + 16 < p.K) {
-                            i4x8_to_f32(w[d][i].z, fa);
-                            i4x8_to_f32(w[d][i].w, fa + 8);
+                            i4x8_to_f32x2(w[d][i].z, wp);
+                            i4x8_to_f32x2(w[d][i].w, wp + 4);
 #pragma unroll
                             for (int jb = 0; jb < NB; ++jb)
-                                if (jb < p.B) acc[jb] += dot16(fa, p.x + (size_t)jb * p.K + k0 + 16);
+                                if (jb < p.B) acc[jb] += dot16x2(wp, p.x + (size_t)jb * p.K + k0 + 16);
                         }
                     }
                 }
