@@ -61,6 +61,8 @@ UNIT = "layer-steps/s"
 # the library's projections take the tensor cores (and a packing kernel) from
 # this many columns (sequences of a step, token columns of a prompt block)
 TC_MIN_COLS = 2
+# seconds the reference arm's --steps + --warmup steps may take
+REFERENCE_BUDGET_S = 100.0
 KERNELS = ("in_proj", "dn_state", "out_proj")
 # stage -> (first, last) index of the five events dn_profile_next_step records
 # (events 1 -> 2 bracket a separate preparation kernel, which this library
@@ -788,9 +790,17 @@ def run_reference(args, dist_ctx):
         init_std = 0.0
     else:
         cfg, B, init_std = WORKLOAD_SPECS[args.workload]
-    seq_steps, dt, used = run_oracle_pool(cfg, B, init_std, host_cores(), steps=args.steps,
-                                          warmup=args.warmup)
-    value = args.steps / dt
+    # each timed step advances n_seq of the B sequences: all of them when
+    # --steps + --warmup whole layer-steps fit the time budget, else as many
+    # as keep the run within it (at least one per host process)
+    cores = host_cores()
+    n_probe, t_probe, _ = run_oracle_pool(cfg, B, init_std, cores, steps=2, warmup=1)
+    t_layer = t_probe / 2
+    n_seq = B
+    if (args.steps + args.warmup) * t_layer > REFERENCE_BUDGET_S:
+        n_seq = max(min(cores, B), min(B, math.ceil(B * REFERENCE_BUDGET_S / ((args.steps + args.warmup) * t_layer))))
+    seq_steps, dt, used = run_oracle_pool(cfg, n_seq, init_std, cores, steps=args.steps, warmup=args.warmup)
+    value = seq_steps / dt / B
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist_ctx.world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -798,9 +808,10 @@ def run_reference(args, dist_ctx):
             "config": {"workload": args.workload, "batch": B, "hidden": cfg.hidden,
                        "v_heads": cfg.n_v_heads, "dk": cfg.dk, "dv": cfg.dv},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
-                             "sample": f"{args.steps} whole layer-steps ({seq_steps} sequence-steps) "
-                                       f"of the batch-{B} layer, sequences spread over {used} host "
-                                       f"processes (one BLAS thread each), float64 numpy oracle"},
+                             "sample": f"{args.steps} timed steps, each advancing {n_seq} of the batch-{B} "
+                                       f"layer's {B} sequences by one token ({seq_steps} sequence-steps in "
+                                       f"{dt:.1f} s), spread over {used} host processes (one BLAS thread "
+                                       f"each), float64 numpy oracle, scaled to layer-steps of batch {B}"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
