@@ -19,7 +19,9 @@
 //      tokens (read once and written once per block instead of once per
 //      token) and walks them in order: decay, delta against the decayed
 //      state, write-back, readout over the updated state; the next token's
-//      inputs are loaded while the current one is computed;
+//      inputs are loaded while the current one is computed (for 128-wide
+//      heads with one decay per head: the chunked form of the same
+//      recurrence, 5' below);
 //   6. the gated RMSNorm of every readout, written as the out_proj's input;
 //   7. the out_proj over all columns, its reduction writing each token's row
 //      of the caller's output and advancing the ring positions by T.
@@ -28,6 +30,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "dn_internal.cuh"
 #include "dn_sched.cuh"
@@ -290,6 +293,188 @@ __global__ void __launch_bounds__(kThreads, 2) recur_kernel(const RecParams p) {
     for (int i = 0; i < NP; ++i) *reinterpret_cast<float4 *>(Sh + (size_t)(r0 + i * RPP) * p.dv) = s[i];
 }
 
+// 5'. The same recurrence in chunks of kChunk tokens (dk = 128, one decay per
+// head): per chunk, with S0 the slice's state at the chunk's start, the
+// cumulative log-decay G_t of its tokens and gamma_t = exp(G_t), the delta
+// rule unrolls to
+//   u_t = beta_t (v_t - gamma_t S0^T k_t - sum_{s<t} exp(G_t - G_s) (k_t.k_s) u_s)
+//   o_t = gamma_t S0^T q_t + sum_{s<=t} exp(G_t - G_s) (q_t.k_s) u_s
+//   S   = gamma_n S0 + sum_t exp(G_n - G_t) k_t u_t^T
+// (u_t is the token's delta, beta_t (v_t - k_t^T S'_t) of the decayed state
+// S'_t; substitute S_{t-1} unrolled from S0 and collect terms).  The k.k and
+// q.k products, S0^T k and S0^T q are dense products over the chunk, the
+// lower-triangular solve for u runs in one warp (lane = column), and the
+// state takes the chunk's outer products in registers: the state is read
+// from shared memory a few times per chunk
+// instead of reduced across the CTA at every token.  Exact algebra of the
+// token recurrence; the rounding differs from it (fp32 throughout).
+constexpr int kChunk = 32;
+constexpr int kKP = 128 + 4;  // padded k / q rows: four rows a warp reads fall in distinct banks
+
+struct ChunkSmem {
+    float K[kChunk][kKP];
+    float Q[kChunk][kKP];
+    float S0[128][DJ];
+    float V[kChunk][DJ];
+    float P[kChunk][DJ];      // S0^T k_t (the slice's columns)
+    float U[kChunk][DJ];
+    float L[kChunk][kChunk];  // exp(G_t - G_s) k_t.k_s, s < t
+    float M[kChunk][kChunk];  // exp(G_t - G_s) q_t.k_s, s <= t
+    float G[kChunk], gam[kChunk], wn[kChunk], beta[kChunk];
+};
+
+__device__ __forceinline__ float dot4(const float4 a, const float4 b) {
+    return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
+}
+__device__ __forceinline__ void fma4(float4 &acc, float a, const float4 b) {
+    acc.x = fmaf(a, b.x, acc.x);
+    acc.y = fmaf(a, b.y, acc.y);
+    acc.z = fmaf(a, b.z, acc.z);
+    acc.w = fmaf(a, b.w, acc.w);
+}
+
+// grid (dv / DJ, n_v, nb); thread (r0, c4) = (tid / 8, tid % 8) holds rows
+// r0 + 32 i (i < 4), columns 4 c4 .. 4 c4 + 3 of the slice's state; thread
+// (tt, cq) (the same numbers) forms token tt's products for columns 4 cq ..
+__global__ void __launch_bounds__(kThreads, 2) recur_chunk_kernel(const RecParams p) {
+    constexpr int DK = 128;
+    extern __shared__ __align__(16) uint8_t chunk_smem[];
+    ChunkSmem &cs = *reinterpret_cast<ChunkSmem *>(chunk_smem);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int jc = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int hq = h / p.group, col0 = jc * DJ, T = p.geo.T;
+    const int c4 = tid & 7, r0 = tid >> 3;
+    const int tt = r0, cq = c4;
+    float *Sh = p.S + ((size_t)(p.geo.b0 + b) * p.n_v + h) * DK * p.dv + col0 + c4 * 4;
+    float4 s[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s[i] = *reinterpret_cast<const float4 *>(Sh + (size_t)(r0 + 32 * i) * p.dv);
+    const float *qb = p.qn + ((size_t)b * p.n_qk + hq) * T * DK;
+    const float *kb = p.kn + ((size_t)b * p.n_qk + hq) * T * DK;
+    const size_t hv = ((size_t)b * p.n_v + h) * T;
+    const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+
+    for (int c0 = 0; c0 < T; c0 += kChunk) {
+        const int n = min(kChunk, T - c0);
+        __syncthreads();  // the last chunk's reads of shared memory are done
+        // 1. the chunk's k^, q^ rows, the slice's v, the gates (tokens past n
+        //    are zero: no write, no decay), the state
+        for (int idx = tid; idx < kChunk * DK / 4; idx += kThreads) {
+            const int t = idx >> 5, r4 = idx & 31;
+            float4 kv = zero4, qv = zero4;
+            if (t < n) {
+                kv = *reinterpret_cast<const float4 *>(kb + (size_t)(c0 + t) * DK + r4 * 4);
+                qv = *reinterpret_cast<const float4 *>(qb + (size_t)(c0 + t) * DK + r4 * 4);
+            }
+            *reinterpret_cast<float4 *>(&cs.K[t][r4 * 4]) = kv;
+            *reinterpret_cast<float4 *>(&cs.Q[t][r4 * 4]) = qv;
+        }
+        {
+            float4 v4 = zero4;
+            if (tt < n) v4 = *reinterpret_cast<const float4 *>(p.vv + (hv + c0 + tt) * p.dv + col0 + cq * 4);
+            *reinterpret_cast<float4 *>(&cs.V[tt][cq * 4]) = v4;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) *reinterpret_cast<float4 *>(&cs.S0[r0 + 32 * i][c4 * 4]) = s[i];
+        if (warp == 0) {
+            float gv = lane < n ? p.gg[hv + c0 + lane] : 0.f;
+            const float bv = lane < n ? p.bb[hv + c0 + lane] : 0.f;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {  // inclusive prefix sum: G_t
+                const float y = __shfl_up_sync(0xffffffffu, gv, o);
+                if (lane >= o) gv += y;
+            }
+            const float gl = __shfl_sync(0xffffffffu, gv, n - 1);  // G of the chunk's last token
+            cs.G[lane] = gv;
+            cs.gam[lane] = expf(gv);
+            cs.wn[lane] = expf(gl - gv);
+            cs.beta[lane] = bv;
+        }
+        __syncthreads();
+        // 2. L, M (token tt against tokens cq + 8 j, j < 4: consecutive padded
+        //    rows across a quarter-warp, no bank conflicts), P = S0^T k_tt and
+        //    S0^T q_tt (one read of S0 for both)
+        float4 oi = zero4;
+        {
+            float a[4] = {0.f, 0.f, 0.f, 0.f}, m[4] = {0.f, 0.f, 0.f, 0.f};
+            float4 pacc = zero4;
+#pragma unroll 4
+            for (int r = 0; r < DK; r += 4) {
+                const float4 kt = *reinterpret_cast<const float4 *>(&cs.K[tt][r]);
+                const float4 qt = *reinterpret_cast<const float4 *>(&cs.Q[tt][r]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float4 ks = *reinterpret_cast<const float4 *>(&cs.K[cq + 8 * j][r]);
+                    a[j] += dot4(kt, ks);
+                    m[j] += dot4(qt, ks);
+                }
+                const float4 s0 = *reinterpret_cast<const float4 *>(&cs.S0[r][cq * 4]);
+                const float4 s1 = *reinterpret_cast<const float4 *>(&cs.S0[r + 1][cq * 4]);
+                const float4 s2 = *reinterpret_cast<const float4 *>(&cs.S0[r + 2][cq * 4]);
+                const float4 s3 = *reinterpret_cast<const float4 *>(&cs.S0[r + 3][cq * 4]);
+                fma4(pacc, kt.x, s0);
+                fma4(pacc, kt.y, s1);
+                fma4(pacc, kt.z, s2);
+                fma4(pacc, kt.w, s3);
+                fma4(oi, qt.x, s0);
+                fma4(oi, qt.y, s1);
+                fma4(oi, qt.z, s2);
+                fma4(oi, qt.w, s3);
+            }
+            const float gt = cs.G[tt];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int si = cq + 8 * j;
+                const float e = expf(gt - cs.G[si]);
+                cs.L[tt][si] = si < tt ? e * a[j] : 0.f;
+                cs.M[tt][si] = si <= tt ? e * m[j] : 0.f;
+            }
+            *reinterpret_cast<float4 *>(&cs.P[tt][cq * 4]) = pacc;
+        }
+        __syncthreads();
+        // 3. warp 0: the triangular solve for u (lane = column)
+        if (warp == 0) {
+            float u[kChunk];
+#pragma unroll
+            for (int t = 0; t < kChunk; ++t) {
+                float acc = fmaf(-cs.gam[t], cs.P[t][lane], cs.V[t][lane]);
+#pragma unroll
+                for (int s2 = 0; s2 < t; ++s2) acc = fmaf(-cs.L[t][s2], u[s2], acc);
+                u[t] = cs.beta[t] * acc;
+                cs.U[t][lane] = u[t];
+            }
+        }
+        __syncthreads();
+        // 4. the readouts o_tt, and the state after the chunk
+        {
+            const float gt = cs.gam[tt];
+            float4 o4 = make_float4(gt * oi.x, gt * oi.y, gt * oi.z, gt * oi.w);
+#pragma unroll 8
+            for (int s2 = 0; s2 < kChunk; ++s2)
+                fma4(o4, cs.M[tt][s2], *reinterpret_cast<const float4 *>(&cs.U[s2][cq * 4]));
+            if (tt < n) *reinterpret_cast<float4 *>(p.o + (hv + c0 + tt) * p.dv + col0 + cq * 4) = o4;
+        }
+        {
+            const float gn = cs.gam[n - 1];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                s[i].x *= gn;
+                s[i].y *= gn;
+                s[i].z *= gn;
+                s[i].w *= gn;
+            }
+            for (int t = 0; t < n; ++t) {
+                const float4 u4 = *reinterpret_cast<const float4 *>(&cs.U[t][c4 * 4]);
+                const float w = cs.wn[t];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) fma4(s[i], cs.K[t][r0 + 32 * i] * w, u4);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) *reinterpret_cast<float4 *>(Sh + (size_t)(r0 + 32 * i) * p.dv) = s[i];
+}
+
 // 6. gated RMSNorm of every readout of the block: fp32 rows for the CUDA-core
 // out_proj, or bf16 hi/lo B-operand tiles (column j = operand rows 2j, 2j+1
 // of its 64-column chunk) for the tensor-core one.  grid (n_v, cols).
@@ -317,6 +502,21 @@ __global__ void __launch_bounds__(kThreads) norm_block_kernel(const float *__res
         *reinterpret_cast<__nv_bfloat16 *>(ot + op_chunk_offset(rh, kc) + e * 2) = hi;
         *reinterpret_cast<__nv_bfloat16 *>(ot + op_chunk_offset(rl, kc) + e * 2) = lo;
     }
+}
+
+cudaError_t launch_recur_chunk(const RecParams &rp, int dv, int n_v, int nb, cudaStream_t st) {
+    static std::atomic<uint64_t> attr_done{0};
+    const cudaError_t e = once_per_device(attr_done, [&](int) {
+        return cudaFuncSetAttribute(recur_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)sizeof(ChunkSmem));
+    });
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(dv / DJ), (unsigned)n_v, (unsigned)nb);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = sizeof(ChunkSmem);
+    cfg.stream = st;
+    return cudaLaunchKernelEx(&cfg, recur_chunk_kernel, rp);
 }
 
 template <int DK>
@@ -425,7 +625,9 @@ cudaError_t launch_prefill_block(const Dims &d, const LayerDev &L, const Prefill
         rp.group = d.n_v / d.n_qk;
         rp.dv = d.dv;
         rp.gw = d.gw;
-        switch (d.dk) {
+        if (d.dk == 128 && d.gw == 1)  // one decay per head: the chunked form
+            e = launch_recur_chunk(rp, d.dv, d.n_v, blk.nb, st);
+        else switch (d.dk) {
             case 32: e = launch_recur<32>(rp, d.dv, d.n_v, blk.nb, st); break;
             case 64: e = launch_recur<64>(rp, d.dv, d.n_v, blk.nb, st); break;
             case 128: e = launch_recur<128>(rp, d.dv, d.n_v, blk.nb, st); break;

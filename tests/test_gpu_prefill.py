@@ -21,7 +21,8 @@ def _assert_ok(w):
 
 def test_prefill_49_token_prompt_35b():
     """The 30-layer stack's prompt length (49 tokens) on the 35B-shape layer
-    at batch 1: one block of 49 columns (tensor-core projections)."""
+    at batch 1: one block of 49 columns (tensor-core projections, the chunked
+    recurrence over a chunk of 32 tokens and one of 17)."""
     wl = custom_workload("pf49", SHAPE_35B, batch=1, steps=49, seed=3)
     _assert_ok(run_prefill_parity(wl, 49, decode_after=3))
 
@@ -32,6 +33,16 @@ def test_prefill_2048_token_prompt_batch8():
     recomputed by the oracle."""
     wl = WORKLOADS["long_prompt_b8"]
     _assert_ok(run_prefill_parity(wl, 2048, sample=np.array([0, 7])))
+
+
+@pytest.mark.parametrize("batch,n_tokens", [(1, 96), (2, 70)])
+def test_prefill_chunked_recurrence_random_state(batch, n_tokens):
+    """The chunked recurrence (128-dim heads, one decay per head) from a
+    random initial state: whole chunks (96 = 3 x 32 tokens in one block) and
+    a ragged last chunk (2 x 70 columns: 70 = 2 x 32 + 6 tokens)."""
+    cfg = DNConfig(hidden=256, n_qk_heads=2, n_v_heads=4, dk=128, dv=128)
+    wl = custom_workload("pfc", cfg, batch=batch, steps=n_tokens, seed=90 + n_tokens, init_std=0.05)
+    _assert_ok(run_prefill_parity(wl, n_tokens, decode_after=2))
 
 
 @pytest.mark.parametrize("batch,n_tokens", [(1, 1), (1, 7), (3, 100), (5, 60), (64, 9), (300, 2)])
@@ -59,10 +70,11 @@ def test_prefill_other_dimensions_and_gates(dims):
     _assert_ok(run_prefill_parity(wl, 40, decode_after=2))
 
 
-@pytest.mark.parametrize("batch,n_tokens", [(1, 5), (1, 49)])
+@pytest.mark.parametrize("batch,n_tokens", [(1, 1), (1, 5), (1, 49)])
 def test_prefill_int4(batch, n_tokens):
-    """A prompt on an int4 layer: 5 columns (the int4 GEMV) and 49 columns
-    (tensor cores on the int8 expansion)."""
+    """A prompt on an int4 layer: one column (the int4 GEMV), 5 and 49
+    columns (tensor cores on the int8 expansion; the chunked recurrence with
+    a partial chunk, and a full and a partial one)."""
     cfg = DNConfig(hidden=2048, n_qk_heads=16, n_v_heads=32, dk=128, dv=128, int4=True)
     wl = custom_workload("pf_i4", cfg, batch=batch, steps=n_tokens, seed=470 + n_tokens, init_std=0.02)
     _assert_ok(run_prefill_parity(wl, n_tokens, decode_after=2))
