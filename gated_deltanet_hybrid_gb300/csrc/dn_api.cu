@@ -287,6 +287,7 @@ DN_API int dn_create(const dn_config *cfg, const dn_weights *w, void *stream, dn
     ALLOC(L.xb_in, xb_bytes_in);
     ALLOC(L.xb_out, xb_bytes_out);
     ALLOC(L.err, 4);
+    ALLOC(L.pool, 4);
 #undef ALLOC
     if (rc == DN_OK && cudaEventCreateWithFlags(&l->step_done, cudaEventDisableTiming) != cudaSuccess) {
         (void)cudaGetLastError();
@@ -322,6 +323,7 @@ DN_API int dn_create(const dn_config *cfg, const dn_weights *w, void *stream, dn
     if (e == cudaSuccess && xb_bytes_in) e = cudaMemsetAsync(L.xb_in, 0, xb_bytes_in, st);
     if (e == cudaSuccess && xb_bytes_out) e = cudaMemsetAsync(L.xb_out, 0, xb_bytes_out, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(L.err, 0, 4, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(L.pool, 0, 4, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) {
         layer_free_all(l);
@@ -638,7 +640,7 @@ DN_API int dn_step(dn_layer *l, int batch, const float *x, const float *g, const
         DN_TRY(l, dn::launch_gemv_i8(d.i4 ? L.w_out4 : L.w_out, L.nrm, L.part_out, L.nseg_out, L.err, d.hidden,
                                      d.v_dim, batch, st, d.i4 != 0));
     DN_TRY(l, dn::launch_splitk_reduce(L.part_out, L.nseg_out, L.s_out, od, d.hidden, dn::plan_k(d, d.v_dim, batch), batch,
-                                       L.rpos, d.conv_k, st));
+                                       L.rpos, d.conv_k, st, 1, 1, 0, 1, L.pool));
     if (prof) DN_TRY(l, cudaEventRecord(l->prof[4], st));
     DN_TRY(l, note_foreign_stream(l, st));  // later state copies wait for this step
     if (ptr_kind == DN_PTR_HOST) {

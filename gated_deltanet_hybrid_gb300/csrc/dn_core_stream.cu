@@ -7,7 +7,14 @@
 // one (sequence, value head) item at a time.  Organised for HBM streaming:
 //
 //  * one CTA per SM walks a contiguous range of items (b-major, so the two
-//    value heads of a q/k head follow each other);
+//    value heads of a q/k head follow each other); at large batches the
+//    ranges are shorter than an even split and the rest of the items form a
+//    pool handed out one at a time (an atomic counter, asked one item before
+//    the answer is needed), so CTAs whose state streams run slower take
+//    fewer items and all of them finish together.  The thread that issues
+//    the tile copies publishes each position's item in a four-slot queue in
+//    shared memory (one mbarrier per slot) for the producer warps; the step's
+//    last kernel puts the counter back to zero;
 //  * each item's 64 KB state tile arrives by one cp.async.bulk copy on an
 //    mbarrier into a 3-deep shared-memory ring;
 //  * 16 consumer warps (512 threads) read the tile into registers (32 values
@@ -69,6 +76,9 @@ constexpr int RPP = NC / LPR;        // 16 rows per pass
 constexpr int NP = D / RPP;          // 8 float4 per consumer thread
 constexpr int PV = 4;                // partial slots loaded unconditionally (more are read on the spot)
 constexpr int kMaxSeqCta = 64;       // sequences one CTA's item range may touch
+// pool items per CTA: with at least kPoolPerCta + 4 items per CTA, each CTA's
+// own range is that many items shorter than an even share
+constexpr int kPoolPerCta = 3;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 // named barriers (0 is __syncthreads)
 constexpr int kBarCons = 1;          // the 512 consumer threads
@@ -95,6 +105,11 @@ struct StreamParams {
     int dev_gates, in_rows; // g, beta from the a/b gate rows that follow the in_rows in_proj rows
     const float *gate_A;   // [n_v] (device gates)
     float l2_eps, q_scale, norm_eps;
+    // item pool (nullptr: every CTA takes an even share of the items):
+    // CTA c takes items [c * n_static, (c + 1) * n_static), then pool items
+    // pool_base + k for the k the counter hands it, while k < pool_n
+    int *pool;
+    int n_static, pool_base, pool_n;
 };
 
 struct __align__(128) StreamSmem {
@@ -108,7 +123,9 @@ struct __align__(128) StreamSmem {
     float o_prev[D];            // the last item's readout, normalised during the next item
     float zw_prev[D];           // its w_norm * silu(z)
     float wn[D];                // gated-RMSNorm weight
-    int dpos[kMaxSeqCta];       // ring positions of the CTA's sequences
+    int dpos[kMaxSeqCta];       // ring positions of the sequences of the CTA's own range
+    int qitem[4];               // the item at position j >= 3 (-1: none), slot (j - 3) % 4
+    uint64_t qfull[4];          // qitem slot written (one arrival by the copy thread)
     uint64_t full[STAGES];      // tile landed
     uint64_t rec_full[2];       // record built (one arrival per producer warp)
     uint64_t rec_empty[2];      // record read (one arrival per consumer warp)
@@ -182,6 +199,33 @@ __device__ __forceinline__ int ld_cg_s32(const int *ptr) {
     asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(ptr));
     return v;
 }
+// The ring position of sequence b: from shared memory for the sequences of
+// the CTA's own range, else (pool items) from global memory (written by the
+// previous step's last kernel, which has completed)
+__device__ __forceinline__ int ring_pos(const StreamParams &p, const StreamSmem &sm, int b0, int nseq, int b) {
+    const unsigned i = (unsigned)(b - b0);
+    return i < (unsigned)nseq ? sm.dpos[i] : ld_cg_s32(p.rpos + 2 * b);
+}
+
+// The item at position j of a CTA's walk, for the producer warps (-1: the
+// walk has ended): the CTA's own range, then the queue slot the copy thread
+// fills one to two items ahead of the consumers (waited for, bounded; false
+// on timeout).
+__device__ __forceinline__ bool item_at(StreamSmem &sm, int i0, int n_s, int j, int &item) {
+    if (j < n_s) {
+        item = i0 + j;
+        return true;
+    }
+    if (j < 3) {
+        item = -1;
+        return true;
+    }
+    const int q = j - 3;
+    if (!mbar_wait(&sm.qfull[q & 3], (q >> 2) & 1)) return false;
+    item = sm.qitem[q & 3];
+    return true;
+}
+
 // The loads of four channels c .. c+3 of one row kind (q, k, v or z) of an
 // item, 16 bytes each: the in_proj segment partials (the first PV slots
 // unconditionally, from clamped addresses, so no load waits for the segment
@@ -204,13 +248,14 @@ __device__ __forceinline__ float4 ld_nc4(const float *ptr) {
     return v;
 }
 
+// (dp: the sequence's ring position)
 template <int KC>
-__device__ __forceinline__ void load_row_fixed(const StreamParams &p, const StreamSmem &sm, int b0, int b, int c,
-                                               bool conv, RowLoads<KC> &r) {
+__device__ __forceinline__ void load_row_fixed(const StreamParams &p, int dp, int b, int c, bool conv,
+                                               RowLoads<KC> &r) {
     r.sc = ld_nc4(p.s_in + c);
     if (!conv) return;  // z rows (uniform across the warp)
     const float *rb = p.ring + (size_t)b * KC * p.conv_ch + c;
-    int slot = sm.dpos[b - b0];
+    int slot = dp;
 #pragma unroll
     for (int m = 0; m < KC - 1; ++m) {  // oldest input first
         r.hist[m] = ld_cg4(rb + (size_t)slot * p.conv_ch);
@@ -258,8 +303,8 @@ __device__ __forceinline__ float4 row_value(const StreamParams &p, int b, int c,
 // conv over the history and the new input xv, then SiLU; the row's owner
 // writes xv into the ring slot that this step does not read
 template <int KC>
-__device__ __forceinline__ float4 conv_silu(const StreamParams &p, const StreamSmem &sm, int b0, int b, int c,
-                                            float4 xv, bool owner, const RowLoads<KC> &r) {
+__device__ __forceinline__ float4 conv_silu(const StreamParams &p, int dp, int b, int c, float4 xv, bool owner,
+                                            const RowLoads<KC> &r) {
     float4 cv = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int m = 0; m < KC - 1; ++m) {
@@ -273,7 +318,7 @@ __device__ __forceinline__ float4 conv_silu(const StreamParams &p, const StreamS
     cv.z = fmaf(r.wc[KC - 1].z, xv.z, cv.z);
     cv.w = fmaf(r.wc[KC - 1].w, xv.w, cv.w);
     if (owner) {
-        int ws = sm.dpos[b - b0] + KC - 1;  // the oldest slot, not read by this step
+        int ws = dp + KC - 1;  // the oldest slot, not read by this step
         if (ws >= KC) ws -= KC;
         *reinterpret_cast<float4 *>(p.ring + ((size_t)b * KC + ws) * p.conv_ch + c) = xv;
     }
@@ -378,44 +423,51 @@ __device__ __forceinline__ float4 gate_values(const StreamParams &p, int b, int 
 }
 
 // Producer warps 0-2: build the conv rows of the record (q^, k^, v) of
-// every item of the CTA's range, one item ahead of the consumers.  Warp `kind` builds
+// every item of the CTA's walk, one item ahead of the consumers.  Warp `kind` builds
 // one row kind (0 q, 1 k, 2 v), lane l channels 4l .. 4l+3 of the head,
 // so a q or k norm is one warp's sum.  The loads of item j+1 are issued as
 // soon as item j's values are computed (the registers are free again), so
-// their latency hides behind the rest of item j.
+// their latency hides behind the rest of item j.  (A failed wait ends the
+// warp's loop on all of its lanes together.)
 template <int KC>
-__device__ void produce(const StreamParams &p, StreamSmem &sm, int i0, int n_items, int b0, int kind, int lane) {
+__device__ void produce(const StreamParams &p, StreamSmem &sm, int i0, int n_s, int b0, int nseq, int kind,
+                        int lane) {
     const int cl = 4 * lane;
     constexpr bool conv = true;
     const bool qk = kind < 2;
     const int base = kind == 0 ? 0 : kind == 1 ? p.qk_dim : 2 * p.qk_dim;
-    int b = b0, h = i0 - b0 * p.n_v, hq = h / p.group;
+    int b = i0 / p.n_v, h = i0 - b * p.n_v, hq = h / p.group;
+    int dp = ring_pos(p, sm, b0, nseq, b);
     RowLoads<KC> r;
     // the first item's loads that the in_proj does not feed go out before the wait
     int c = base + (qk ? hq : h) * D + cl;
-    load_row_fixed(p, sm, b0, b, c, conv, r);
+    load_row_fixed(p, dp, b, c, conv, r);
     pdl_wait();
     load_row_part(p, b, c, r);
     bool reuse = false;  // item j has the q/k head of item j-1
-    for (int j = 0; j < n_items; ++j) {
+    for (int j = 0;; ++j) {
         const int rb = j & 1;
         c = base + (qk ? hq : h) * D + cl;
         float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
         if (!(qk && reuse)) {
             // v rows belong to one item; q/k rows are written by the q/k head's first value head
-            u = conv_silu(p, sm, b0, b, c, row_value(p, b, c, r), kind == 2 || h == hq * p.group, r);
+            u = conv_silu(p, dp, b, c, row_value(p, b, c, r), kind == 2 || h == hq * p.group, r);
         }
 
         // item j+1 and its loads
-        const int bn = h + 1 == p.n_v ? b + 1 : b, hn = h + 1 == p.n_v ? 0 : h + 1, hqn = hn / p.group;
-        const bool reuse_n = bn == b && hqn == hq;
-        if (j + 1 < n_items) {
-            if (!(qk && reuse_n)) {
-                const int cn = base + (qk ? hqn : hn) * D + cl;
-                load_row_fixed(p, sm, b0, bn, cn, conv, r);
-                load_row_part(p, bn, cn, r);
-            }
-
+        int nxt;
+        if (!__all_sync(0xffffffffu, item_at(sm, i0, n_s, j + 1, nxt))) {
+            sm.failed = 1;
+            break;
+        }
+        const int bn = nxt / p.n_v, hn = nxt - bn * p.n_v, hqn = hn / p.group;
+        const bool reuse_n = nxt >= 0 && bn == b && hqn == hq;
+        int dpn = dp;
+        if (nxt >= 0 && !(qk && reuse_n)) {
+            const int cn = base + (qk ? hqn : hn) * D + cl;
+            dpn = ring_pos(p, sm, b0, nseq, bn);
+            load_row_fixed(p, dpn, bn, cn, conv, r);
+            load_row_part(p, bn, cn, r);
         }
         float4 outv = u;
         if (qk) {
@@ -428,7 +480,7 @@ __device__ void produce(const StreamParams &p, StreamSmem &sm, int i0, int n_ite
             }
         }
         // record buffer rb is free once the consumers are done with item j-2
-        if (j >= 2 && !mbar_wait(&sm.rec_empty[rb], ((j >> 1) - 1) & 1)) {
+        if (!__all_sync(0xffffffffu, j < 2 || mbar_wait(&sm.rec_empty[rb], ((j >> 1) - 1) & 1))) {
             sm.failed = 1;
             break;
         }
@@ -436,9 +488,11 @@ __device__ void produce(const StreamParams &p, StreamSmem &sm, int i0, int n_ite
 
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.rec_full[rb]);  // release: the record's writes come first
+        if (nxt < 0) break;
         b = bn;
         h = hn;
         hq = hqn;
+        dp = dpn;
         reuse = reuse_n;
     }
 }
@@ -448,30 +502,35 @@ __device__ void produce(const StreamParams &p, StreamSmem &sm, int i0, int n_ite
 // consumers, with their loads one item ahead of their use.  Its own loop, so
 // that its registers do not add to those of the conv-row warps.
 template <int KC>
-__device__ void produce_z_gates(const StreamParams &p, StreamSmem &sm, int i0, int n_items, int b0, int lane) {
+__device__ void produce_z_gates(const StreamParams &p, StreamSmem &sm, int i0, int n_s, int lane) {
     const int cl = 4 * lane;
-    int b = b0, h = i0 - b0 * p.n_v;
+    int b = i0 / p.n_v, h = i0 - b * p.n_v;
     RowLoads<KC> r;  // (conv fields unused)
     GateLoads G;
-    load_row_fixed(p, sm, b0, b, p.conv_ch + h * D + cl, false, r);
+    load_row_fixed(p, 0, b, p.conv_ch + h * D + cl, false, r);
     load_gates_fixed(p, h, i0, cl, G);
     pdl_wait();
     load_row_part(p, b, p.conv_ch + h * D + cl, r);
     load_gates_part(p, b, h, cl, G);
-    for (int j = 0; j < n_items; ++j) {
+    for (int j = 0;; ++j) {
         const int rb = j & 1;
         const float4 xz = row_value(p, b, p.conv_ch + h * D + cl, r);
         const float4 uz = make_float4(silu_f(xz.x), silu_f(xz.y), silu_f(xz.z), silu_f(xz.w));
         float bj;
         const float4 gj = gate_values(p, b, h, cl, G, bj);
-        const int bn = h + 1 == p.n_v ? b + 1 : b, hn = h + 1 == p.n_v ? 0 : h + 1;
-        if (j + 1 < n_items) {
-            load_row_fixed(p, sm, b0, bn, p.conv_ch + hn * D + cl, false, r);
+        int nxt;
+        if (!__all_sync(0xffffffffu, item_at(sm, i0, n_s, j + 1, nxt))) {
+            sm.failed = 1;
+            break;
+        }
+        const int bn = nxt / p.n_v, hn = nxt - bn * p.n_v;
+        if (nxt >= 0) {
+            load_row_fixed(p, 0, bn, p.conv_ch + hn * D + cl, false, r);
             load_row_part(p, bn, p.conv_ch + hn * D + cl, r);
-            load_gates_fixed(p, hn, i0 + j + 1, cl, G);
+            load_gates_fixed(p, hn, nxt, cl, G);
             load_gates_part(p, bn, hn, cl, G);
         }
-        if (j >= 2 && !mbar_wait(&sm.rec_empty[rb], ((j >> 1) - 1) & 1)) {
+        if (!__all_sync(0xffffffffu, j < 2 || mbar_wait(&sm.rec_empty[rb], ((j >> 1) - 1) & 1))) {
             sm.failed = 1;
             break;
         }
@@ -480,6 +539,7 @@ __device__ void produce_z_gates(const StreamParams &p, StreamSmem &sm, int i0, i
         if (lane == 0) sm.beta[rb] = bj;
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.rec_full[rb]);
+        if (nxt < 0) break;
         b = bn;
         h = hn;
     }
@@ -490,15 +550,23 @@ __device__ void produce_z_gates(const StreamParams &p, StreamSmem &sm, int i0, i
 // updated tile goes back into its stage and leaves by one bulk store; the
 // stage takes the item STAGES ahead once that store has read it (checked
 // during the next item).  The readout's gated RMSNorm is finished by warps
-// 4-7 during the next item.  Returns the number of tile copies issued.
-__device__ int consume(const StreamParams &p, StreamSmem &sm, int i0, int n_items, int b0, int t) {
+// 4-7 during the next item.  Thread kTma also decides the item of each
+// position from 3 on (the CTA's own range, then the pool) two items ahead,
+// when it requests that item's tile, and publishes it in the queue.
+// Returns the number of tile copies issued.
+__device__ int consume(const StreamParams &p, StreamSmem &sm, int i0, int n_s, int t) {
     const int warp = t >> 5, lane = t & 31;
     const int c4 = t % LPR, r0 = t / LPR;
-    int issued = n_items < STAGES ? n_items : STAGES;
-    int b = b0, h = i0 - b0 * p.n_v, b_prev = 0, h_prev = 0;
-    int j = 0;
-    for (; j < n_items; ++j) {
-        const int item = i0 + j, st = j % STAGES, rb = j & 1;
+    int issued = n_s < STAGES ? n_s : STAGES;
+    int b_prev = 0, h_prev = 0;
+    int grab = -1;  // (thread kTma) the pool's answer for the next position to decide
+    bool clean = true;
+    for (int j = 0;; ++j) {
+        // (the queue slot was written two items ago, before a consumer barrier)
+        const int item = j < n_s ? i0 + j : j < 3 ? -1 : sm.qitem[(j - 3) & 3];
+        if (item < 0) break;
+        const int b = item / p.n_v, h = item - b * p.n_v;
+        const int st = j % STAGES, rb = j & 1;
         bool ok = mbar_wait(&sm.full[st], (j / STAGES) & 1);
         float *tile = sm.tile[st];
         float4 s[NP];
@@ -527,13 +595,28 @@ __device__ int consume(const StreamParams &p, StreamSmem &sm, int i0, int n_item
         *reinterpret_cast<float4 *>(red + r0 * D + c4 * 4) = acc;
         if (!bar_and(kBarCons, NC, ok)) {  // no consumer gives up on a wait alone
             sm.failed = 1;
+            clean = false;
             break;
         }
-        if (t == kTma && j >= 1 && j - 1 + STAGES < n_items) {
-            // the stage of item j-1 is free once its bulk store has read it
-            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-            load_tile(sm, (j - 1) % STAGES, p, item - 1 + STAGES);
-            issued = j + STAGES;
+        if (t == kTma && j >= 1) {
+            // position j+2: its item, published for the producers, and its
+            // tile into the stage of item j-1 (free once its bulk store has
+            // read it)
+            const int pos = j - 1 + STAGES;
+            int nxt = -1;
+            if (pos < n_s)
+                nxt = i0 + pos;
+            else if (grab >= 0 && grab < p.pool_n)
+                nxt = p.pool_base + grab;
+            sm.qitem[(pos - 3) & 3] = nxt;
+            mbar_arrive(&sm.qfull[(pos - 3) & 3]);
+            if (nxt >= 0) {
+                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                load_tile(sm, (j - 1) % STAGES, p, nxt);
+                issued = pos + 1;
+            }
+            // ask the pool for position pos+1 now; the answer is read an item later
+            grab = (p.pool != nullptr && nxt >= 0 && pos + 1 >= n_s) ? atomicAdd(p.pool, 1) : -1;
         }
         if (t < D) {
             // delta against the decayed state
@@ -587,12 +670,8 @@ __device__ int consume(const StreamParams &p, StreamSmem &sm, int i0, int n_item
         if (lane == 0) mbar_arrive(&sm.rec_empty[rb]);
         b_prev = b;
         h_prev = h;
-        if (++h == p.n_v) {
-            h = 0;
-            ++b;
-        }
     }
-    if (j == n_items) {  // (uniform) the last item's norm
+    if (clean) {  // (uniform) the last item's norm
         bar_sync(kBarCons, NC);
         if (t >= D && t < 2 * D) store_norm(p, sm, sm.o_prev[t - D], sm.zw_prev[t - D], b_prev, h_prev, t - D);
     }
@@ -605,11 +684,18 @@ __global__ void __launch_bounds__(NT, 1) dn_core_stream_kernel(const StreamParam
     StreamSmem &sm = *reinterpret_cast<StreamSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    const int i0 = (int)(((unsigned)blockIdx.x * (unsigned)p.items) / gridDim.x);
-    const int i1 = (int)(((unsigned)(blockIdx.x + 1) * (unsigned)p.items) / gridDim.x);
-    const int n_items = i1 - i0;  // >= 1: the grid has at most one CTA per item
+    // the CTA's own range [i0, i0 + n_s): n_s >= 1 (the grid has at most one
+    // CTA per item; with a pool, n_s >= 4)
+    int i0, n_s;
+    if (p.pool != nullptr) {
+        i0 = (int)blockIdx.x * p.n_static;
+        n_s = p.n_static;
+    } else {
+        i0 = (int)(((unsigned)blockIdx.x * (unsigned)p.items) / gridDim.x);
+        n_s = (int)(((unsigned)(blockIdx.x + 1) * (unsigned)p.items) / gridDim.x) - i0;
+    }
     const int b0 = i0 / p.n_v;
-    const int nseq = (i1 - 1) / p.n_v - b0 + 1;
+    const int nseq = (i0 + n_s - 1) / p.n_v - b0 + 1;
 
     if (t == 0) {
         for (int s = 0; s < STAGES; ++s)
@@ -619,10 +705,12 @@ __global__ void __launch_bounds__(NT, 1) dn_core_stream_kernel(const StreamParam
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&sm.rec_empty[r])),
                          "r"(NC / 32));
         }
+        for (int q = 0; q < 4; ++q)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&sm.qfull[q])));
         sm.failed = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         // the state is not written by the in_proj kernel
-        for (int j = 0; j < STAGES && j < n_items; ++j) load_tile(sm, j, p, i0 + j);
+        for (int j = 0; j < STAGES && j < n_s; ++j) load_tile(sm, j, p, i0 + j);
     }
     // the norm weights and the sequences' ring positions (advanced by the
     // previous step's last kernel, which has completed)
@@ -632,13 +720,16 @@ __global__ void __launch_bounds__(NT, 1) dn_core_stream_kernel(const StreamParam
 
     int issued = 0;
     if (warp < NC / 32) {
-        pdl_wait();  // (consumers read nothing the in_proj writes; the wait keeps completion transitive)
+        // (consumers read nothing the in_proj writes; the wait keeps
+        // completion transitive, and the pool counter, zeroed by the previous
+        // step's last kernel, is only asked after it)
+        pdl_wait();
         if (t == 0) pdl_trigger();
-        issued = consume(p, sm, i0, n_items, b0, t);
+        issued = consume(p, sm, i0, n_s, t);
     } else if (warp < NC / 32 + 3) {
-        produce<KC>(p, sm, i0, n_items, b0, warp - NC / 32, lane);
+        produce<KC>(p, sm, i0, n_s, b0, nseq, warp - NC / 32, lane);
     } else {
-        produce_z_gates<KC>(p, sm, i0, n_items, b0, lane);
+        produce_z_gates<KC>(p, sm, i0, n_s, lane);
     }
     __syncthreads();
     if (t == kTma) {
@@ -715,6 +806,15 @@ cudaError_t launch_dn_core_stream(const Dims &d, const LayerDev &L, int B, const
     p.dev_gates = d.dev_gates;
     p.in_rows = d.in_rows;
     p.gate_A = L.gate_A;
+    const int grid = std::min(num_sms(), p.items);
+    p.pool = nullptr;
+    p.n_static = p.pool_base = p.pool_n = 0;
+    if (L.pool != nullptr && p.items / grid >= kPoolPerCta + 4) {
+        p.pool = L.pool;
+        p.n_static = p.items / grid - kPoolPerCta;
+        p.pool_base = grid * p.n_static;
+        p.pool_n = p.items - p.pool_base;
+    }
     switch (d.conv_k) {
         case 2: return launch_kc<2>(p, st);
         case 3: return launch_kc<3>(p, st);

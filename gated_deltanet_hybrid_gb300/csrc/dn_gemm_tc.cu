@@ -571,9 +571,11 @@ __global__ void pack_b_kernel(const float *__restrict__ x, uint8_t *__restrict__
 __global__ void splitk_reduce_kernel(const float *__restrict__ part, const int *__restrict__ nseg_tab,
                                      const float *__restrict__ s, float *__restrict__ y,
                                      SchedView sv, int M, int B, int32_t *__restrict__ rpos,
-                                     int conv_k, int T, int Sr, int t0, int adv) {
+                                     int conv_k, int T, int Sr, int t0, int adv, int *__restrict__ pool_reset) {
     pdl_trigger();  // the next step's first kernels may be launched already
     pdl_wait();
+    // the state kernel's item pool, for the next step (that kernel has completed)
+    if (pool_reset != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *pool_reset = 0;
     if (rpos != nullptr && blockIdx.x == 0 && blockIdx.y == 0) {
         for (int b = threadIdx.x; b < B / T; b += blockDim.x) {
             int2 q = reinterpret_cast<int2 *>(rpos)[b];
@@ -680,7 +682,7 @@ cudaError_t launch_gemm_i8_tc(const uint8_t *Wt, const uint8_t *xb, float *part,
 
 cudaError_t launch_splitk_reduce(const float *part, const int *nseg, const float *s, float *y, int M,
                                  int K, int B, int32_t *rpos_advance, int conv_k, cudaStream_t st, int T,
-                                 int Sr, int t0, int adv) {
+                                 int Sr, int t0, int adv, int *pool_reset) {
     const GemmPlan g = plan_tc_gemm(M, K, B);
     const SchedView sv{g.U, g.G, g.UT, g.MT, g.max_seg};
     cudaLaunchConfig_t cfg = {};
@@ -690,7 +692,7 @@ cudaError_t launch_splitk_reduce(const float *part, const int *nseg, const float
     PdlAttr pdl;
     pdl.apply(cfg);
     return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, part, nseg, s, y, sv, M, B, rpos_advance,
-                              conv_k, T, Sr, t0, adv);
+                              conv_k, T, Sr, t0, adv, pool_reset);
 }
 
 }  // namespace dn

@@ -56,6 +56,7 @@ struct LayerDev {
     uint8_t *xb_in;        // packed B-operand tiles of x   [chunks][KT_in][16 KB]
     uint8_t *xb_out;       // packed B-operand tiles of the gated-norm output [chunks][KT_out][16 KB]
     int *err;              // device-side error word (bounded waits that gave up)
+    int *pool;             // the state kernel's item-pool counter (zero between steps)
 };
 
 // Prompt processing (dn_prefill) works on blocks of up to kPrefillCols token
@@ -142,7 +143,7 @@ cudaError_t launch_gemm_i8_tc(const uint8_t *Wt, const uint8_t *xb, float *part,
 // defaults, row j, one step).
 cudaError_t launch_splitk_reduce(const float *part, const int *nseg, const float *s, float *y, int M,
                                  int K, int B, int32_t *rpos_advance, int conv_k, cudaStream_t st, int T = 1,
-                                 int Sr = 1, int t0 = 0, int adv = 1);
+                                 int Sr = 1, int t0 = 0, int adv = 1, int *pool_reset = nullptr);
 constexpr size_t kOpTile = 16384;  // bytes of one packed B-operand tile (64 seqs x 64 k, hi+lo)
 // Byte offset, inside a packed B-operand tile (128 operand rows x 64 bf16;
 // row 2b = hi, row 2b+1 = lo of sequence b), of the 16-byte chunk holding
