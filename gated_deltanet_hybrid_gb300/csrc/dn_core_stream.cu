@@ -42,7 +42,9 @@
 //  * the first three state tiles, the ring positions and the norm weights
 //    are requested before the kernel waits for the in_proj kernel
 //    (programmatic dependent launch): the in_proj writes only the partials
-//    and segment counts.
+//    and segment counts.  In pool mode the CTAs that start beside the
+//    tensor-core in_proj (on the SMs it leaves free) also pull the first two
+//    tiles of every other CTA into L2 while they wait (warm_l2).
 //
 // Every mbarrier wait is bounded (about one second of the global timer); on
 // timeout the kernel records an error in `err`, leaves its loop (the
@@ -79,6 +81,9 @@ constexpr int kMaxSeqCta = 64;       // sequences one CTA's item range may touch
 // pool items per CTA: with at least kPoolPerCta + 4 items per CTA, each CTA's
 // own range is that many items shorter than an even share
 constexpr int kPoolPerCta = 3;
+// the first tiles of each CTA that starts after the in_proj, which the CTAs
+// that start beside it pull into L2 (pool mode)
+constexpr int kWarmTiles = 2;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 // named barriers (0 is __syncthreads)
 constexpr int kBarCons = 1;          // the 512 consumer threads
@@ -110,6 +115,7 @@ struct StreamParams {
     // pool_base + k for the k the counter hands it, while k < pool_n
     int *pool;
     int n_static, pool_base, pool_n;
+    int pf_ctas;  // CTAs 0 .. pf_ctas-1 start beside the in_proj and warm L2 (0: none)
 };
 
 struct __align__(128) StreamSmem {
@@ -678,6 +684,24 @@ __device__ int consume(const StreamParams &p, StreamSmem &sm, int i0, int n_s, i
     return issued;
 }
 
+// Warm-up of L2 by the first pf_ctas CTAs.  The tensor-core in_proj leaves
+// those SMs free, so these CTAs start while it runs, with nothing to do until
+// it completes; the other CTAs start only as the in_proj's CTAs leave, a few
+// microseconds before its end, and their first tile copies would come from
+// HBM late.  So these CTAs pull the first kWarmTiles tiles of every other
+// CTA into L2 (one prefetch per 128-byte line; the tiles of position 0 of all
+// CTAs first).
+__device__ void warm_l2(const StreamParams &p, int t) {
+    const int G = gridDim.x, E = p.pf_ctas, late = G - E;
+    for (int L = blockIdx.x; L < late * kWarmTiles; L += E) {
+        const int pos = L / late, c = E + L % late;
+        if (pos >= p.n_static) continue;
+        const char *tile = reinterpret_cast<const char *>(p.S + (size_t)(c * p.n_static + pos) * (D * D));
+        for (int off = t * 128; off < (int)kTileBytes; off += NT * 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(tile + off));
+    }
+}
+
 template <int KC>
 __global__ void __launch_bounds__(NT, 1) dn_core_stream_kernel(const StreamParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -718,6 +742,7 @@ __global__ void __launch_bounds__(NT, 1) dn_core_stream_kernel(const StreamParam
     for (int i = t; i < nseq; i += NT) sm.dpos[i] = p.rpos[2 * (b0 + i)];
     __syncthreads();
 
+    if ((int)blockIdx.x < p.pf_ctas) warm_l2(p, t);
     int issued = 0;
     if (warp < NC / 32) {
         // (consumers read nothing the in_proj writes; the wait keeps
@@ -808,12 +833,14 @@ cudaError_t launch_dn_core_stream(const Dims &d, const LayerDev &L, int B, const
     p.gate_A = L.gate_A;
     const int grid = std::min(num_sms(), p.items);
     p.pool = nullptr;
-    p.n_static = p.pool_base = p.pool_n = 0;
+    p.n_static = p.pool_base = p.pool_n = p.pf_ctas = 0;
     if (L.pool != nullptr && p.items / grid >= kPoolPerCta + 4) {
         p.pool = L.pool;
         p.n_static = p.items / grid - kPoolPerCta;
         p.pool_base = grid * p.n_static;
         p.pool_n = p.items - p.pool_base;
+        // the SMs the tensor-core in_proj leaves free host the first CTAs
+        if (tc && grid == num_sms() && gp.G < grid) p.pf_ctas = grid - gp.G;
     }
     switch (d.conv_k) {
         case 2: return launch_kc<2>(p, st);
