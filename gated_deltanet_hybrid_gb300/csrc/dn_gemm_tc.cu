@@ -72,7 +72,15 @@ using dev::global_ns;
 using dev::mbar_arrive;
 using dev::mbar_arrive_expect_tx;
 using dev::mbar_init;
+using dev::instr_desc;
+using dev::mma_bf16_ts_x4;
+using dev::mma_commit;
+using dev::smem_desc_sw128;
 using dev::smem_u32;
+using dev::tc_fence_after;
+using dev::tc_fence_before;
+using dev::tmem_ld16;
+using dev::tmem_st32;
 
 constexpr int BM = 128;          // weight rows per tile (MMA M)
 constexpr int BK = 64;           // k per weight tile
@@ -152,95 +160,6 @@ __device__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_fl
             if (global_ns() - t0 > kWaitLimitNs) return false;
         }
     }
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor for the 128-byte swizzled K-major layout
-// (bits 46..48 hold the descriptor format's fixed value 0b001): rows of 64 bf16
-// (128 bytes) stored contiguously, 8-row groups 1024 bytes apart, and within
-// each 1024-byte group the 16-byte chunk c of row r stored at chunk position
-// c ^ (r & 7).  The leading offset is unused in this mode; a K step of 16
-// elements inside the 128-byte row is a 32-byte advance of the start address
-// (the hardware applies the XOR to the computed addresses), so groups must be
-// 1024-byte aligned.  Layout-type field (bits 61..63) = 2.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((addr >> 4) & 0x3FFFu);
-    d |= (uint64_t)1 << 16;
-    d |= (uint64_t)(1024u >> 4) << 32;
-    d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
-    return d;
-}
-
-// kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major,
-// N >> 3 at bits 17..22, M >> 4 at bits 24..28.
-__device__ __forceinline__ uint32_t instr_desc(int M, int N) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
-}
-
-// Four K steps of 16: D (tensor memory) (+)= A (tensor memory, lane = row,
-// 32-bit column = two consecutive k; 8 columns per step) x B (shared-memory
-// descriptor, 32 bytes further per step)^T.  The first step overwrites D
-// when `accumulate` is 0.  One asm block with precomputed operands: for
-// 128 x 128 x 16 steps the issuing thread's own instruction count, not the
-// tensor core, otherwise sets the pace.
-__device__ __forceinline__ void mma_bf16_ts_x4(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                               uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "setp.eq.b32 q, %4, %4;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %6, %3, q;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %3, q;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %10, %3, q;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(a_tmem + 8u), "l"(bdesc + 2u),
-        "r"(a_tmem + 16u), "l"(bdesc + 4u), "r"(a_tmem + 24u), "l"(bdesc + 6u)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint64_t *bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// 32 consecutive 32-bit columns of this thread's tensor-memory lane, then
-// wait until the stores are done
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t v[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
-        "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
-        "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-        : "memory");
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // 4 int8 -> 4 bf16, exact, without float conversions: 0x43 above the low

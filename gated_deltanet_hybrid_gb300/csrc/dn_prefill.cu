@@ -32,6 +32,7 @@
 #include <algorithm>
 #include <atomic>
 
+#include "dn_device.cuh"
 #include "dn_internal.cuh"
 #include "dn_sched.cuh"
 
@@ -193,6 +194,7 @@ struct RecParams {
     float *o;
     Geo geo;
     int n_v, n_qk, group, dv, gw;
+    int *err;  // set when a bounded wait gives up
 };
 
 template <int DK>
@@ -475,6 +477,341 @@ __global__ void __launch_bounds__(kThreads, 2) recur_chunk_kernel(const RecParam
     for (int i = 0; i < 4; ++i) *reinterpret_cast<float4 *>(Sh + (size_t)(r0 + 32 * i) * p.dv) = s[i];
 }
 
+// 5''. The chunked recurrence on the tensor cores (dk = dv = 128, one decay
+// per head): the algebra of 5', with the three dense products of a chunk
+// as tcgen05 MMAs (kind::f16, fp32 accumulation in tensor memory), each
+// operand split into bf16 hi + lo and every product taken as
+// hi*hi + hi*lo + lo*hi (about 2^-16 relative per term, far inside the
+// decode step's tolerance).  One CTA of 128 threads per (value head,
+// sequence); thread j owns value column j, which is tensor-memory lane j.
+// The state lives in tensor memory for the whole block, transposed (lane j,
+// column i holds S[i][j]), as the accumulator of the update.  Per chunk:
+//   1. the gates; the chunk's k^, q^ rows as B operand tiles (64 rows: k^
+//      tokens, then q^ tokens) and as the A operand [k^; q^] (lane = token
+//      row); S0^T as an A operand; the accumulator scaled to gamma_n S0;
+//   2. MMA: D1 = [k^; q^] k^^T (k.k and q.k), D2 = S0^T [k^; q^]^T
+//      (S0^T k_t and S0^T q_t in lane j);
+//   3. L, M from D1 with the decays; every thread solves the chunk's
+//      lower-triangular system for its column of u (tokens in order) and
+//      forms its column of the readouts;
+//   4. MMA: S^T += U^T (w k^)^T with w_t = exp(G_n - G_t): A = U^T (lane j),
+//      B = the chunk's weighted k^ as 128 rows of 32 tokens.
+// Tensor memory (512 columns, one CTA per SM):
+constexpr int kTcThreads = 128;
+constexpr uint32_t kTcCols = 512;
+constexpr uint32_t kColS = 0;       // S^T, fp32
+constexpr uint32_t kColAsHi = 128;  // S0^T as bf16 pairs (k = i), hi and lo
+constexpr uint32_t kColAsLo = 192;
+constexpr uint32_t kColAkqHi = 256; // [k^; q^] as bf16 pairs, lanes 0-63 (64-127 zero)
+constexpr uint32_t kColAkqLo = 320;
+constexpr uint32_t kColD2 = 384;    // 64 columns: S0^T k_t (t < 32), S0^T q_t (32 + t)
+constexpr uint32_t kColD1 = 448;    // 32 columns: k_r.k_s (lane r < 32), q_r.k_s (lane 32 + r)
+constexpr uint32_t kColAuHi = 480;  // U^T as bf16 pairs (k = token), hi and lo
+constexpr uint32_t kColAuLo = 496;
+
+struct __align__(1024) TcChunkSmem {
+    union {
+        struct {
+            // B operand tiles in the 128-byte swizzled K-major layout (op_chunk_offset)
+            uint8_t bkq[2][2][8192];  // [hi, lo][k half]: 64 rows (k^ tokens, q^ tokens) x 64 k
+            uint8_t bw[2][16384];     // [hi, lo]: 128 rows (key channel) x 32 tokens (the first 64 bytes)
+        };
+        float st[128 * 128];  // the state on its way in and out (bulk copies), [i][j]
+    };
+    float kf[kChunk][128];    // the chunk's k^ rows
+    float L[kChunk][kChunk + 1];
+    float M[kChunk][kChunk + 1];
+    float G[kChunk], gam[kChunk], wn[kChunk], beta[kChunk];
+    uint64_t mma_done, s_full;
+    uint32_t tmem_base;
+};
+
+// x0, x1 -> bf16 pairs hi = bf16(x), lo = bf16(x - hi) (x0 in the low halves)
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+
+// mbarrier phase wait, bounded (about one second of the global timer)
+__device__ bool tc_wait(uint64_t *bar, uint32_t parity) {
+    const uint64_t t0 = dev::global_ns();
+    for (uint32_t it = 0;; ++it) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred q;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, q;\n\t}"
+            : "=r"(done)
+            : "r"(dev::smem_u32(bar)), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if ((it & 63u) == 63u && dev::global_ns() - t0 > 1000000000ull) return false;
+    }
+}
+
+// the MMAs of a 3-pass product: D (+)= A x B^T over K = 128 (two 64-k
+// halves), A hi/lo in tensor memory, B hi/lo tiles 8 KB apart per k half
+__device__ __forceinline__ void mma3_k128(uint32_t d, uint32_t a_hi, uint32_t a_lo, const uint8_t *b_hi,
+                                          const uint8_t *b_lo, uint32_t idesc, bool accumulate) {
+    for (int pass = 0; pass < 3; ++pass) {
+        const uint32_t a = pass == 2 ? a_lo : a_hi;
+        const uint8_t *bt = pass == 1 ? b_lo : b_hi;
+        for (int kh = 0; kh < 2; ++kh)
+            dev::mma_bf16_ts_x4(d, a + 32u * kh, dev::smem_desc_sw128(dev::smem_u32(bt + 8192 * kh)), idesc,
+                                (accumulate || pass > 0 || kh > 0) ? 1u : 0u);
+    }
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) recur_tc_kernel(const RecParams p) {
+    constexpr int DK = 128;
+    extern __shared__ uint8_t tc_smem_raw[];
+    TcChunkSmem &cs = *reinterpret_cast<TcChunkSmem *>(
+        (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int hq = h / p.group, T = p.geo.T;
+    float *Sh = p.S + ((size_t)(p.geo.b0 + b) * p.n_v + h) * DK * DK;
+    const float *qb = p.qn + ((size_t)b * p.n_qk + hq) * T * DK;
+    const float *kb = p.kn + ((size_t)b * p.n_qk + hq) * T * DK;
+    const size_t hv = ((size_t)b * p.n_v + h) * T;
+
+    if (tid == 0) {
+        dev::mbar_init(&cs.mma_done, 1);
+        dev::mbar_init(&cs.s_full, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        // the head's state (64 KB) by one bulk copy
+        dev::mbar_arrive_expect_tx(&cs.s_full, DK * DK * 4);
+        dev::bulk_g2s(dev::smem_u32(cs.st), Sh, DK * DK * 4, &cs.s_full);
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         dev::smem_u32(&cs.tmem_base)),
+                     "r"(kTcCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    dev::tc_fence_before();
+    __syncthreads();
+    dev::tc_fence_after();
+    const uint32_t tbase = cs.tmem_base;
+    const uint32_t tm = tbase + ((uint32_t)(warp * 32) << 16);  // this warp's lane quarter
+
+    // the state into tensor memory, transposed (thread j takes column j)
+    bool ok = tc_wait(&cs.s_full, 0);
+    for (int i0 = 0; i0 < DK; i0 += 32) {
+        uint32_t r[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(cs.st[(i0 + i) * DK + tid]);
+        dev::tmem_st32(tm + kColS + i0, r);
+    }
+    if (warp >= 2) {  // rows 64-127 of [k^; q^]: zero for good
+        uint32_t z[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) z[i] = 0u;
+        for (uint32_t c = 0; c < 128; c += 32) dev::tmem_st32(tm + kColAkqHi + c, z);
+    }
+
+    uint32_t phase = 0;
+    ok = __syncthreads_and(ok) != 0;  // (and the staging area is free again)
+    for (int c0 = 0; c0 < T && ok; c0 += kChunk) {
+        const int n = min(kChunk, T - c0);
+        // 1. gates (tokens past n: no decay, no write)
+        if (warp == 0) {
+            float gv = lane < n ? p.gg[hv + c0 + lane] : 0.f;
+            const float bv = lane < n ? p.bb[hv + c0 + lane] : 0.f;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {  // inclusive prefix sum: G_t
+                const float y = __shfl_up_sync(0xffffffffu, gv, o);
+                if (lane >= o) gv += y;
+            }
+            const float gl = __shfl_sync(0xffffffffu, gv, n - 1);
+            cs.G[lane] = gv;
+            cs.gam[lane] = expf(gv);
+            cs.wn[lane] = expf(gl - gv);
+            cs.beta[lane] = bv;
+        }
+        float v[kChunk];  // column j of the chunk's v
+#pragma unroll
+        for (int t = 0; t < kChunk; ++t) v[t] = t < n ? p.vv[(hv + c0 + t) * p.dv + tid] : 0.f;
+        // k^, q^ rows: B tiles and fp32 k^ (64 rows x 16 eight-wide k chunks;
+        // every load issued before the first is used)
+        float4 xs[2 * 64 * 16 / kTcThreads];
+#pragma unroll
+        for (int m = 0; m < 64 * 16 / kTcThreads; ++m) {
+            const int it = tid + m * kTcThreads, row = it >> 4, kc = it & 15, t = row & 31;
+            xs[2 * m] = xs[2 * m + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t < n) {
+                const float *src = (row < 32 ? kb : qb) + (size_t)(c0 + t) * DK + kc * 8;
+                xs[2 * m] = *reinterpret_cast<const float4 *>(src);
+                xs[2 * m + 1] = *reinterpret_cast<const float4 *>(src + 4);
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < 64 * 16 / kTcThreads; ++m) {
+            const int it = tid + m * kTcThreads, row = it >> 4, kc = it & 15, t = row & 31;
+            const float4 x0 = xs[2 * m], x1 = xs[2 * m + 1];
+            if (row < 32) {
+                *reinterpret_cast<float4 *>(&cs.kf[t][kc * 8]) = x0;
+                *reinterpret_cast<float4 *>(&cs.kf[t][kc * 8 + 4]) = x1;
+            }
+            uint4 hi, lo;
+            split_bf16x2(x0.x, x0.y, hi.x, lo.x);
+            split_bf16x2(x0.z, x0.w, hi.y, lo.y);
+            split_bf16x2(x1.x, x1.y, hi.z, lo.z);
+            split_bf16x2(x1.z, x1.w, hi.w, lo.w);
+            const uint32_t off = op_chunk_offset(row, kc & 7);
+            *reinterpret_cast<uint4 *>(cs.bkq[0][kc >> 3] + off) = hi;
+            *reinterpret_cast<uint4 *>(cs.bkq[1][kc >> 3] + off) = lo;
+        }
+        // the A operand [k^; q^]: warp 0 the k^ tokens, warp 1 the q^ tokens
+        if (warp < 2) {
+            const float *src = (warp == 0 ? kb : qb) + (size_t)(c0 + lane) * DK;
+            for (int half = 0; half < 2; ++half) {
+                uint32_t hi[32], lo[32];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (lane < n) x = *reinterpret_cast<const float4 *>(src + half * 64 + 2 * e);
+                    split_bf16x2(x.x, x.y, hi[e], lo[e]);
+                    split_bf16x2(x.z, x.w, hi[e + 1], lo[e + 1]);
+                }
+                dev::tmem_st32(tm + kColAkqHi + 32u * half, hi);
+                dev::tmem_st32(tm + kColAkqLo + 32u * half, lo);
+            }
+        }
+        __syncthreads();
+        // S0^T as the A operand, and the accumulator scaled to gamma_n S0
+        {
+            const float gn = cs.gam[n - 1];
+            for (int i0 = 0; i0 < DK; i0 += 32) {
+                uint32_t r[32], hi[16], lo[16];
+                dev::tmem_ld32(tm + kColS + i0, r);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    split_bf16x2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]), hi[e], lo[e]);
+                dev::tmem_st16(tm + kColAsHi + i0 / 2, hi);
+                dev::tmem_st16(tm + kColAsLo + i0 / 2, lo);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(gn * __uint_as_float(r[e]));
+                dev::tmem_st32(tm + kColS + i0, r);
+            }
+        }
+        // 2. D1 and D2
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // B tiles -> the tensor core
+        dev::tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            dev::tc_fence_after();
+            mma3_k128(tbase + kColD1, tbase + kColAkqHi, tbase + kColAkqLo, cs.bkq[0][0], cs.bkq[1][0],
+                      dev::instr_desc(128, 32), false);
+            mma3_k128(tbase + kColD2, tbase + kColAsHi, tbase + kColAsLo, cs.bkq[0][0], cs.bkq[1][0],
+                      dev::instr_desc(128, 64), false);
+            dev::mma_commit(&cs.mma_done);
+        }
+        ok = tc_wait(&cs.mma_done, phase);
+        phase ^= 1u;
+        dev::tc_fence_after();
+        // 3. L, M (warps 0 and 1: lane = token), S0^T k_t and S0^T q_t (lane j)
+        if (warp < 2) {
+            uint32_t r[32];
+            dev::tmem_ld32(tm + kColD1, r);
+            const float gt = cs.G[lane];
+#pragma unroll
+            for (int s2 = 0; s2 < kChunk; ++s2) {
+                const float e = expf(gt - cs.G[s2]) * __uint_as_float(r[s2]);
+                if (warp == 0)
+                    cs.L[lane][s2] = s2 < lane ? e : 0.f;
+                else
+                    cs.M[lane][s2] = s2 <= lane ? e : 0.f;
+            }
+        }
+        uint32_t pk[32], pq[32];
+        dev::tmem_ld32(tm + kColD2, pk);
+        dev::tmem_ld32(tm + kColD2 + 32, pq);
+        __syncthreads();
+        float u[kChunk];
+#pragma unroll
+        for (int t = 0; t < kChunk; ++t) {
+            float acc = fmaf(-cs.gam[t], __uint_as_float(pk[t]), v[t]);
+#pragma unroll
+            for (int s2 = 0; s2 < t; ++s2) acc = fmaf(-cs.L[t][s2], u[s2], acc);
+            u[t] = cs.beta[t] * acc;
+        }
+#pragma unroll
+        for (int t = 0; t < kChunk; ++t) {
+            if (t < n) {
+                float o = cs.gam[t] * __uint_as_float(pq[t]);
+#pragma unroll
+                for (int s2 = 0; s2 <= t; ++s2) o = fmaf(cs.M[t][s2], u[s2], o);
+                p.o[(hv + c0 + t) * p.dv + tid] = o;
+            }
+        }
+        // 4. A = U^T (lane j), B = the weighted k^ (row i = this thread)
+        {
+            uint32_t hi[16], lo[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) split_bf16x2(u[2 * e], u[2 * e + 1], hi[e], lo[e]);
+            dev::tmem_st16(tm + kColAuHi, hi);
+            dev::tmem_st16(tm + kColAuLo, lo);
+#pragma unroll
+            for (int kc = 0; kc < 4; ++kc) {
+                uint32_t wh[4], wl[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int t0 = 8 * kc + 2 * e;
+                    split_bf16x2(cs.wn[t0] * cs.kf[t0][tid], cs.wn[t0 + 1] * cs.kf[t0 + 1][tid], wh[e], wl[e]);
+                }
+                const uint32_t off = op_chunk_offset(tid, kc);
+                *reinterpret_cast<uint4 *>(cs.bw[0] + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+                *reinterpret_cast<uint4 *>(cs.bw[1] + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+            }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        dev::tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            dev::tc_fence_after();
+            const uint32_t idesc = dev::instr_desc(128, 128);
+            for (int pass = 0; pass < 3; ++pass)
+                dev::mma_bf16_ts_x2(tbase + kColS, tbase + (pass == 2 ? kColAuLo : kColAuHi),
+                                    dev::smem_desc_sw128(dev::smem_u32(cs.bw[pass == 1 ? 1 : 0])), idesc, 1u);
+            dev::mma_commit(&cs.mma_done);
+        }
+        ok = tc_wait(&cs.mma_done, phase) && ok;
+        phase ^= 1u;
+        dev::tc_fence_after();
+        ok = __syncthreads_and(ok) != 0;
+    }
+    if (ok) {  // the state back, through the staging area and one bulk store
+        for (int i0 = 0; i0 < DK; i0 += 32) {
+            uint32_t r[32];
+            dev::tmem_ld32(tm + kColS + i0, r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) cs.st[(i0 + i) * DK + tid] = __uint_as_float(r[i]);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();
+        if (tid == 0) {
+            asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(Sh),
+                         "r"(dev::smem_u32(cs.st)), "r"(DK * DK * 4)
+                         : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        }
+    }
+    dev::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        dev::tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(kTcCols)
+                     : "memory");
+    }
+    if (tid == 0 && !ok) atomicOr(p.err, 1);
+}
+
 // 6. gated RMSNorm of every readout of the block: fp32 rows for the CUDA-core
 // out_proj, or bf16 hi/lo B-operand tiles (column j = operand rows 2j, 2j+1
 // of its 64-column chunk) for the tensor-core one.  grid (n_v, cols).
@@ -517,6 +854,23 @@ cudaError_t launch_recur_chunk(const RecParams &rp, int dv, int n_v, int nb, cud
     cfg.dynamicSmemBytes = sizeof(ChunkSmem);
     cfg.stream = st;
     return cudaLaunchKernelEx(&cfg, recur_chunk_kernel, rp);
+}
+
+cudaError_t launch_recur_tc(const RecParams &rp, int n_v, int nb, cudaStream_t st) {
+    // over half of an SM's shared memory: one CTA per SM, which then holds
+    // all of its tensor memory
+    const size_t smem = std::max<size_t>(sizeof(TcChunkSmem) + 1024, 116 * 1024);
+    static std::atomic<uint64_t> attr_done{0};
+    const cudaError_t e = once_per_device(attr_done, [&](int) {
+        return cudaFuncSetAttribute(recur_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    });
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)n_v, (unsigned)nb);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    return cudaLaunchKernelEx(&cfg, recur_tc_kernel, rp);
 }
 
 template <int DK>
@@ -625,7 +979,13 @@ cudaError_t launch_prefill_block(const Dims &d, const LayerDev &L, const Prefill
         rp.group = d.n_v / d.n_qk;
         rp.dv = d.dv;
         rp.gw = d.gw;
-        if (d.dk == 128 && d.gw == 1)  // one decay per head: the chunked form
+        rp.err = L.err;
+        // one decay per head: the chunked form; for 128 x 128 heads on the
+        // tensor cores (one CTA per head and sequence) when that gives every
+        // SM a CTA, else on the CUDA cores in 32-column slices
+        if (d.dk == 128 && d.dv == 128 && d.gw == 1 && d.n_v * blk.nb >= num_sms())
+            e = launch_recur_tc(rp, d.n_v, blk.nb, st);
+        else if (d.dk == 128 && d.gw == 1)
             e = launch_recur_chunk(rp, d.dv, d.n_v, blk.nb, st);
         else switch (d.dk) {
             case 32: e = launch_recur<32>(rp, d.dv, d.n_v, blk.nb, st); break;

@@ -22,27 +22,44 @@ def _assert_ok(w):
 def test_prefill_49_token_prompt_35b():
     """The 30-layer stack's prompt length (49 tokens) on the 35B-shape layer
     at batch 1: one block of 49 columns (tensor-core projections, the chunked
-    recurrence over a chunk of 32 tokens and one of 17)."""
+    recurrence on the CUDA cores over a chunk of 32 tokens and one of 17)."""
     wl = custom_workload("pf49", SHAPE_35B, batch=1, steps=49, seed=3)
     _assert_ok(run_prefill_parity(wl, 49, decode_after=3))
 
 
 def test_prefill_2048_token_prompt_batch8():
     """The long-prompt workload as one prompt: batch 8, 2048 tokens with
-    exp(g) in [0.9, 1] (64 blocks of 8 x 32 columns), sequences 0 and 7
-    recomputed by the oracle."""
+    exp(g) in [0.9, 1] (64 blocks of 8 x 32 columns; the chunked recurrence
+    on the tensor cores), sequences 0 and 7 recomputed by the oracle."""
     wl = WORKLOADS["long_prompt_b8"]
     _assert_ok(run_prefill_parity(wl, 2048, sample=np.array([0, 7])))
 
 
 @pytest.mark.parametrize("batch,n_tokens", [(1, 96), (2, 70)])
 def test_prefill_chunked_recurrence_random_state(batch, n_tokens):
-    """The chunked recurrence (128-dim heads, one decay per head) from a
+    """The chunked recurrence on the CUDA cores (128-dim heads, one decay per
+    head, fewer (value head, sequence) pairs than SMs) from a
     random initial state: whole chunks (96 = 3 x 32 tokens in one block) and
     a ragged last chunk (2 x 70 columns: 70 = 2 x 32 + 6 tokens)."""
     cfg = DNConfig(hidden=256, n_qk_heads=2, n_v_heads=4, dk=128, dv=128)
     wl = custom_workload("pfc", cfg, batch=batch, steps=n_tokens, seed=90 + n_tokens, init_std=0.05)
     _assert_ok(run_prefill_parity(wl, n_tokens, decode_after=2))
+
+
+@pytest.mark.parametrize("shape,batch,n_tokens", [("35b", 5, 70), ("small", 40, 13)])
+def test_prefill_tensor_core_recurrence_random_state(shape, batch, n_tokens):
+    """The chunked recurrence on the tensor cores (128-dim heads, one decay
+    per head, at least one (value head, sequence) CTA per SM) from a random
+    initial state.  35B shape at batch 5: blocks of 51 tokens, so a whole
+    chunk and a ragged one of 19, then a block of 19 tokens (sequences 0 and
+    4 recomputed by the oracle).  Four value heads at batch 40: blocks of 6,
+    6 and 1 tokens."""
+    if shape == "35b":
+        cfg, sample = SHAPE_35B, np.array([0, 4])
+    else:
+        cfg, sample = DNConfig(hidden=256, n_qk_heads=2, n_v_heads=4, dk=128, dv=128), np.array([0, 17, 39])
+    wl = custom_workload("pftc", cfg, batch=batch, steps=n_tokens, seed=700 + batch, init_std=0.05)
+    _assert_ok(run_prefill_parity(wl, n_tokens, sample=sample, decode_after=2))
 
 
 @pytest.mark.parametrize("batch,n_tokens", [(1, 1), (1, 7), (3, 100), (5, 60), (64, 9), (300, 2)])
