@@ -13,7 +13,10 @@
 //      (the first K-1 reach back into the ring), SiLU, the q/k L2 norms and
 //      the query scale, silu(z) and the gates (the caller's, or from the
 //      layer's a/b rows), written head-major and token-contiguous;
-//   4. one kernel moves the ring to the block's last K-1 inputs;
+//   4. one kernel moves the ring to the block's last K-1 inputs
+//      (for 128-wide heads and blocks of several sequences 2-4 are one
+//      kernel per (row tile, sequence), which reads each partial once and
+//      keeps the conv window in registers);
 //   5. the recurrence kernel: one block per (column slice, value head,
 //      sequence) holds its dk x DJ slice of the state in registers for all T
 //      tokens (read once and written once per block instead of once per
@@ -48,6 +51,8 @@ __device__ __forceinline__ float sigmoid_f(float b) { return 1.0f / (1.0f + expf
 struct Geo {
     int b0, nb, t0, T, S, cols;
 };
+
+constexpr int kChunk = 32;  // tokens per step of the chunked kernels
 
 // 1. xg[j] = x[(b0 + j / T) * S + t0 + j % T]
 __global__ void gather_rows_kernel(const float *__restrict__ x, float *__restrict__ xg, int hidden, Geo g) {
@@ -183,6 +188,186 @@ __global__ void ring_block_kernel(const float *__restrict__ xin, float *__restri
     }
 }
 
+// 2-4 fused, for 128-wide heads (one in_proj row tile = one head).  One CTA
+// of 128 threads per (row tile, sequence of the block); thread c takes row
+// 128 mt + c through the block's T tokens, 32 at a time: the in_proj output
+// (segment partials in slot order, times the row scale) and then, by the
+// row's kind,
+//   q, k rows:  conv over the ring's history and the block's inputs (the
+//               window in registers), SiLU, the L2 norm over the tile (a
+//               fixed-order sum through shared memory), the query scale;
+//   v rows:     conv, SiLU (and the v head's CTA copies the caller's gates);
+//   z rows:     SiLU;
+//   gate rows:  (device gates) -A softplus(a), sigmoid(b);
+// and at the end the conv rows' last K-1 inputs go into the ring, whose
+// position moves with the reduction at the block's end.  Each partial and
+// ring value is read once, and no scaled-row buffer goes through memory.
+struct TileParams {
+    const float *part;     // in_proj segment partials, their counts, the row scales
+    const int *nseg;
+    const float *s_in;
+    float *ring;
+    const int32_t *rpos;
+    const float *wconv_t;
+    const float *g, *beta;  // caller's gates (host gates)
+    const float *gate_A;    // [n_v] (device gates)
+    float *qn, *kn, *vv, *zs, *gg, *bb;
+    Geo geo;
+    int MT, max_seg, conv_ch, qk_dim, in_rows, proj_rows, n_qk, n_v, gw, dev_gates;
+    float l2_eps, q_scale;
+};
+
+constexpr int kTileSlots = 4;  // partial slots loaded ahead (2 to 5 segments per tile on the 35B shape)
+
+template <int K>
+__global__ void __launch_bounds__(128) prep_tile_kernel(const TileParams p) {
+    constexpr int D = 128;
+    __shared__ float red[D][kChunk + 1];
+    __shared__ float inv[kChunk];
+    const int mt = blockIdx.x, b = blockIdx.y, c = threadIdx.x;
+    const int row = mt * D + c, T = p.geo.T, sb = p.geo.b0 + b;
+    const bool active = row < p.proj_rows;
+    const bool conv = row < p.conv_ch;  // (q, k, v: uniform over the tile)
+    const bool isq = row < p.qk_dim, isk = !isq && row < 2 * p.qk_dim;
+    const float sc = active ? p.s_in[row] : 0.f;
+    float w[K], prev[K - 1];  // taps; the last K-1 inputs before the current 32 tokens
+    int dpos = 0;
+#pragma unroll
+    for (int m = 0; m < K; ++m) w[m] = 0.f;
+#pragma unroll
+    for (int m = 0; m < K - 1; ++m) prev[m] = 0.f;
+    if (conv) {
+        dpos = p.rpos[2 * sb];
+#pragma unroll
+        for (int m = 0; m < K; ++m) w[m] = p.wconv_t[(size_t)m * p.conv_ch + row];
+#pragma unroll
+        for (int m = 0; m < K - 1; ++m) {  // oldest first
+            int slot = dpos + m;
+            if (slot >= K) slot -= K;
+            prev[m] = p.ring[((size_t)sb * K + slot) * p.conv_ch + row];
+        }
+    }
+    for (int s0 = 0; s0 < T; s0 += kChunk) {
+        const int nt = min(kChunk, T - s0);
+        float x[kChunk], u[kChunk];
+        // the partials of 16 tokens at a time: the first kTileSlots slots of
+        // every token requested before any is summed (from clamped, always
+        // valid addresses: tokens past nt take the last column, slots past
+        // max_seg slot 0), the rest read on the spot
+#pragma unroll
+        for (int g0 = 0; g0 < kChunk; g0 += 16) {
+            float pv[16][kTileSlots];
+            int nsv[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int j = b * T + s0 + min(g0 + i, nt - 1);  // block column
+                const int tile = (j >> 6) * p.MT + mt;
+                nsv[i] = p.nseg[tile];
+                const float *pp = p.part + ((size_t)tile * p.max_seg * 64 + (j & 63)) * D + c;
+#pragma unroll
+                for (int k = 0; k < kTileSlots; ++k) pv[i][k] = __ldcg(pp + (size_t)(k < p.max_seg ? k : 0) * (64 * D));
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int tt = g0 + i;
+                float acc = 0.f;
+#pragma unroll
+                for (int k = 0; k < kTileSlots; ++k)
+                    if (k < nsv[i]) acc += pv[i][k];
+                if (nsv[i] > kTileSlots) {
+                    const int j = b * T + s0 + min(tt, nt - 1);
+                    const int tile = (j >> 6) * p.MT + mt;
+                    const float *pp = p.part + ((size_t)tile * p.max_seg * 64 + (j & 63)) * D + c;
+                    for (int k = kTileSlots; k < nsv[i]; ++k) acc += __ldcg(pp + (size_t)k * (64 * D));
+                }
+                x[tt] = (active && tt < nt) ? sc * acc : 0.f;
+            }
+        }
+        if (conv) {
+#pragma unroll
+            for (int tt = 0; tt < kChunk; ++tt) {
+                float a = 0.f;
+#pragma unroll
+                for (int m = 0; m < K; ++m) {  // tap m meets input tt - (K - 1) + m; tap K-1 the current one
+                    const int ti = tt - (K - 1) + m;
+                    a = fmaf(w[m], ti >= 0 ? x[ti] : prev[ti + K - 1], a);
+                }
+                u[tt] = silu_f(a);
+            }
+            // the window for the next tokens: the last K-1 of (prev ++ x[0, nt)),
+            // slid one input at a time (fixed register indices)
+#pragma unroll
+            for (int tt = 0; tt < kChunk; ++tt) {
+                if (tt < nt) {
+#pragma unroll
+                    for (int m = 0; m < K - 2; ++m) prev[m] = prev[m + 1];
+                    prev[K - 2] = x[tt];
+                }
+            }
+        }
+        if (isq || isk) {  // the head's L2 norm per token
+#pragma unroll
+            for (int tt = 0; tt < kChunk; ++tt) red[c][tt] = u[tt] * u[tt];
+            __syncthreads();
+            if (c < kChunk) {
+                float ss = 0.f;
+                for (int r = 0; r < D; ++r) ss += red[r][c];
+                inv[c] = (1.0f / sqrtf(ss + p.l2_eps)) * (isq ? p.q_scale : 1.0f);
+            }
+            __syncthreads();
+            const int hq = isq ? mt : mt - p.n_qk;
+            float *dst = (isq ? p.qn : p.kn) + (((size_t)b * p.n_qk + hq) * T + s0) * D + c;
+#pragma unroll
+            for (int tt = 0; tt < kChunk; ++tt)
+                if (tt < nt) dst[(size_t)tt * D] = u[tt] * inv[tt];
+            __syncthreads();  // red and inv are taken again for the next tokens
+        } else if (conv) {  // v
+            const int h = mt - 2 * p.n_qk;
+            float *dst = p.vv + (((size_t)b * p.n_v + h) * T + s0) * D + c;
+#pragma unroll
+            for (int tt = 0; tt < kChunk; ++tt)
+                if (tt < nt) dst[(size_t)tt * D] = u[tt];
+            if (!p.dev_gates) {  // the caller's gates of this head: (token, key channel) per thread
+                for (int idx = c; idx < nt * p.gw; idx += D) {
+                    const int tt = idx / p.gw, k = idx - tt * p.gw;
+                    const size_t tok = (size_t)sb * p.geo.S + p.geo.t0 + s0 + tt;  // the caller's row
+                    const size_t hv = ((size_t)b * p.n_v + h) * T + s0 + tt;
+                    p.gg[hv * p.gw + k] = p.g[(tok * p.n_v + h) * p.gw + k];
+                    if (k == 0) p.bb[hv] = p.beta[tok * p.n_v + h];
+                }
+            }
+        } else if (row < p.in_rows) {  // z
+            const int h = (row - p.conv_ch) / D;
+            float *dst = p.zs + (((size_t)b * p.n_v + h) * T + s0) * D + c;
+#pragma unroll
+            for (int tt = 0; tt < kChunk; ++tt)
+                if (tt < nt) dst[(size_t)tt * D] = silu_f(x[tt]);
+        } else if (active) {  // the a/b gate rows (device gates)
+            const int r = row - p.in_rows;
+            const bool is_a = r < p.n_v * p.gw;
+            const int h = is_a ? r / p.gw : r - p.n_v * p.gw, k = is_a ? r % p.gw : 0;
+#pragma unroll
+            for (int tt = 0; tt < kChunk; ++tt) {
+                if (tt < nt) {
+                    const size_t hv = ((size_t)b * p.n_v + h) * T + s0 + tt;
+                    if (is_a)
+                        p.gg[hv * p.gw + k] = -p.gate_A[h] * softplus_f(x[tt]);
+                    else
+                        p.bb[hv] = sigmoid_f(x[tt]);
+                }
+            }
+        }
+    }
+    if (conv) {  // the ring after the block: its last K-1 inputs, at the advanced slots
+        int slot = (dpos + T) % K;
+#pragma unroll
+        for (int m = 0; m < K - 1; ++m) {
+            p.ring[((size_t)sb * K + slot) * p.conv_ch + row] = prev[m];
+            if (++slot == K) slot = 0;
+        }
+    }
+}
+
 // 5. the recurrence over the block's T tokens for one column slice of one
 // value head of one sequence: the dk x 32 slice of the state lives in
 // registers (thread: rows r0 + 32 i, columns 4 c4 .. 4 c4 + 3).
@@ -310,7 +495,6 @@ __global__ void __launch_bounds__(kThreads, 2) recur_kernel(const RecParams p) {
 // from shared memory a few times per chunk
 // instead of reduced across the CTA at every token.  Exact algebra of the
 // token recurrence; the rounding differs from it (fp32 throughout).
-constexpr int kChunk = 32;
 constexpr int kKP = 128 + 4;  // padded k / q rows: four rows a warp reads fall in distinct banks
 
 struct ChunkSmem {
@@ -906,6 +1090,55 @@ cudaError_t launch_prefill_block(const Dims &d, const LayerDev &L, const Prefill
                            st, d.i4 != 0);
     }
     if (e != cudaSuccess) return e;
+    const GemmPlan gpi = plan_tc_gemm(d.proj_rows, plan_k(d, d.hidden, cols), cols);
+    if (d.dk == 128 && d.dv == 128 && d.conv_k <= 8 && gpi.MT * blk.nb >= num_sms()) {
+        // 2-4 in one kernel, when its (row tile, sequence) CTAs cover the SMs
+        // (one sequence's prompt has more parallelism in the three kernels)
+        const GemmPlan &gp = gpi;
+        TileParams tp;
+        tp.part = P.part_in;
+        tp.nseg = P.nseg_in;
+        tp.s_in = L.s_in;
+        tp.ring = L.ring;
+        tp.rpos = L.rpos;
+        tp.wconv_t = L.wconv_t;
+        tp.g = blk.g;
+        tp.beta = blk.beta;
+        tp.gate_A = L.gate_A;
+        tp.qn = P.qn;
+        tp.kn = P.kn;
+        tp.vv = P.vv;
+        tp.zs = P.zs;
+        tp.gg = P.gg;
+        tp.bb = P.bb;
+        tp.geo = g;
+        tp.MT = gp.MT;
+        tp.max_seg = gp.max_seg;
+        tp.conv_ch = d.conv_ch;
+        tp.qk_dim = d.qk_dim;
+        tp.in_rows = d.in_rows;
+        tp.proj_rows = d.proj_rows;
+        tp.n_qk = d.n_qk;
+        tp.n_v = d.n_v;
+        tp.gw = d.gw;
+        tp.dev_gates = d.dev_gates;
+        tp.l2_eps = d.l2_eps;
+        tp.q_scale = d.q_scale;
+        cudaLaunchConfig_t c = {};
+        c.gridDim = dim3((unsigned)gp.MT, (unsigned)blk.nb);
+        c.blockDim = dim3(128);
+        c.stream = st;
+        switch (d.conv_k) {
+            case 2: e = cudaLaunchKernelEx(&c, prep_tile_kernel<2>, tp); break;
+            case 3: e = cudaLaunchKernelEx(&c, prep_tile_kernel<3>, tp); break;
+            case 4: e = cudaLaunchKernelEx(&c, prep_tile_kernel<4>, tp); break;
+            case 5: e = cudaLaunchKernelEx(&c, prep_tile_kernel<5>, tp); break;
+            case 6: e = cudaLaunchKernelEx(&c, prep_tile_kernel<6>, tp); break;
+            case 7: e = cudaLaunchKernelEx(&c, prep_tile_kernel<7>, tp); break;
+            default: e = cudaLaunchKernelEx(&c, prep_tile_kernel<8>, tp); break;
+        }
+        if (e != cudaSuccess) return e;
+    } else {
     // 2. scaled rows
     {
         const GemmPlan gp = plan_tc_gemm(d.proj_rows, plan_k(d, d.hidden, cols), cols);
@@ -962,6 +1195,7 @@ cudaError_t launch_prefill_block(const Dims &d, const LayerDev &L, const Prefill
         if ((e = cudaLaunchKernelEx(&c, ring_block_kernel, (const float *)P.xin, L.ring, (const int32_t *)L.rpos, g,
                                     d.conv_k, d.conv_ch, d.proj_rows)) != cudaSuccess)
             return e;
+    }
     }
     // 5. the recurrence
     {

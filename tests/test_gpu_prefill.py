@@ -46,18 +46,27 @@ def test_prefill_chunked_recurrence_random_state(batch, n_tokens):
     _assert_ok(run_prefill_parity(wl, n_tokens, decode_after=2))
 
 
-@pytest.mark.parametrize("shape,batch,n_tokens", [("35b", 5, 70), ("small", 40, 13)])
-def test_prefill_tensor_core_recurrence_random_state(shape, batch, n_tokens):
-    """The chunked recurrence on the tensor cores (128-dim heads, one decay
-    per head, at least one (value head, sequence) CTA per SM) from a random
-    initial state.  35B shape at batch 5: blocks of 51 tokens, so a whole
-    chunk and a ragged one of 19, then a block of 19 tokens (sequences 0 and
-    4 recomputed by the oracle).  Four value heads at batch 40: blocks of 6,
-    6 and 1 tokens."""
+@pytest.mark.parametrize("shape,batch,n_tokens,gates", [
+    ("35b", 5, 70, {}),
+    ("small", 40, 13, {}),
+    ("small", 40, 13, {"device_gates": True}),
+    ("small", 40, 13, {"key_gate": True}),
+])
+def test_prefill_many_sequences_random_state(shape, batch, n_tokens, gates):
+    """Blocks of many sequences on 128-wide heads, from a random initial
+    state: the fused partial-sum / conv / norm / ring kernel (one CTA per
+    in_proj row tile and sequence) and, with one decay per head, the chunked
+    recurrence on the tensor cores.  35B shape at batch 5: blocks of 51
+    tokens, so a whole chunk and a ragged one of 19, then a block of 19
+    tokens (sequences 0 and 4 recomputed by the oracle).  Four value heads
+    at batch 40: blocks of 6, 6 and 1 tokens, with the caller's gates, gates
+    from the layer's a/b rows, and per-key-channel gates (whose recurrence
+    stays token-serial)."""
     if shape == "35b":
         cfg, sample = SHAPE_35B, np.array([0, 4])
     else:
-        cfg, sample = DNConfig(hidden=256, n_qk_heads=2, n_v_heads=4, dk=128, dv=128), np.array([0, 17, 39])
+        cfg = DNConfig(hidden=256, n_qk_heads=2, n_v_heads=4, dk=128, dv=128, **gates)
+        sample = np.array([0, 17, 39])
     wl = custom_workload("pftc", cfg, batch=batch, steps=n_tokens, seed=700 + batch, init_std=0.05)
     _assert_ok(run_prefill_parity(wl, n_tokens, sample=sample, decode_after=2))
 
