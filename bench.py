@@ -606,6 +606,28 @@ def bench_stack(cfg, batches, n_layers, steps, warmup, seed, use_graph, dist_ctx
     return res
 
 
+def prefill_blocks(B, S):
+    """(sequences, token columns) of each block dn_prefill cuts a prompt into:
+    up to 256 sequences at a time, 256 // sequences tokens per block."""
+    for b0 in range(0, B, 256):
+        nb = min(256, B - b0)
+        T = max(1, 256 // nb)
+        for t0 in range(0, S, T):
+            yield nb, nb * min(T, S - t0)
+
+
+def prefill_block_kernels(cfg, nb, cols, torch):
+    """Kernels dn_prefill launches for one block: gather, (pack +) in_proj,
+    steps 2-4 (one kernel for 128-wide heads when (in_proj row tiles x
+    sequences) covers the SMs, else row sums, conv/norms and ring), the
+    recurrence, the gated norm, the out_proj and its reduction."""
+    in_rows = 2 * cfg.n_qk_heads * cfg.dk + 2 * cfg.n_v_heads * cfg.dv
+    proj_rows = in_rows + (cfg.n_v_heads * cfg.gate_width + cfg.n_v_heads if cfg.device_gates else 0)
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    fused = cfg.dk == 128 and cfg.dv == 128 and cfg.conv_k <= 8 and -(-proj_rows // 128) * nb >= sms
+    return 1 + (2 if cols >= TC_MIN_COLS else 1) + (1 if fused else 3) + 4
+
+
 def bench_prefill(cfg, B, S, n_layers, seed, dist_ctx, torch, abi, init_std=0.0, repeats_min=3):
     """Prompts through dn_prefill: each timed region runs one prompt of S
     tokens for all B sequences on each of n_layers layer objects (distinct
@@ -635,14 +657,7 @@ def bench_prefill(cfg, B, S, n_layers, seed, dist_ctx, torch, abi, init_std=0.0,
                 run(i)
 
     ms_list, t0, t1 = timed_regions(region, n_layers, dist_ctx, torch, min_repeats=repeats_min, min_total_s=0.3)
-    # kernels per prompt: per block of up to 256 token columns, gather, (pack +)
-    # in_proj, row sums, prep, ring, recurrence, norm, out_proj, reduction
-    launches = 0
-    for b0 in range(0, B, 256):
-        nb = min(256, B - b0)
-        T = max(1, 256 // nb)
-        for t0 in range(0, S, T):
-            launches += 10 if nb * min(T, S - t0) >= TC_MIN_COLS else 9
+    launches = sum(prefill_block_kernels(cfg, nb, cols, torch) for nb, cols in prefill_blocks(B, S))
     del graph
     for h in layers:
         abi.dn_destroy(h)
@@ -815,6 +830,18 @@ def run_reference(args, dist_ctx):
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_prefill_only(args, torch, dist_ctx):
+    """One prompt shape through dn_prefill (the secondary prompt keys of the
+    default run, for any B and S)."""
+    from gated_deltanet_hybrid_gb300 import abi
+    B, S = (int(v) for v in args.prefill.split(","))
+    r = bench_prefill(SHAPE_35B, B, S, args.layers, 5, dist_ctx, torch, abi)
+    return {"metric": "prompt tokens/s", "value": B * S / (r["ms"] / 1e3), "unit": "tokens/s",
+            "ms_per_prompt": r["ms"], "batch": B, "prompt_tokens": S, "layers_rotated": args.layers,
+            "gpu_launches": r["launches"], "region": r["region"],
+            "api": "dn_prefill (one call per prompt), cuda graph"}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -830,6 +857,9 @@ def main(argv=None):
                     help="also measure the batch-1 workload")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill", metavar="B,S",
+                    help="only time prompts of S tokens for B sequences through dn_prefill "
+                         "(35B-shape layer) and print their line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -843,7 +873,10 @@ def main(argv=None):
             if not torch.cuda.is_available():
                 raise SystemExit("bench.py --impl ours needs a CUDA device")
             torch.cuda.set_device(dist_ctx.local_rank)
-            line = (run_stack if args.workload in STACK_SPECS else run_ours)(args, torch, dist_ctx)
+            if args.prefill:
+                line = run_prefill_only(args, torch, dist_ctx)
+            else:
+                line = (run_stack if args.workload in STACK_SPECS else run_ours)(args, torch, dist_ctx)
         if line is not None and dist_ctx.rank == 0:
             print(json.dumps(line), flush=True)
     finally:
