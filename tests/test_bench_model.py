@@ -40,3 +40,37 @@ def test_state_stage_dominates_at_batch_64():
     kb = bench.kernel_bytes(SHAPE_35B, 64)
     assert kb["dn_state"] == 281_166_336
     assert kb["dn_state"] / bench.step_bytes(SHAPE_35B, 64) > 0.9
+
+
+class _Torch152:
+    """Stands in for torch.cuda's device query: a GB300 has 152 SMs."""
+
+    class cuda:
+        @staticmethod
+        def current_device():
+            return 0
+
+        @staticmethod
+        def get_device_properties(_):
+            return type("Props", (), {"multi_processor_count": 152})()
+
+
+def test_prefill_blocks_and_kernel_counts():
+    """The prompt bench's launch claim: dn_prefill cuts a prompt into blocks
+    of up to 256 token columns (256 // B tokens for B sequences), and a block
+    launches gather, (pack +) in_proj, steps 2-4, the recurrence, the gated
+    norm, the out_proj and its reduction, where steps 2-4 are one kernel for
+    128-wide heads once (in_proj row tiles x sequences) covers the SMs."""
+    blocks = list(bench.prefill_blocks(8, 2048))
+    assert len(blocks) == 64 and set(blocks) == {(8, 256)}
+    assert list(bench.prefill_blocks(1, 49)) == [(1, 49)]
+    assert list(bench.prefill_blocks(3, 100)) == [(3, 255), (3, 45)]  # 85 + 15 tokens
+    assert list(bench.prefill_blocks(300, 2)) == [(256, 256), (256, 256), (44, 88)]  # 1 token per block
+    t = _Torch152
+    # 35B shape: 96 row tiles, so one sequence (96 CTAs) keeps the three kernels
+    assert bench.prefill_block_kernels(SHAPE_35B, 8, 256, t) == 1 + 2 + 1 + 4
+    assert bench.prefill_block_kernels(SHAPE_35B, 2, 256, t) == 1 + 2 + 1 + 4
+    assert bench.prefill_block_kernels(SHAPE_35B, 1, 49, t) == 1 + 2 + 3 + 4
+    assert bench.prefill_block_kernels(SHAPE_35B, 1, 1, t) == 1 + 1 + 3 + 4  # the GEMV, no pack
+    # 32-wide heads never fuse steps 2-4
+    assert bench.prefill_block_kernels(TINY, 256, 256, t) == 1 + 2 + 3 + 4
