@@ -212,7 +212,13 @@ int dn_step(dn_layer *layer, int batch, const float *x, const float *g, const fl
  * The prompt runs in blocks of up to 256 token columns (sequences x
  * tokens): per block the in_proj and the out_proj run once over all of its
  * columns (tensor cores from 2 columns), and each head's state stays on chip
- * for all of the block's tokens.  Device pointers only; the call enqueues on
+ * for all of the block's tokens.  With one decay per head (no
+ * DN_FLAG_KEY_GATE) and 128-wide keys the recurrence takes its chunked form
+ * (32-token chunks; on the tensor cores for 128 x 128 heads when the block
+ * holds a (head, sequence) pair per SM): the same algebra in another
+ * summation order, so the results equal those of the dn_step calls up to
+ * rounding (within the decode step's tolerance), not bit for bit.
+ * Device pointers only; the call enqueues on
  * `stream` (NULL: the layer's stream) and returns.  The first call on a layer
  * allocates its scratch (about 80 MB for the 35B shape; counted by
  * dn_device_bytes, freed by dn_destroy), so make it before any stream
