@@ -606,12 +606,16 @@ def bench_stack(cfg, batches, n_layers, steps, warmup, seed, use_graph, dist_ctx
     return res
 
 
+PREFILL_COLS = 512  # dn_prefill's block: token columns (sequences x tokens)
+
+
 def prefill_blocks(B, S):
     """(sequences, token columns) of each block dn_prefill cuts a prompt into:
-    up to 256 sequences at a time, 256 // sequences tokens per block."""
-    for b0 in range(0, B, 256):
-        nb = min(256, B - b0)
-        T = max(1, 256 // nb)
+    up to PREFILL_COLS sequences at a time, PREFILL_COLS // sequences tokens
+    per block."""
+    for b0 in range(0, B, PREFILL_COLS):
+        nb = min(PREFILL_COLS, B - b0)
+        T = max(1, PREFILL_COLS // nb)
         for t0 in range(0, S, T):
             yield nb, nb * min(T, S - t0)
 

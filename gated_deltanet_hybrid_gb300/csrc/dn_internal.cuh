@@ -62,7 +62,10 @@ struct LayerDev {
 // Prompt processing (dn_prefill) works on blocks of up to kPrefillCols token
 // columns: nb sequences x T tokens each, column j = sequence j / T, token
 // j % T of the block.  Its scratch is allocated on the first dn_prefill call.
-constexpr int kPrefillCols = 256;
+// (512 columns against 256: each head's state moves in and out of the
+// recurrence once per 64 tokens of an 8-sequence prompt instead of 32, and
+// half as many launches; 8 x 2048 tokens 1.94 -> 2.37 M tokens/s.)
+constexpr int kPrefillCols = 512;
 struct PrefillDev {
     float *xg;                 // [cols][hidden] the block's x rows
     uint8_t *xb_in;            // packed bf16 hi/lo tiles of xg (tensor-core in_proj)

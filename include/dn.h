@@ -209,7 +209,7 @@ int dn_step(dn_layer *layer, int batch, const float *x, const float *g, const fl
  *   g    [batch][n_tokens][n_v_heads](gw)   device (NULL with device gates)
  *   beta [batch][n_tokens][n_v_heads]       device (NULL with device gates)
  *   out  [batch][n_tokens][hidden]          device (written)
- * The prompt runs in blocks of up to 256 token columns (sequences x
+ * The prompt runs in blocks of up to 512 token columns (sequences x
  * tokens): per block the in_proj and the out_proj run once over all of its
  * columns (tensor cores from 2 columns), and each head's state stays on chip
  * for all of the block's tokens.  With one decay per head (no
@@ -220,7 +220,7 @@ int dn_step(dn_layer *layer, int batch, const float *x, const float *g, const fl
  * rounding (within the decode step's tolerance), not bit for bit.
  * Device pointers only; the call enqueues on
  * `stream` (NULL: the layer's stream) and returns.  The first call on a layer
- * allocates its scratch (about 80 MB for the 35B shape; counted by
+ * allocates its scratch (about 140 MB for the 35B shape; counted by
  * dn_device_bytes, freed by dn_destroy), so make it before any stream
  * capture.  Errors: DN_EINVAL (sizes, NULL or misaligned pointers, gates
  * against the layer's flags, another device current), DN_ENOMEM,

@@ -57,19 +57,19 @@ class _Torch152:
 
 def test_prefill_blocks_and_kernel_counts():
     """The prompt bench's launch claim: dn_prefill cuts a prompt into blocks
-    of up to 256 token columns (256 // B tokens for B sequences), and a block
+    of up to 512 token columns (512 // B tokens for B sequences), and a block
     launches gather, (pack +) in_proj, steps 2-4, the recurrence, the gated
     norm, the out_proj and its reduction, where steps 2-4 are one kernel for
     128-wide heads once (in_proj row tiles x sequences) covers the SMs."""
     blocks = list(bench.prefill_blocks(8, 2048))
-    assert len(blocks) == 64 and set(blocks) == {(8, 256)}
+    assert len(blocks) == 32 and set(blocks) == {(8, 512)}
     assert list(bench.prefill_blocks(1, 49)) == [(1, 49)]
-    assert list(bench.prefill_blocks(3, 100)) == [(3, 255), (3, 45)]  # 85 + 15 tokens
-    assert list(bench.prefill_blocks(300, 2)) == [(256, 256), (256, 256), (44, 88)]  # 1 token per block
+    assert list(bench.prefill_blocks(3, 200)) == [(3, 510), (3, 90)]  # 170 + 30 tokens
+    assert list(bench.prefill_blocks(600, 2)) == [(512, 512), (512, 512), (88, 176)]  # 1 token per block
     t = _Torch152
     # 35B shape: 96 row tiles, so one sequence (96 CTAs) keeps the three kernels
-    assert bench.prefill_block_kernels(SHAPE_35B, 8, 256, t) == 1 + 2 + 1 + 4
-    assert bench.prefill_block_kernels(SHAPE_35B, 2, 256, t) == 1 + 2 + 1 + 4
+    assert bench.prefill_block_kernels(SHAPE_35B, 8, 512, t) == 1 + 2 + 1 + 4
+    assert bench.prefill_block_kernels(SHAPE_35B, 2, 512, t) == 1 + 2 + 1 + 4
     assert bench.prefill_block_kernels(SHAPE_35B, 1, 49, t) == 1 + 2 + 3 + 4
     assert bench.prefill_block_kernels(SHAPE_35B, 1, 1, t) == 1 + 1 + 3 + 4  # the GEMV, no pack
     # 32-wide heads never fuse steps 2-4

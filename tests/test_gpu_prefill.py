@@ -29,7 +29,7 @@ def test_prefill_49_token_prompt_35b():
 
 def test_prefill_2048_token_prompt_batch8():
     """The long-prompt workload as one prompt: batch 8, 2048 tokens with
-    exp(g) in [0.9, 1] (64 blocks of 8 x 32 columns; the chunked recurrence
+    exp(g) in [0.9, 1] (32 blocks of 8 x 64 columns; the chunked recurrence
     on the tensor cores), sequences 0 and 7 recomputed by the oracle."""
     wl = WORKLOADS["long_prompt_b8"]
     _assert_ok(run_prefill_parity(wl, 2048, sample=np.array([0, 7])))
@@ -56,10 +56,10 @@ def test_prefill_many_sequences_random_state(shape, batch, n_tokens, gates):
     """Blocks of many sequences on 128-wide heads, from a random initial
     state: the fused partial-sum / conv / norm / ring kernel (one CTA per
     in_proj row tile and sequence) and, with one decay per head, the chunked
-    recurrence on the tensor cores.  35B shape at batch 5: blocks of 51
-    tokens, so a whole chunk and a ragged one of 19, then a block of 19
-    tokens (sequences 0 and 4 recomputed by the oracle).  Four value heads
-    at batch 40: blocks of 6, 6 and 1 tokens, with the caller's gates, gates
+    recurrence on the tensor cores.  35B shape at batch 5: one block of 70
+    tokens, two whole chunks and a ragged one of 6 (sequences 0 and 4
+    recomputed by the oracle).  Four value heads at batch 40: blocks of 12
+    and 1 tokens, with the caller's gates, gates
     from the layer's a/b rows, and per-key-channel gates (whose recurrence
     stays token-serial)."""
     if shape == "35b":
@@ -71,11 +71,11 @@ def test_prefill_many_sequences_random_state(shape, batch, n_tokens, gates):
     _assert_ok(run_prefill_parity(wl, n_tokens, sample=sample, decode_after=2))
 
 
-@pytest.mark.parametrize("batch,n_tokens", [(1, 1), (1, 7), (3, 100), (5, 60), (64, 9), (300, 2)])
+@pytest.mark.parametrize("batch,n_tokens", [(1, 1), (1, 7), (3, 200), (5, 60), (64, 9), (600, 2)])
 def test_prefill_tiny_blocks(batch, n_tokens):
     """Block shapes: one token (the CUDA-core projections), a few columns,
-    ragged last blocks (3 x 100 -> 85 + 15 tokens), 64 sequences, more than
-    256 sequences (two sequence groups); random initial state, so the first
+    ragged last blocks (3 x 200 -> 170 + 30 tokens), 64 sequences, more than
+    512 sequences (two sequence groups); random initial state, so the first
     tokens' convolution reads the ring."""
     wl = custom_workload("pft", TINY, batch=batch, steps=n_tokens, seed=40 + batch, init_std=0.1)
     sample = np.array(sorted({0, batch // 2, batch - 1}))
