@@ -23,8 +23,9 @@
 //      token) and walks them in order: decay, delta against the decayed
 //      state, write-back, readout over the updated state; the next token's
 //      inputs are loaded while the current one is computed (for 128-wide
-//      heads with one decay per head: the chunked form of the same
-//      recurrence, 5' below);
+//      keys with one decay per head: the chunked form of the same
+//      recurrence, 5' below; for 128 x 128 heads, when the block holds a
+//      (head, sequence) pair per SM, on the tensor cores, 5'' below);
 //   6. the gated RMSNorm of every readout, written as the out_proj's input;
 //   7. the out_proj over all columns, its reduction writing each token's row
 //      of the caller's output and advancing the ring positions by T.
