@@ -116,19 +116,34 @@ def load_peaks() -> tuple[float, str]:
         return 6800.0, "fallback"
 
 
-def kernel_source_hash() -> str:
+# the files each profiled kernel is built from: its translation unit, the
+# library headers it includes and the public header they include
+KERNEL_SOURCES = {
+    "dn_state": ("gated_deltanet_hybrid_gb300/csrc/dn_core_stream.cu", "gated_deltanet_hybrid_gb300/csrc/dn_device.cuh",
+                 "gated_deltanet_hybrid_gb300/csrc/dn_internal.cuh", "gated_deltanet_hybrid_gb300/csrc/dn_sched.cuh",
+                 "include/dn.h"),
+}
+
+
+def kernel_source_hash(kernel: str | None = None) -> str:
+    """sha256 (first 16 hex digits) of a profiled kernel's source files
+    (KERNEL_SOURCES), or of every .cu/.cuh file of the library."""
+    if kernel is None:
+        csrc = os.path.join("gated_deltanet_hybrid_gb300", "csrc")
+        files = sorted(os.path.join(csrc, f) for f in os.listdir(os.path.join(ROOT, csrc)) if f.endswith((".cu", ".cuh")))
+    else:
+        files = sorted(KERNEL_SOURCES[kernel])
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "gated_deltanet_hybrid_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + b"\0" + fh.read())
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(os.path.basename(f).encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel: str, workload: str) -> float | None:
     """DRAM bytes per launch from the committed ncu summary of this kernel
-    and workload, if it was taken from the current kernel sources."""
+    and workload, if it was taken from the kernel's current sources (the
+    summary's source_hash against kernel_source_hash(kernel))."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(path):
         return None
@@ -138,7 +153,7 @@ def ncu_traffic(kernel: str, workload: str) -> float | None:
             if ":" in line and line.strip().startswith(("- source_hash", "- dram_bytes_per_launch")):
                 k, v = line.strip()[2:].split(":", 1)
                 vals[k.strip()] = v.strip().strip("`")
-    if vals.get("source_hash") != kernel_source_hash():
+    if kernel not in KERNEL_SOURCES or vals.get("source_hash") != kernel_source_hash(kernel):
         return None
     try:
         return float(vals["dram_bytes_per_launch"])
